@@ -1,0 +1,161 @@
+"""ctypes binding of the C ABI declared in ``include/moe_layer.h``.
+
+Argument marshalling only: every step of the layer runs in the CUDA library.  The
+functions keep the C names and take raw integers for device pointers and streams.
+Loading fails loudly if the library has not been built; nothing here falls back to
+any other implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_layer.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe_layer.h")
+
+STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_BOUNDS", 7: "MOE_ERR_WORKSPACE",
+}
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_ALIGNMENT = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS, MOE_ERR_WORKSPACE = 4, 5, 6, 7
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        detail = ""
+        try:
+            d = lib().moe_last_error_detail()
+            detail = d.decode() if d else ""
+        except Exception:  # pragma: no cover - the library itself failed to load
+            pass
+        super().__init__(f"{where}: {STATUS.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+class MoeConfig(C.Structure):
+    _fields_ = [(n, C.c_int) for n in
+                ("hidden", "n_experts", "top_k", "inter", "shared_inter", "group_size", "bits", "max_tokens")]
+
+
+class MoeQMat(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("scales", C.c_void_p), ("biases", C.c_void_p)]
+
+
+class MoeWeights(C.Structure):
+    _fields_ = [("gate", MoeQMat), ("up", MoeQMat), ("down", MoeQMat),
+                ("sh_gate", MoeQMat), ("sh_up", MoeQMat), ("sh_down", MoeQMat),
+                ("router_w", C.c_void_p), ("router_bias", C.c_void_p), ("shared_gate_w", C.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run bit_expert_layer_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        P, I, S = C.c_void_p, C.c_int, C.c_int
+        L.moe_workspace_bytes.argtypes = [C.POINTER(MoeConfig)]
+        L.moe_workspace_bytes.restype = C.c_size_t
+        L.moe_layer_create.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights), P, C.c_size_t, C.POINTER(P)]
+        L.moe_layer_create.restype = S
+        L.moe_route.argtypes = [P, P, I, P, P, P, P, P, P]
+        L.moe_route.restype = S
+        L.moe_forward.argtypes = [P, P, I, P, P]
+        L.moe_forward.restype = S
+        L.moe_forward_residual.argtypes = [P, P, I, P, P]
+        L.moe_forward_residual.restype = S
+        L.moe_stack_forward.argtypes = [P, I, P, I, P]
+        L.moe_stack_forward.restype = S
+        L.moe_stack_forward_host.argtypes = [P, I, P, I, P, P]
+        L.moe_stack_forward_host.restype = S
+        L.moe_forward_launches.argtypes = [I]
+        L.moe_forward_launches.restype = I
+        L.moe_layer_get_error.argtypes = [P]
+        L.moe_layer_get_error.restype = S
+        L.moe_layer_destroy.argtypes = [P]
+        L.moe_layer_destroy.restype = None
+        L.moe_status_string.argtypes = [S]
+        L.moe_status_string.restype = C.c_char_p
+        L.moe_last_error_detail.argtypes = []
+        L.moe_last_error_detail.restype = C.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> int:
+    if status != MOE_OK:
+        raise MoEError(status, where)
+    return status
+
+
+# --- same names as the C entry points -------------------------------------------------
+
+def moe_workspace_bytes(cfg: MoeConfig) -> int:
+    return int(lib().moe_workspace_bytes(C.byref(cfg)))
+
+
+def moe_layer_create(cfg: MoeConfig, weights: MoeWeights, workspace: int, workspace_bytes: int) -> int:
+    h = C.c_void_p()
+    _check(lib().moe_layer_create(C.byref(cfg), C.byref(weights), C.c_void_p(workspace), workspace_bytes,
+                                  C.byref(h)), "moe_layer_create")
+    return h.value
+
+
+def moe_route(layer: int, x: int, T: int, topk_idx: int = 0, topk_w: int = 0, counts: int = 0,
+              offsets: int = 0, perm: int = 0, stream: int = 0) -> None:
+    _check(lib().moe_route(layer, x, T, topk_idx or None, topk_w or None, counts or None, offsets or None,
+                           perm or None, stream or None), "moe_route")
+
+
+def moe_forward(layer: int, x: int, T: int, out: int, stream: int = 0) -> None:
+    _check(lib().moe_forward(layer, x, T, out, stream or None), "moe_forward")
+
+
+def moe_forward_residual(layer: int, x: int, T: int, out: int, stream: int = 0) -> None:
+    _check(lib().moe_forward_residual(layer, x, T, out, stream or None), "moe_forward_residual")
+
+
+def _handles(layers):
+    arr = (C.c_void_p * len(layers))(*layers)
+    return arr
+
+
+def moe_stack_forward(layers, x_io: int, T: int, stream: int = 0) -> None:
+    arr = _handles(layers)
+    _check(lib().moe_stack_forward(C.cast(arr, C.c_void_p), len(layers), x_io, T, stream or None),
+           "moe_stack_forward")
+
+
+def moe_stack_forward_host(layers, x_host: int, T: int, out_host: int, stream: int = 0) -> None:
+    arr = _handles(layers)
+    _check(lib().moe_stack_forward_host(C.cast(arr, C.c_void_p), len(layers), x_host, T, out_host,
+                                        stream or None), "moe_stack_forward_host")
+
+
+def moe_forward_launches(T: int) -> int:
+    return int(lib().moe_forward_launches(T))
+
+
+def moe_layer_get_error(layer: int) -> int:
+    return int(lib().moe_layer_get_error(layer))
+
+
+def moe_layer_destroy(layer: int) -> None:
+    lib().moe_layer_destroy(layer)
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions declared in include/moe_layer.h."""
+    import re
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))

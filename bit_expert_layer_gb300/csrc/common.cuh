@@ -1,0 +1,276 @@
+// common.cuh -- sm_103a building blocks shared by the layer's kernels: mbarriers,
+// TMA tile loads, tcgen05 (TMEM allocation, MMA, commit, loads), the shared-memory
+// matrix descriptor for 128-byte-swizzled K-major bf16 tiles, bounded waits that
+// record a timeout instead of hanging, and the constants of the one layer shape.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ----------------------------------------------------------------- layer shape
+constexpr int HID = 2048;        // hidden size
+constexpr int NEXP = 256;        // routed experts
+constexpr int TOPK = 8;          // experts kept per token
+constexpr int INTER = 512;       // routed expert intermediate size
+constexpr int SH_INTER = 512;    // shared expert intermediate size
+constexpr int GROUP = 64;        // quantisation group along the input dim
+constexpr int SHARED_E = NEXP;   // the shared expert's index in the tile tables
+
+// ----------------------------------------------------------------- device error word
+enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_BOUNDS = 2u };
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
+
+// ----------------------------------------------------------------- kernel geometry
+// Router (prefill): 128 tokens per CTA, 256 experts + 16 shared-gate rows on N.
+constexpr int RT_BM = 128;
+constexpr int RT_STAGES = 4;
+constexpr int RT_A_BYTES = RT_BM * 64 * 2;          // 16 KB  x tile
+constexpr int RT_B_BYTES = NEXP * 64 * 2;           // 32 KB  router tile
+constexpr int RT_G_BYTES = 16 * 64 * 2;             //  2 KB  shared-gate tile (1 real row)
+constexpr int RT_STAGE_BYTES = RT_A_BYTES + RT_B_BYTES + RT_G_BYTES;
+constexpr int RT_SMEM = RT_STAGES * RT_STAGE_BYTES + 1024 + 3072;
+constexpr int RT_THREADS = 128;
+
+// Grouped expert GEMMs: 128 weight rows (M) x up to 256 tokens (N) per tile, K step 64
+// (= one quantisation group).
+constexpr int GX_BM = 128;
+constexpr int GX_BN = 256;
+constexpr int GX_XBOX = 32;                         // token rows per TMA box
+constexpr int GX_A_BYTES = GX_BM * 64 * 2;          // 16 KB dequantised tile
+constexpr int GX_X_BYTES = GX_BN * 64 * 2;          // 32 KB activation tile
+constexpr int GX_P_BYTES = GX_BM * 32;              //  4 KB packed 4-bit tile (8 words/row)
+// gate/up: two A tiles + X + two packed tiles per stage
+constexpr int GU_STAGES = 3;
+constexpr int GU_STAGE_BYTES = 2 * GX_A_BYTES + GX_X_BYTES + 2 * GX_P_BYTES;
+constexpr int GU_SMEM = GU_STAGES * GU_STAGE_BYTES + 1024 + 512;
+constexpr int GU_THREADS = 320;                     // producer, MMA, 8 dequant/epilogue warps
+constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
+// down: one A tile + X + one packed tile per stage; double-buffered accumulator
+constexpr int DN_STAGES = 4;
+constexpr int DN_STAGE_BYTES = GX_A_BYTES + GX_X_BYTES + GX_P_BYTES;
+constexpr int DN_SMEM = DN_STAGES * DN_STAGE_BYTES + 1024 + 512;
+constexpr int DN_THREADS = 320;                     // producer, MMA, 4 dequant, 4 epilogue warps
+constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
+
+// scatter: one CTA per router block of 128 tokens (1024 slots)
+constexpr int SC_THREADS = 256;
+
+// decode path (T <= 8)
+constexpr int DEC_MAX_T = 8;
+constexpr int DEC_MAX_ACTIVE = 8 * DEC_MAX_T + 1;
+
+// ----------------------------------------------------------------- small helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+
+// ----------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete.  Gives up after WAIT_LIMIT_NS
+// (or as soon as another thread of the CTA has given up, via *abort): records
+// ERRBIT_TIMEOUT in the device error word and returns false.  Never hangs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
+                                          volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      atomicOr(err, ERRBIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// 2-D tiled load into shared memory, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// ----------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one CTA.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive fp32 columns: thread i gets lane (base lane + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+}
+
+// Shared-memory matrix descriptor for a K-major bf16 tile stored with the 128-byte
+// swizzle: rows of 128 bytes (64 elements), 8-row atoms of 1024 bytes, atoms
+// contiguous.  The tile base must be 1024-byte aligned; advancing along K inside the
+// 128-byte row is done by adding the byte offset to the start address.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+  d |= static_cast<uint64_t>(1) << 16;                    // leading-dim offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride between 8-row atoms
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version for tcgen05
+  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ----------------------------------------------------------------- 4-bit dequant
+// One packed word holds codes q0..q7 (low nibble first).  Returns the eight weights
+// w = scale * q + bias as bf16, each rounded once (fma.rn.bf16x2 of the exact code),
+// stored in the order (q0,q4),(q1,q5),(q2,q6),(q3,q7): the same K interleave that the
+// activation tiles are written in.  `ms` = (scale, scale), `mb` = (bias, bias).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 ms, __nv_bfloat162 mb) {
+  const __nv_bfloat162 k128 = __halves2bfloat162(__ushort_as_bfloat16(0x4300), __ushort_as_bfloat16(0x4300));
+  uint32_t p[4];
+  p[0] = (w & 0x000F000Fu) | 0x43004300u;
+  p[1] = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+  p[2] = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+  p[3] = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+  uint4 o;
+  uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&p[i]);   // 128 + q, exact
+    v = __hsub2(v, k128);                                              // q, exact
+    __nv_bfloat162 r = __hfma2(v, ms, mb);                             // one rounding
+    op[i] = *reinterpret_cast<uint32_t*>(&r);
+  }
+  return o;
+}
+
+// Reorder eight consecutive bf16 (e0..e7 in four words) into the interleave above.
+__device__ __forceinline__ uint4 interleave8(uint4 v) {
+  uint4 o;
+  o.x = __byte_perm(v.x, v.z, 0x5410);   // e0, e4
+  o.y = __byte_perm(v.x, v.z, 0x7632);   // e1, e5
+  o.z = __byte_perm(v.y, v.w, 0x5410);   // e2, e6
+  o.w = __byte_perm(v.y, v.w, 0x7632);   // e3, e7
+  return o;
+}
+
+// Column position of feature f inside an interleaved row (inverse of the order above).
+__host__ __device__ __forceinline__ int ilv_pos(int f) {
+  const int i = f & 7;
+  return (f & ~7) | (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+}  // namespace moe

@@ -1,0 +1,117 @@
+// internal.h -- parameter blocks and launch entry points shared by the library's
+// translation units (host side).  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct RouteParams {
+  const __nv_bfloat16* x;
+  int T;
+  const float* router_bias;  // [256] or nullptr (staged by the kernel)
+  int* topk_idx;             // [T][8]
+  float* topk_w;             // [T][8]
+  int* hist;                 // [nblk][256] per-router-block expert histogram
+  int* row_dst;              // [9T] destination row of each permuted row (shared part written here)
+  float* row_w;              // [9T] weight of each permuted row (shared part written here)
+  unsigned int* err;
+};
+
+struct ScanParams {
+  const int* hist;    // [nblk][256]
+  int nblk;
+  int T;
+  int* base;          // [nblk][256] first permuted row of (block, expert)
+  int* counts;        // [257]: 256 experts + shared (= T)
+  int* offsets;       // [258]: exclusive scan; [256] = 8T, [257] = 9T
+  int* tiles_gu;      // [258]: prefix of gate/up tiles per expert (shared = 256), [257] = total
+  int* tiles_dn;      // [258]: same for the down GEMM
+};
+
+struct ScatterParams {
+  const int* topk_idx;
+  const float* topk_w;
+  const int* base;
+  int T;
+  int* row_dst;       // [9T] (routed part) == permutation of slot ids
+  float* row_w;       // [9T]
+  const __nv_bfloat16* x;
+  __nv_bfloat16* x_perm;   // [9T][2048], K-interleaved rows
+  int gather;
+  unsigned int* err;
+};
+
+struct GateUpParams {
+  const int* tiles;      // [258]
+  const int* offsets;    // [258]
+  const int* counts;     // [257]
+  const uint16_t* g_scales; const uint16_t* g_biases;    // [256][512][32]
+  const uint16_t* u_scales; const uint16_t* u_biases;
+  const uint16_t* sg_scales; const uint16_t* sg_biases;  // [512][32]
+  const uint16_t* su_scales; const uint16_t* su_biases;
+  __nv_bfloat16* h;      // [9T][512], K-interleaved columns
+  unsigned int* err;
+};
+
+struct DownParams {
+  const int* tiles;      // [258]
+  const int* offsets;
+  const int* counts;
+  const uint16_t* d_scales; const uint16_t* d_biases;    // [256][2048][8]
+  const uint16_t* sd_scales; const uint16_t* sd_biases;  // [2048][8]
+  const int* row_dst;
+  const float* row_w;
+  __nv_bfloat16* y;      // [9T][2048]
+  int T;
+  unsigned int* err;
+};
+
+struct DecodeParams {
+  const __nv_bfloat16* x;
+  int T;
+  const __nv_bfloat16* router_w;
+  const float* router_bias;
+  const __nv_bfloat16* shared_gate_w;
+  float* logits;         // [8][257]
+  unsigned int* counter;
+  int* topk_idx;         // [T][8]
+  float* topk_w;
+  int* counts;           // [257]
+  int* offsets;          // [258]
+  int* perm;             // [8T]
+  int* act_expert;       // [65]
+  float* act_w;          // [65][8]
+  int* n_active;
+  // expert weights (packed words / bf16 bits)
+  const uint32_t* gq; const uint16_t* gs; const uint16_t* gb;     // routed gate
+  const uint32_t* uq; const uint16_t* us; const uint16_t* ub;     // routed up
+  const uint32_t* dq; const uint16_t* ds; const uint16_t* db;     // routed down
+  const uint32_t* sgq; const uint16_t* sgs; const uint16_t* sgb;  // shared gate
+  const uint32_t* suq; const uint16_t* sus; const uint16_t* sub;  // shared up
+  const uint32_t* sdq; const uint16_t* sds; const uint16_t* sdb;  // shared down
+  __nv_bfloat16* hw;     // [65][8][512] weighted, K-interleaved
+  __nv_bfloat16* out;    // [T][2048]
+  int residual;
+  unsigned int* err;
+};
+
+// launchers (return the first launch error)
+cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const CUtensorMap& tm_gs,
+                                  const RouteParams& p, cudaStream_t s);
+cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
+cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s);
+cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
+                          const CUtensorMap& squ, const CUtensorMap& xperm, const GateUpParams& p, int grid,
+                          cudaStream_t s);
+cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
+                        const DownParams& p, int grid, cudaStream_t s);
+cudaError_t launch_combine(const __nv_bfloat16* y, const __nv_bfloat16* x, __nv_bfloat16* out, int T,
+                           int residual, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int route_only, cudaStream_t s);
+cudaError_t set_kernel_attributes();
+
+}  // namespace moe

@@ -1,0 +1,428 @@
+// moe_layer.cu -- the C ABI (include/moe_layer.h): load-time validation, workspace
+// carving, TMA descriptors and the launch sequences of the prefill and decode paths.
+//
+// Lily accepts exactly one model layout and refuses every other one when it loads
+// (aimanavo.com, "Why is Perplexity's local AI Lily faster than MLX", section "Only one
+// 4-bit checkpoint of a pinned revision runs"; news.mantis.guru, "Perplexity opened
+// Lily", section "Rust drives the model, Metal computes"): moe_layer_create does the
+// same for the layer's shape and quantisation, and for pointer alignment.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+#include "moe_layer.h"
+
+namespace moe {
+cudaError_t set_router_attributes();
+cudaError_t set_gemm_attributes();
+}  // namespace moe
+
+using namespace moe;
+
+struct moe_layer {
+  moe_config_t cfg;
+  moe_weights_t w;
+  uint8_t* ws;
+  size_t ws_bytes;
+  int num_sms;
+  // workspace segments
+  unsigned int* err;
+  unsigned int* dec_counter;
+  __nv_bfloat16* gs16;
+  int *hist, *base, *counts, *offsets, *tiles_gu, *tiles_dn;
+  int* topk_idx;
+  float* topk_w;
+  int* row_dst;
+  float* row_w;
+  __nv_bfloat16 *x_perm, *h, *y, *x_io;
+  float* dec_logits;
+  int* dec_act_expert;
+  float* dec_act_w;
+  int* dec_n_active;
+  __nv_bfloat16* dec_hw;
+  // TMA descriptors of the weights and of the workspace buffers
+  CUtensorMap tm_wr, tm_gs, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_xperm, tm_h;
+};
+
+namespace {
+
+thread_local char g_detail[256] = "";
+
+void set_detail(const char* what, cudaError_t e) {
+  snprintf(g_detail, sizeof g_detail, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int MAX_TOKENS = 65536;
+
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t bytes) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+// Lays out the workspace for max_tokens Tm; with L == nullptr only sizes it.
+size_t carve(int Tm, uint8_t* base, moe_layer* L) {
+  Carver c{base};
+  moe_layer tmp;
+  moe_layer* d = L ? L : &tmp;
+  const size_t nblk = (Tm + RT_BM - 1) / RT_BM;
+  const size_t rows = 9ull * Tm;
+  d->err = c.take<unsigned int>(256);
+  d->dec_counter = c.take<unsigned int>(256);
+  d->gs16 = c.take<__nv_bfloat16>(16ull * HID * 2);
+  d->hist = c.take<int>(nblk * NEXP * 4);
+  d->base = c.take<int>(nblk * NEXP * 4);
+  d->counts = c.take<int>((NEXP + 1) * 4);
+  d->offsets = c.take<int>((NEXP + 2) * 4);
+  d->tiles_gu = c.take<int>((NEXP + 2) * 4);
+  d->tiles_dn = c.take<int>((NEXP + 2) * 4);
+  d->topk_idx = c.take<int>(static_cast<size_t>(Tm) * TOPK * 4);
+  d->topk_w = c.take<float>(static_cast<size_t>(Tm) * TOPK * 4);
+  d->row_dst = c.take<int>(rows * 4);
+  d->row_w = c.take<float>(rows * 4);
+  d->x_perm = c.take<__nv_bfloat16>(rows * HID * 2);
+  d->h = c.take<__nv_bfloat16>(rows * INTER * 2);
+  d->y = c.take<__nv_bfloat16>(rows * HID * 2);
+  d->x_io = c.take<__nv_bfloat16>(static_cast<size_t>(Tm) * HID * 2);
+  d->dec_logits = c.take<float>(DEC_MAX_T * (NEXP + 1) * 4);
+  d->dec_act_expert = c.take<int>(DEC_MAX_ACTIVE * 4);
+  d->dec_act_w = c.take<float>(DEC_MAX_ACTIVE * DEC_MAX_T * 4);
+  d->dec_n_active = c.take<int>(4);
+  d->dec_hw = c.take<__nv_bfloat16>(static_cast<size_t>(DEC_MAX_ACTIVE) * DEC_MAX_T * INTER * 2);
+  return (c.off + 255) & ~size_t(255);
+}
+
+bool config_ok(const moe_config_t* c) {
+  return c->hidden == HID && c->n_experts == NEXP && c->top_k == TOPK && c->inter == INTER &&
+         c->shared_inter == SH_INTER && c->group_size == GROUP && c->bits == 4 && c->max_tokens >= 1 &&
+         c->max_tokens <= MAX_TOKENS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, cols, rows, cols * 2, 64, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_packed(CUtensorMap* m, const void* base, uint64_t words, uint64_t rows) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, words, rows, words * 4, 8, GX_BM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool qmat_ok(const moe_qmat_t& q, moe_status_t* st) {
+  if (!q.q || !q.scales || !q.biases) { *st = MOE_ERR_INVALID_ARG; return false; }
+  if (!aligned(q.q, 16) || !aligned(q.scales, 16) || !aligned(q.biases, 16)) { *st = MOE_ERR_ALIGNMENT; return false; }
+  return true;
+}
+
+bool ranges_overlap(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+moe_status_t cuda_fail(const char* what, cudaError_t e) {
+  set_detail(what, e);
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(call, what)                       \
+  do {                                            \
+    const cudaError_t e_ = (call);                \
+    if (e_ != cudaSuccess) return cuda_fail(what, e_); \
+  } while (0)
+
+moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaStream_t s) {
+  const int nblk = (T + RT_BM - 1) / RT_BM;
+  CUtensorMap tm_x;
+  if (!encode_bf16_rows(&tm_x, x, HID, T, RT_BM)) return MOE_ERR_CUDA;
+  RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist,
+                 L->row_dst, L->row_w, L->err};
+  MOE_TRY(launch_router_prefill(tm_x, L->tm_wr, L->tm_gs, rp, s), "router launch");
+  ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->tiles_gu, L->tiles_dn};
+  MOE_TRY(launch_scan(sp, s), "scan launch");
+  ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->row_w,
+                    static_cast<const __nv_bfloat16*>(x), L->x_perm, gather, L->err};
+  MOE_TRY(launch_scatter(scp, nblk, s), "scatter launch");
+  return MOE_OK;
+}
+
+DecodeParams decode_params(moe_layer* L, const void* x, int T, void* out, int residual) {
+  DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.T = T;
+  p.router_w = static_cast<const __nv_bfloat16*>(L->w.router_w);
+  p.router_bias = L->w.router_bias;
+  p.shared_gate_w = static_cast<const __nv_bfloat16*>(L->w.shared_gate_w);
+  p.logits = L->dec_logits;
+  p.counter = L->dec_counter;
+  p.topk_idx = L->topk_idx;
+  p.topk_w = L->topk_w;
+  p.counts = L->counts;
+  p.offsets = L->offsets;
+  p.perm = L->row_dst;
+  p.act_expert = L->dec_act_expert;
+  p.act_w = L->dec_act_w;
+  p.n_active = L->dec_n_active;
+  auto Q = [](const moe_qmat_t& m, const uint32_t*& q, const uint16_t*& sc, const uint16_t*& bi) {
+    q = static_cast<const uint32_t*>(m.q);
+    sc = static_cast<const uint16_t*>(m.scales);
+    bi = static_cast<const uint16_t*>(m.biases);
+  };
+  Q(L->w.gate, p.gq, p.gs, p.gb);
+  Q(L->w.up, p.uq, p.us, p.ub);
+  Q(L->w.down, p.dq, p.ds, p.db);
+  Q(L->w.sh_gate, p.sgq, p.sgs, p.sgb);
+  Q(L->w.sh_up, p.suq, p.sus, p.sub);
+  Q(L->w.sh_down, p.sdq, p.sds, p.sdb);
+  p.hw = L->dec_hw;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.residual = residual;
+  p.err = L->err;
+  return p;
+}
+
+moe_status_t forward_impl(moe_layer* L, const void* x, int T, void* out, int residual, cudaStream_t s) {
+  if (T <= DEC_MAX_T) {
+    const DecodeParams p = decode_params(L, x, T, out, residual);
+    MOE_TRY(launch_decode(p, 0, s), "decode launch");
+    return MOE_OK;
+  }
+  const moe_status_t st = route_prefill(L, x, T, 1, s);
+  if (st != MOE_OK) return st;
+  auto U16 = [](const void* p) { return static_cast<const uint16_t*>(p); };
+  const moe_weights_t& w = L->w;
+  GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
+                  U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
+                  U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
+                  L->h, L->err};
+  // upper bound of the tile count: every touched expert adds at most one partial token block
+  const long long tok_blocks = (8ll * T + GX_BN - 1) / GX_BN + (8ll * T < NEXP ? 8ll * T : NEXP) +
+                               (T + GX_BN - 1) / GX_BN;
+  const int grid_gu = static_cast<int>(tok_blocks * GU_MBLK < L->num_sms ? tok_blocks * GU_MBLK : L->num_sms);
+  const int grid_dn = static_cast<int>(tok_blocks * DN_MBLK < L->num_sms ? tok_blocks * DN_MBLK : L->num_sms);
+  MOE_TRY(launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_xperm, gp, grid_gu, s), "gate/up launch");
+  DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
+                U16(w.sh_down.scales), U16(w.sh_down.biases), L->row_dst, L->row_w, L->y, T, L->err};
+  MOE_TRY(launch_down(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_dn, s), "down launch");
+  MOE_TRY(launch_combine(L->y, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(out), T,
+                         residual, s),
+          "combine launch");
+  return MOE_OK;
+}
+
+moe_status_t check_call(moe_layer* L, const void* x, int T, const void* out) {
+  if (!L || !x || !out) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config_t* cfg) {
+  if (!cfg || !config_ok(cfg)) return 0;
+  return carve(cfg->max_tokens, nullptr, nullptr);
+}
+
+moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weights, void* workspace,
+                              size_t workspace_bytes, moe_layer_t** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !weights) return MOE_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = MOE_OK;
+  const moe_qmat_t* mats[6] = {&weights->gate, &weights->up, &weights->down,
+                               &weights->sh_gate, &weights->sh_up, &weights->sh_down};
+  for (const moe_qmat_t* m : mats)
+    if (!qmat_ok(*m, &st)) return st;
+  if (!weights->router_w || !weights->shared_gate_w || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(weights->router_w, 16) || !aligned(weights->shared_gate_w, 16) ||
+      (weights->router_bias && !aligned(weights->router_bias, 16)) || !aligned(workspace, 256))
+    return MOE_ERR_ALIGNMENT;
+  const size_t need = carve(cfg->max_tokens, nullptr, nullptr);
+  if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+
+  moe_layer* L = new (std::nothrow) moe_layer;
+  if (!L) return MOE_ERR_CUDA;
+  std::memset(L, 0, sizeof *L);
+  L->cfg = *cfg;
+  L->w = *weights;
+  L->ws = static_cast<uint8_t*>(workspace);
+  L->ws_bytes = workspace_bytes;
+  carve(cfg->max_tokens, L->ws, L);
+
+  auto fail = [&](moe_status_t s) { delete L; return s; };
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(cuda_fail("device query", e));
+  if (!get_encode()) {
+    snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled entry point unavailable");
+    return fail(MOE_ERR_CUDA);
+  }
+  if ((e = set_router_attributes()) != cudaSuccess || (e = set_gemm_attributes()) != cudaSuccess)
+    return fail(cuda_fail("kernel attributes", e));
+  // workspace constants: the error word, the decode ticket, the 16-row shared-gate tile
+  if ((e = cudaMemset(L->err, 0, 256)) != cudaSuccess || (e = cudaMemset(L->dec_counter, 0, 256)) != cudaSuccess ||
+      (e = cudaMemset(L->gs16, 0, 16ull * HID * 2)) != cudaSuccess ||
+      (e = cudaMemcpy(L->gs16, weights->shared_gate_w, HID * 2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+      (e = cudaDeviceSynchronize()) != cudaSuccess)
+    return fail(cuda_fail("workspace init", e));
+
+  const int Tm = cfg->max_tokens;
+  bool ok = encode_bf16_rows(&L->tm_wr, weights->router_w, HID, NEXP, NEXP) &&
+            encode_bf16_rows(&L->tm_gs, L->gs16, HID, 16, 16) &&
+            encode_packed(&L->tm_qg, weights->gate.q, HID / 8, static_cast<uint64_t>(NEXP) * INTER) &&
+            encode_packed(&L->tm_qu, weights->up.q, HID / 8, static_cast<uint64_t>(NEXP) * INTER) &&
+            encode_packed(&L->tm_sqg, weights->sh_gate.q, HID / 8, SH_INTER) &&
+            encode_packed(&L->tm_squ, weights->sh_up.q, HID / 8, SH_INTER) &&
+            encode_packed(&L->tm_qd, weights->down.q, INTER / 8, static_cast<uint64_t>(NEXP) * HID) &&
+            encode_packed(&L->tm_sqd, weights->sh_down.q, SH_INTER / 8, HID) &&
+            encode_bf16_rows(&L->tm_xperm, L->x_perm, HID, 9ull * Tm, GX_XBOX) &&
+            encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX);
+  if (!ok) return fail(MOE_ERR_CUDA);
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(moe_layer_t* L, const void* x, int T, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, moe_stream_t stream) {
+  if (!L || !x) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16)) return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T <= DEC_MAX_T) {
+    const DecodeParams p = decode_params(L, x, T, nullptr, 0);
+    MOE_TRY(launch_decode(p, 1, s), "decode router launch");
+  } else {
+    const moe_status_t st = route_prefill(L, x, T, 0, s);
+    if (st != MOE_OK) return st;
+  }
+  const size_t slots = static_cast<size_t>(T) * TOPK;
+  if (topk_idx) MOE_TRY(cudaMemcpyAsync(topk_idx, L->topk_idx, slots * 4, cudaMemcpyDeviceToDevice, s), "copy idx");
+  if (topk_w) MOE_TRY(cudaMemcpyAsync(topk_w, L->topk_w, slots * 4, cudaMemcpyDeviceToDevice, s), "copy w");
+  if (counts) MOE_TRY(cudaMemcpyAsync(counts, L->counts, NEXP * 4, cudaMemcpyDeviceToDevice, s), "copy counts");
+  if (offsets)
+    MOE_TRY(cudaMemcpyAsync(offsets, L->offsets, (NEXP + 1) * 4, cudaMemcpyDeviceToDevice, s), "copy offsets");
+  if (perm) MOE_TRY(cudaMemcpyAsync(perm, L->row_dst, slots * 4, cudaMemcpyDeviceToDevice, s), "copy perm");
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(moe_layer_t* L, const void* x, int T, void* out, moe_stream_t stream) {
+  const moe_status_t st = check_call(L, x, T, out);
+  if (st != MOE_OK) return st;
+  if (ranges_overlap(x, out, static_cast<size_t>(T) * HID * 2)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(L, x, T, out, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward_residual(moe_layer_t* L, const void* x, int T, void* out, moe_stream_t stream) {
+  const moe_status_t st = check_call(L, x, T, out);
+  if (st != MOE_OK) return st;
+  if (x != out && ranges_overlap(x, out, static_cast<size_t>(T) * HID * 2)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(L, x, T, out, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x_io, int T, moe_stream_t stream) {
+  if (!layers || n_layers < 1 || !x_io) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_status_t st = check_call(layers[l], x_io, T, x_io);
+    if (st != MOE_OK) return st;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_status_t st = forward_impl(layers[l], x_io, T, x_io, 1, reinterpret_cast<cudaStream_t>(stream));
+    if (st != MOE_OK) return st;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, const void* x_host, int T,
+                                    void* out_host, moe_stream_t stream) {
+  if (!layers || n_layers < 1 || !x_host || !out_host || !layers[0]) return MOE_ERR_INVALID_ARG;
+  moe_layer* L0 = layers[0];
+  if (T < 1 || T > L0->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(T) * HID * 2;
+  MOE_TRY(cudaMemcpyAsync(L0->x_io, x_host, bytes, cudaMemcpyHostToDevice, s), "copy in");
+  const moe_status_t st = moe_stack_forward(layers, n_layers, L0->x_io, T, stream);
+  if (st != MOE_OK) return st;
+  MOE_TRY(cudaMemcpyAsync(out_host, L0->x_io, bytes, cudaMemcpyDeviceToHost, s), "copy out");
+  return MOE_OK;
+}
+
+int moe_forward_launches(int T) { return T <= DEC_MAX_T ? 3 : 6; }
+
+moe_status_t moe_layer_get_error(moe_layer_t* L) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail("synchronize", e);
+  unsigned int v = 0;
+  if ((e = cudaMemcpy(&v, L->err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail("read error word", e);
+  if ((e = cudaMemset(L->err, 0, 4)) != cudaSuccess) return cuda_fail("clear error word", e);
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail("synchronize", e);
+  if (v & ERRBIT_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v & ERRBIT_BOUNDS) return MOE_ERR_DEVICE_BOUNDS;
+  return MOE_OK;
+}
+
+void moe_layer_destroy(moe_layer_t* L) { delete L; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported layer shape or quantisation";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+}  // extern "C"

@@ -1,0 +1,339 @@
+// router.cu -- on-device routing for the prefill path, with no host synchronisation
+// anywhere (Lily keeps mixture-of-experts routing on the GPU and drops the per-layer
+// CPU sync: aimanavo.com, "Why is Perplexity's local AI Lily faster than MLX",
+// section "Prefill and decode are not treated as the same job"; dzen.guru,
+// "Perplexity opened the Lily engine", section "Where the speed-up comes from").
+//
+//   router_prefill_kernel  logits = x W_r^T on tcgen05 (bf16 in, fp32 accumulate in
+//                          TMEM), plus the shared-expert gate g_s . x as 16 extra
+//                          N columns; per token: top-8 by logit with lowest-index
+//                          ties, weights exp(l_k - l_1) / sum (equal to softmax over
+//                          all 256 followed by renormalisation over the 8), the
+//                          shared gate sigmoid, and a per-CTA expert histogram.
+//   route_scan_kernel      per-expert counts, exclusive-scan offsets, the first
+//                          permuted row of every (router block, expert), and the
+//                          tile tables of both grouped GEMMs.
+//   route_scatter_kernel   stable permutation of the slots t*8+k into expert order,
+//                          the per-row weight, and the gather of x into x_perm
+//                          (8 routed copies + 1 shared copy per token).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(RT_THREADS, 1)
+    router_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wr,
+                          const __grid_constant__ CUtensorMap tm_gs, RouteParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RT_STAGES * RT_STAGE_BYTES);  // full[4] empty[4] done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  int* hist_s = reinterpret_cast<int*>(tmem_slot + 4);
+  float* bias_s = reinterpret_cast<float*>(hist_s + NEXP);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bias_s + NEXP);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.x * RT_BM;
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[4]), done = smem_u32(&bars[8]);
+
+  if (tid == 0) {
+    for (int s = 0; s < RT_STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < NEXP; i += RT_THREADS) {
+    hist_s[i] = 0;
+    bias_s[i] = p.router_bias ? p.router_bias[i] : 0.0f;
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr int NKB = HID / 64;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_wr);
+    tma_prefetch_desc(&tm_gs);
+    int issued = 0;
+    for (int kb = 0; kb < NKB; ++kb) {
+      const int s = kb % RT_STAGES;
+      const uint32_t ph = (kb / RT_STAGES) & 1;
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, abort_flag)) break;
+      uint8_t* st = smem + s * RT_STAGE_BYTES;
+      mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
+      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kb * 64, m0);
+      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kb * 64, 0);
+      tma_load_2d(smem_u32(st + RT_A_BYTES + RT_B_BYTES), &tm_gs, full0 + 8 * s, kb * 64, 0);
+      issued = kb + 1;
+    }
+    if (*abort_flag) {
+      // drain copies still in flight before the CTA's shared memory goes away
+      for (int kb = (issued > RT_STAGES ? issued - RT_STAGES : 0); kb < issued; ++kb) {
+        const int s = kb % RT_STAGES;
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(full0 + 8 * s, (kb / RT_STAGES) & 1) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    const uint32_t id_r = idesc_bf16(128, 256), id_g = idesc_bf16(128, 16);
+    for (int kb = 0; kb < NKB; ++kb) {
+      const int s = kb % RT_STAGES;
+      const uint32_t ph = (kb / RT_STAGES) & 1;
+      if (!mbar_wait(full0 + 8 * s, ph, p.err, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t a = smem_u32(smem + s * RT_STAGE_BYTES);
+      const uint32_t b = a + RT_A_BYTES, g = b + RT_B_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = sdesc_sw128(a + kk * 32);
+        const uint32_t acc = (kb | kk) != 0;
+        umma_bf16(tmem, ad, sdesc_sw128(b + kk * 32), id_r, acc);
+        umma_bf16(tmem + 256, ad, sdesc_sw128(g + kk * 32), id_g, acc);
+      }
+      umma_commit(empty0 + 8 * s);
+    }
+    umma_commit(done);   // also covers an early exit: all issued MMAs complete first
+  }
+  __syncwarp();
+
+  // ---- epilogue: thread = token row (TMEM lane), all four warps
+  bool ok = mbar_wait(done, 0, p.err, abort_flag);
+  ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
+  tc_fence_after();
+  const int t = m0 + tid;
+  if (ok) {
+    float tv[TOPK];
+    int ti[TOPK];
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) { tv[k] = -INFINITY; ti[k] = NEXP; }
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < NEXP / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(lane_base + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = c * 32 + j;
+        const float v = __uint_as_float(r[j]) + bias_s[e];
+        if (v > tv[TOPK - 1]) {          // strictly greater: equal logits keep the lower index
+          tv[TOPK - 1] = v;
+          ti[TOPK - 1] = e;
+#pragma unroll
+          for (int k = TOPK - 1; k > 0; --k) {
+            if (tv[k] > tv[k - 1]) {
+              const float fv = tv[k]; tv[k] = tv[k - 1]; tv[k - 1] = fv;
+              const int iv = ti[k]; ti[k] = ti[k - 1]; ti[k - 1] = iv;
+            }
+          }
+        }
+      }
+    }
+    uint32_t gr;
+    tmem_ld1(lane_base + 256, gr);
+    tmem_ld_wait();
+    if (t < p.T) {
+      float ex[TOPK], sum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) { ex[k] = expf(tv[k] - tv[0]); sum += ex[k]; }
+      const float inv = 1.0f / sum;
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) {
+        p.topk_idx[t * TOPK + k] = ti[k];
+        p.topk_w[t * TOPK + k] = ex[k] * inv;
+        atomicAdd(&hist_s[ti[k]], 1);
+      }
+      const float z = __uint_as_float(gr);
+      const float sg = 1.0f / (1.0f + expf(-z));
+      const int srow = 8 * p.T + t;
+      p.row_dst[srow] = srow;
+      p.row_w[srow] = sg;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  for (int i = tid; i < NEXP; i += RT_THREADS) p.hist[blockIdx.x * NEXP + i] = hist_s[i];
+  if (warp == 1) {
+    tc_fence_after();
+    if (lane == 0 && *abort_flag) {
+      // MMAs issued before an abort finish before their columns are released
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void __launch_bounds__(256) route_scan_kernel(ScanParams p) {
+  __shared__ int sc[NEXP];
+  __shared__ int s_tot[2];
+  const int e = threadIdx.x;
+  int c = 0;
+#pragma unroll 4
+  for (int b = 0; b < p.nblk; ++b) {
+    const int h = p.hist[b * NEXP + e];
+    p.base[b * NEXP + e] = c;
+    c += h;
+  }
+  // block-wide inclusive scan (Hillis-Steele) of the counts
+  sc[e] = c;
+  __syncthreads();
+  for (int off = 1; off < NEXP; off <<= 1) {
+    const int v = (e >= off) ? sc[e - off] : 0;
+    __syncthreads();
+    sc[e] += v;
+    __syncthreads();
+  }
+  const int excl = sc[e] - c;
+  for (int b = 0; b < p.nblk; ++b) p.base[b * NEXP + e] += excl;
+  p.counts[e] = c;
+  p.offsets[e] = excl;
+  __syncthreads();
+  // tiles per expert: ceil(count / 256) token blocks x row blocks
+  const int nblk_tok = (c + GX_BN - 1) / GX_BN;
+  const int tg = nblk_tok * GU_MBLK, td = nblk_tok * DN_MBLK;
+  sc[e] = tg;
+  __syncthreads();
+  for (int off = 1; off < NEXP; off <<= 1) {
+    const int v = (e >= off) ? sc[e - off] : 0;
+    __syncthreads();
+    sc[e] += v;
+    __syncthreads();
+  }
+  p.tiles_gu[e] = sc[e] - tg;
+  if (e == NEXP - 1) s_tot[0] = sc[e];
+  __syncthreads();
+  sc[e] = td;
+  __syncthreads();
+  for (int off = 1; off < NEXP; off <<= 1) {
+    const int v = (e >= off) ? sc[e - off] : 0;
+    __syncthreads();
+    sc[e] += v;
+    __syncthreads();
+  }
+  p.tiles_dn[e] = sc[e] - td;
+  if (e == NEXP - 1) s_tot[1] = sc[e];
+  __syncthreads();
+  if (e == 0) {
+    const int sh_blk = (p.T + GX_BN - 1) / GX_BN;
+    p.counts[NEXP] = p.T;
+    p.offsets[NEXP] = 8 * p.T;
+    p.offsets[NEXP + 1] = 9 * p.T;
+    p.tiles_gu[NEXP] = s_tot[0];
+    p.tiles_gu[NEXP + 1] = s_tot[0] + sh_blk * GU_MBLK;
+    p.tiles_dn[NEXP] = s_tot[1];
+    p.tiles_dn[NEXP + 1] = s_tot[1] + sh_blk * DN_MBLK;
+  }
+}
+
+__global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams p) {
+  constexpr int SLOTS = RT_BM * TOPK;   // 1024 slots per router block
+  __shared__ int idx_s[SLOTS];
+  __shared__ int pos_s[SLOTS];
+  __shared__ int wh[8][NEXP];
+  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot0 = b * SLOTS;
+  const int nslots = min(SLOTS, p.T * TOPK - slot0);
+  for (int i = tid; i < SLOTS; i += SC_THREADS) idx_s[i] = (i < nslots) ? p.topk_idx[slot0 + i] : -1;
+  for (int i = tid; i < 8 * NEXP; i += SC_THREADS) (&wh[0][0])[i] = 0;
+  __syncthreads();
+  // pass 1: histogram of each warp's 128 consecutive slots
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = idx_s[warp * 128 + j * 32 + lane];
+    if (e >= 0) atomicAdd(&wh[warp][e], 1);
+  }
+  __syncthreads();
+  // pass 2: per expert, each warp's first global row (block base + earlier warps)
+  {
+    const int e = tid;
+    int run = p.base[b * NEXP + e];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = wh[w][e];
+      wh[w][e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // pass 3: stable ranks, slot order inside each warp's range
+  const int n8 = 8 * p.T;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int s = warp * 128 + j * 32 + lane;
+    const int e = idx_s[s];
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int pos = -1;
+    if (e >= 0) pos = wh[warp][e] + rank;
+    __syncwarp();
+    if (e >= 0 && rank == 0) wh[warp][e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0 && (e >= NEXP || pos < 0 || pos >= n8)) {
+      atomicOr(p.err, ERRBIT_BOUNDS);
+      pos = -1;
+    }
+    pos_s[s] = pos;
+    if (pos >= 0) {
+      p.row_dst[pos] = slot0 + s;
+      p.row_w[pos] = p.topk_w[slot0 + s];
+    }
+  }
+  __syncthreads();
+  if (!p.gather) return;
+  // gather: one warp per token; one read of x, nine interleaved copies
+  const int t0 = b * RT_BM;
+  for (int tl = warp; tl < RT_BM; tl += SC_THREADS / 32) {
+    const int t = t0 + tl;
+    if (t >= p.T) break;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * HID);
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = interleave8(ldg_nc_v4(src + lane + 32 * c));
+#pragma unroll 1
+    for (int k = 0; k <= TOPK; ++k) {
+      const int pos = (k < TOPK) ? pos_s[tl * TOPK + k] : n8 + t;
+      if (pos < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(p.x_perm + static_cast<size_t>(pos) * HID);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dst[lane + 32 * c] = v[c];
+    }
+  }
+}
+
+cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const CUtensorMap& tm_gs,
+                                  const RouteParams& p, cudaStream_t s) {
+  const int nblk = (p.T + RT_BM - 1) / RT_BM;
+  router_prefill_kernel<<<nblk, RT_THREADS, RT_SMEM, s>>>(tm_x, tm_wr, tm_gs, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
+  route_scan_kernel<<<1, NEXP, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
+  route_scatter_kernel<<<nblk, SC_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t set_router_attributes() {
+  return cudaFuncSetAttribute(router_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
+}
+
+}  // namespace moe

@@ -1,0 +1,152 @@
+/*
+ * moe_layer.h -- C ABI of a GB300 (sm_103a) library for the mixture-of-experts
+ * layer of Qwen3.6-35B-A3B over MLX affine 4-bit expert weights.
+ *
+ * What the layer is.  Lily, Perplexity's engine for this one model, scores all 256
+ * experts for every token, keeps 8 and adds one shared expert (aimanavo.com, "Why is
+ * Perplexity's local AI Lily faster than MLX", section "Qwen3.6's 256 experts and two
+ * layer kinds make the MLX/Lily gap").  Its weights are MLX affine 4-bit with group
+ * size 64, and anything else is refused when the model loads (same page, section
+ * "Only one 4-bit checkpoint of a pinned revision runs"; news.mantis.guru, "Perplexity
+ * opened Lily", section "Rust drives the model, Metal computes").  Prefill dequantises
+ * the 4-bit weights inside grouped GEMMs and keeps routing on the GPU with no host
+ * synchronisation; decode is bound by memory reads of the weights (aimanavo.com,
+ * section "Prefill and decode are not treated as the same job"; dzen.guru,
+ * "Perplexity opened the Lily engine", section "Where the speed-up comes from").
+ *
+ * The maths, per token x (bf16, hidden 2048):
+ *   w[o][i]  = scale[o][i/64] * q[o][i] + bias[o][i/64]   q = nibble i%8 of word i/8,
+ *                                                         low nibble first
+ *   l_e      = fp32 dot(x, W_r[e]) (+ router_bias[e])     e = 0..255
+ *   top-8 of softmax(l) (ties: lowest expert index), weights renormalised to sum 1
+ *   y_e      = W_down,e ( silu(W_gate,e x) * (W_up,e x) )
+ *   out      = sum_k w_k y_{e_k} + sigmoid(g_s . x) * y_shared   (+ x for *_residual)
+ *   rounded once to bf16.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except the *_host
+ *     entry, whose x/out are host pointers.  bf16 tensors are passed as void*.
+ *   - Nothing throws.  A status code is returned; host-side argument checks return
+ *     before any work is enqueued.
+ *   - Calls are asynchronous on `stream` and never synchronise the host (except
+ *     moe_layer_create, moe_layer_get_error and the *_host entry's copies as noted).
+ *   - The library never allocates device memory: all scratch lives in the caller's
+ *     workspace.  One workspace may back several layers that run one after another
+ *     on one stream; two calls that overlap in time need two workspaces.
+ *   - Device-side failures (a bounded wait that gave up, an index out of range) never
+ *     trap: they set a word in the workspace that moe_layer_get_error reads.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_layer moe_layer_t;        /* opaque; owned by the library */
+typedef struct CUstream_st* moe_stream_t;    /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* NULL pointer, T out of range, aliasing not allowed */
+    MOE_ERR_UNSUPPORTED = 2,    /* shapes or quantisation other than the one layer supported */
+    MOE_ERR_ALIGNMENT = 3,      /* a pointer not 16-byte aligned (workspace: 256-byte) */
+    MOE_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed */
+    MOE_ERR_TIMEOUT = 5,        /* a device-side bounded wait gave up */
+    MOE_ERR_DEVICE_BOUNDS = 6,  /* a device-side index check failed */
+    MOE_ERR_WORKSPACE = 7       /* workspace smaller than moe_workspace_bytes() */
+} moe_status_t;
+
+/* The layer's shape.  Only hidden 2048, 256 experts, top-8, intermediate 512, shared
+ * intermediate 512, group 64, 4 bits is accepted (Lily's own load-time refusal of every
+ * other checkpoint, cited above); max_tokens (1..65536) sizes the workspace. */
+typedef struct {
+    int hidden, n_experts, top_k, inter, shared_inter, group_size, bits, max_tokens;
+} moe_config_t;
+
+/* One MLX affine 4-bit matrix [out][in]: q uint32 [out][in/8] (eight codes per word,
+ * low nibble first), scales and biases bf16 [out][in/64].  Routed experts are stacked
+ * along a leading expert axis: q [256][out][in/8], scales/biases [256][out][in/64]. */
+typedef struct {
+    const void* q;
+    const void* scales;
+    const void* biases;
+} moe_qmat_t;
+
+typedef struct {
+    moe_qmat_t gate, up, down;          /* routed: gate/up [256][512][2048], down [256][2048][512] */
+    moe_qmat_t sh_gate, sh_up, sh_down; /* shared: gate/up [512][2048], down [2048][512] */
+    const void* router_w;               /* bf16 [256][2048] */
+    const float* router_bias;           /* fp32 [256] added to the logits before softmax, or NULL */
+    const void* shared_gate_w;          /* bf16 [2048] */
+} moe_weights_t;
+
+/* Bytes of device workspace a layer with this config needs (0 if the config is refused). */
+size_t moe_workspace_bytes(const moe_config_t* cfg);
+
+/* Validate the config and weights and bind them to `workspace` (device, 256-byte
+ * aligned, at least moe_workspace_bytes bytes, owned by the caller and kept alive as
+ * long as the layer).  Weights are borrowed for the layer's lifetime.  Synchronises
+ * the current device once (to initialise workspace constants).  On success *out
+ * receives a layer to free with moe_layer_destroy.
+ * Errors: INVALID_ARG (NULL), UNSUPPORTED (shape), ALIGNMENT, WORKSPACE, CUDA. */
+moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weights,
+                              void* workspace, size_t workspace_bytes, moe_layer_t** out);
+
+/* Routing only (router logits, softmax, top-8, renormalisation, expert histogram,
+ * exclusive-scan offsets and the stable token permutation), all on the device.
+ *   x        bf16 [T][2048]
+ *   topk_idx int32 [T][8]   experts in rank order
+ *   topk_w   fp32  [T][8]   renormalised weights
+ *   counts   int32 [256]    slots per expert
+ *   offsets  int32 [257]    exclusive scan of counts
+ *   perm     int32 [T*8]    slot ids t*8+k grouped by expert, ascending within one
+ * Any output pointer may be NULL.  1 <= T <= max_tokens. */
+moe_status_t moe_route(moe_layer_t* layer, const void* x, int T, int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, moe_stream_t stream);
+
+/* out[T][2048] (bf16) = the layer applied to x[T][2048] (bf16).  T <= 8 takes the
+ * decode path (dequant-GEMV kernels), larger T the prefill path (grouped tcgen05
+ * GEMMs).  out must not overlap x.  1 <= T <= max_tokens. */
+moe_status_t moe_forward(moe_layer_t* layer, const void* x, int T, void* out, moe_stream_t stream);
+
+/* out = x + layer(x), the residual form used between stacked layers.  out == x
+ * (in place) is allowed; a partial overlap is not. */
+moe_status_t moe_forward_residual(moe_layer_t* layer, const void* x, int T, void* out, moe_stream_t stream);
+
+/* x_io <- layer[n-1]( ... layer[0](x_io) ... ) with the residual add after every layer,
+ * in place on the device.  All layers must share one workspace. */
+moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x_io, int T, moe_stream_t stream);
+
+/* The same stack from HOST memory: copies x_host (bf16 [T][2048]) into the shared
+ * workspace's I/O buffer, runs the stack and copies the result to out_host, all
+ * enqueued on `stream`.  With pinned host buffers the copies are asynchronous and the
+ * caller must synchronise the stream before reading out_host. */
+moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, const void* x_host, int T,
+                                    void* out_host, moe_stream_t stream);
+
+/* Number of kernel launches one moe_forward of T tokens enqueues (for accounting). */
+int moe_forward_launches(int T);
+
+/* Synchronise the device, read and clear the layer's device error word.
+ * MOE_OK if nothing was recorded. */
+moe_status_t moe_layer_get_error(moe_layer_t* layer);
+
+/* Free the layer object (not the workspace or the weights, which the caller owns). */
+void moe_layer_destroy(moe_layer_t* layer);
+
+/* A static string naming a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* The calling thread's description of the last CUDA/driver failure behind an
+ * MOE_ERR_CUDA status (empty if none).  Valid until the thread's next call. */
+const char* moe_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

@@ -1,0 +1,210 @@
+"""Parity of the CUDA layer (through the C ABI) with the CPU oracle, on the GPU.
+
+Workloads are the seeded synthetic layer at its real shapes: T=32 (the reference
+configuration), T=1 and 8 (decode), T=512 uniform, T=4096 with the skewed log-Zipf
+router bias, a sweep of ragged T, all tokens forced onto one expert set, in-place
+residual, determinism, a short stack, and argument errors.  The rules are in
+tests/parity.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import synth
+from parity import bf16_to_f64, check_output, check_routing, check_tables
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_expert_layer_gb300.build import build
+    build()
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    from bit_expert_layer_gb300 import layer
+    return layer
+
+
+@pytest.fixture(scope="module")
+def host0():
+    return synth.make_layer(0)
+
+
+@pytest.fixture(scope="module")
+def dev0(lib, host0):
+    w = lib.DeviceWeights(host0)
+    return lib.MoELayer(w, max_tokens=4096)
+
+
+def to_dev(x_np):
+    return torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def to_host(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run(layer, x_np, residual=False):
+    x = to_dev(x_np)
+    out = layer.forward(x, residual=residual)
+    r = layer.route(x)
+    torch.cuda.synchronize()
+    assert layer.get_error() == 0
+    return to_host(out), {k: v.cpu().numpy() for k, v in r.items()}
+
+
+def full_check(oracle, L, layer, x, residual=False, sample=None):
+    out, r = run(layer, x, residual)
+    rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
+    check_tables(r["idx"], r["counts"], r["offsets"], r["perm"])
+    err, scale = check_output(oracle, L, x, out, tokens=sample, residual=residual, alt=alt)
+    return rep, err, scale
+
+
+def test_reference_T32(oracle, host0, dev0):
+    x = synth.make_x(0, 32)
+    rep, err, scale = full_check(oracle, host0, dev0, x)
+    print(f"T=32 {rep} max_err={err:.3e} scale={scale:.3e}")
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode(oracle, host0, dev0, T):
+    x = synth.make_x(0, T)
+    rep, err, scale = full_check(oracle, host0, dev0, x)
+    print(f"T={T} {rep} max_err={err:.3e} scale={scale:.3e}")
+
+
+@pytest.mark.parametrize("T", [2, 3, 7, 9, 31, 33, 127, 128, 129])
+def test_ragged_sweep(oracle, host0, dev0, T):
+    x = synth.make_x(100 + T, T)
+    full_check(oracle, host0, dev0, x)
+
+
+def test_prefill_T512(oracle, host0, dev0):
+    x = synth.make_x(0, 512)
+    rng = np.random.default_rng(512)
+    sample = np.unique(np.concatenate([rng.choice(512, 120, replace=False), np.arange(504, 512)]))
+    rep, err, scale = full_check(oracle, host0, dev0, x, sample=sample)
+    print(f"T=512 {rep} max_err={err:.3e} scale={scale:.3e}")
+
+
+def test_skewed_T4096(oracle, lib):
+    L = synth.make_layer(0, skew=True)
+    layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=4096)
+    x = synth.make_x(0, 4096)
+    out, r = run(layer, x)
+    rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
+    check_tables(r["idx"], r["counts"], r["offsets"], r["perm"])
+    counts = r["counts"]
+    heavy = np.argsort(-counts)[:3]
+    rng = np.random.default_rng(4096)
+    sample = set(rng.choice(4096, 64, replace=False).tolist()) | set(range(4088, 4096))
+    for e in heavy:   # tokens from the heaviest experts' last (ragged) tiles
+        slots = r["perm"][r["offsets"][e]:r["offsets"][e + 1]]
+        sample |= set((slots[-4:] // 8).tolist())
+    light = [e for e in range(256) if 0 < counts[e] <= 2][:4]
+    for e in light:
+        slots = r["perm"][r["offsets"][e]:r["offsets"][e + 1]]
+        sample |= set((slots // 8).tolist())
+    sample = np.array(sorted(sample))
+    err, scale = check_output(oracle, L, x, out, tokens=sample, alt=alt)
+    print(f"T=4096 skew {rep} touched={int((counts > 0).sum())} top={sorted(counts)[-3:]} "
+          f"max_err={err:.3e} scale={scale:.3e}")
+
+
+def test_all_tokens_on_one_expert_set(oracle, lib):
+    L = synth.make_layer(7)
+    chosen = [3, 17, 40, 77, 100, 150, 200, 255]
+    bias = np.zeros(256, np.float32)
+    bias[chosen] = 20.0
+    L.router_bias = bias
+    layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=1024)
+    x = synth.make_x(7, 600)
+    out, r = run(layer, x)
+    assert set(np.unique(r["idx"]).tolist()) == set(chosen)
+    assert all(r["counts"][e] == 600 for e in chosen)
+    rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
+    rng = np.random.default_rng(600)
+    sample = np.unique(np.concatenate([rng.choice(600, 60, replace=False), np.arange(590, 600)]))
+    check_output(oracle, L, x, out, tokens=sample, alt=alt)
+
+
+@pytest.mark.parametrize("T", [5, 40])
+def test_residual_in_place(oracle, host0, dev0, T):
+    x_np = synth.make_x(9, T)
+    x = to_dev(x_np)
+    dev0.forward(x, out=x, residual=True)
+    torch.cuda.synchronize()
+    assert dev0.get_error() == 0
+    out = to_host(x)
+    r = dev0.route(to_dev(x_np))
+    rep, alt = check_routing(oracle, host0, x_np, r["idx"].cpu().numpy(), r["w"].cpu().numpy())
+    check_output(oracle, host0, x_np, out, residual=True, alt=alt)
+
+
+def test_deterministic(host0, dev0):
+    for T in (300, 6):
+        x = to_dev(synth.make_x(11, T))
+        a = dev0.forward(x)
+        b = dev0.forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_short_stack(oracle, lib):
+    hosts = [synth.make_layer(seed=l, layer=l) for l in range(3)]
+    ws = lib.new_workspace(64)
+    layers = [lib.MoELayer(lib.DeviceWeights(h), max_tokens=64, workspace=ws) for h in hosts]
+    stack = lib.MoEStack(layers)
+    for T in (24, 5):
+        x_np = synth.make_x(12, T)
+        x = to_dev(x_np)
+        stack.forward_(x)
+        torch.cuda.synchronize()
+        got = to_host(x)
+        # the oracle chains its own bf16 outputs; tokens with a routing near-tie in any
+        # layer are left out (their downstream value depends on the valid choice made)
+        cur = x_np.copy()
+        keep = np.ones(T, bool)
+        for h in hosts:
+            r = oracle.forward(h, cur, residual=True)
+            keep &= r["gap"] > 1e-4
+            cur = r["out"]
+        # about 2% of tokens sit within 1e-4 of a tie at each layer of this router
+        assert keep.sum() >= T // 2
+        ref = bf16_to_f64(cur[keep])
+        err = np.max(np.abs(bf16_to_f64(got[keep]) - ref))
+        assert err <= 1e-2 * np.max(np.abs(ref)), err
+        # the host-memory entry gives the same bytes as the device entry
+        xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        stack.forward_host(xh, oh)
+        torch.cuda.synchronize()
+        assert np.array_equal(oh.numpy().view(np.uint16), got)
+
+
+def test_argument_errors(lib, dev0):
+    from bit_expert_layer_gb300 import _abi
+    x = to_dev(synth.make_x(0, 16))
+    out = torch.empty_like(x)
+    with pytest.raises(_abi.MoEError) as ei:
+        _abi.moe_forward(dev0.handle, x.data_ptr(), 0, out.data_ptr())
+    assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
+    with pytest.raises(_abi.MoEError) as ei:
+        _abi.moe_forward(dev0.handle, x.data_ptr(), 5000, out.data_ptr())
+    assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
+    with pytest.raises(_abi.MoEError) as ei:
+        _abi.moe_forward(dev0.handle, x.data_ptr() + 2, 8, out.data_ptr())
+    assert ei.value.status == _abi.MOE_ERR_ALIGNMENT
+    with pytest.raises(_abi.MoEError) as ei:
+        _abi.moe_forward(dev0.handle, x.data_ptr(), 16, x.data_ptr() + 4096)
+    assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
+    with pytest.raises(_abi.MoEError) as ei:
+        _abi.moe_forward_residual(dev0.handle, x.data_ptr(), 16, x.data_ptr() + 4096)
+    assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert dev0.get_error() == 0
