@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 4-bit MoE layer library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload ``stack40-T16384+T1``: 40 independently seeded MoE layers of
+Qwen3.6-35B-A3B's shape (18.2 GB of MLX affine 4-bit weights, residual add between
+layers, no attention).  One step = one prefill pass of T=16384 tokens through the
+40 layers plus one decode pass of T=1 token through the 40 layers, i.e. every step
+of the layer's hot path (routing, permutation, grouped gate/up and down GEMMs,
+combine, and the decode GEMVs).  Inputs are synthetic and seeded (``synth``).
+
+``value`` is MoE-layer tokens/s: (16384 + 1) tokens x 40 layers / step time, timed
+with CUDA events on the launching stream, inputs resident in HBM, max over ranks.
+The weights read per step (18.2 GB) are far larger than L2, so no L2 flush is needed.
+``e2e`` is the same metric through the C entry ``moe_stack_forward_host`` with the
+input copied from pinned host memory and the output copied back inside the timed
+region.  ``roofline`` is for the dominant kernel (the grouped gate/up GEMM), timed live
+by the library's event profiler during the timed steps.  ``cpu_baseline`` times the
+CPU oracle on a bounded sample.  With N>1 (torchrun) every rank runs an independent
+replica on its own GPU (weak scaling, no collective on the data path).
+
+``--impl reference`` times the CPU oracle (the only reference that exists: the pages'
+engine is Metal-only) on a bounded sample per step of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+METRIC = "MoE-layer tokens/s (prefill T=512..16K), decode µs/layer; % HBM/BF16 roofline"
+UNIT = "layer-tokens/s"
+FLOP_PER_TOKEN = 57_675_776          # per layer: 8 routed + 1 shared SwiGLU expert, router, shared gate
+GATEUP_FLOP_PER_ROW = 2 * 2 * 512 * 2048
+LAYER_BYTES = 455_806_976
+
+WORKLOADS = {
+    "stack40-T16384+T1": dict(layers=40, T_prefill=16384, T_decode=1, skew=False),
+    "layer-T4096-skew": dict(layers=1, T_prefill=4096, T_decode=0, skew=True),
+    "layer-T512": dict(layers=1, T_prefill=512, T_decode=0, skew=False),
+    "layer-T32": dict(layers=1, T_prefill=32, T_decode=0, skew=False),
+    "decode-T1": dict(layers=40, T_prefill=0, T_decode=1, skew=False),
+    "decode-T8": dict(layers=40, T_prefill=0, T_decode=8, skew=False),
+}
+DEFAULT_WORKLOAD = "stack40-T16384+T1"
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def make_hosts(wl):
+    import synth
+    n = wl["layers"]
+    if n == 1:
+        return [synth.make_layer(0, skew=wl["skew"])]
+    with ThreadPoolExecutor(4) as ex:
+        return list(ex.map(lambda l: synth.stack_layer(l, threads=2), range(n)))
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("expert_gemm.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "bit_expert_layer_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per gate/up launch from a committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
+
+
+def oracle_sample(hosts, wl, n_prefill: int, n_decode: int):
+    """Time the CPU oracle on a bounded sample of the workload; returns (layer-tokens, s, threads)."""
+    import synth
+    from oracle import Oracle, default_threads
+    o = Oracle()
+    threads = default_threads()
+    n_layers = len(hosts)
+    resid = n_layers > 1
+    layer_tokens = 0
+    t0 = time.perf_counter()
+    for T, n in ((wl["T_prefill"], n_prefill), (wl["T_decode"], n_decode)):
+        if T == 0 or n == 0:
+            continue
+        x = synth.make_x(0, T)[:n]
+        for h in hosts:
+            x = o.forward(h, x, residual=resid, nthreads=threads)["out"]
+        layer_tokens += n * n_layers
+    return layer_tokens, time.perf_counter() - t0, threads
+
+
+def run_reference(args, wl):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    hosts = make_hosts(wl)
+    n_pf = 4 if wl["T_prefill"] else 0
+    n_dc = 1 if wl["T_decode"] else 0
+    for _ in range(args.warmup):
+        oracle_sample(hosts[:1], wl, 1, 0 if n_pf else 1)
+    tot_tokens, tot_s, threads = 0, 0.0, 1
+    for _ in range(args.steps):
+        n, s, threads = oracle_sample(hosts, wl, n_pf, n_dc)
+        tot_tokens += n
+        tot_s += s
+    value = tot_tokens / tot_s
+    sample = (f"per step: {n_pf} of the {wl['T_prefill']} prefill tokens and {n_dc} decode token(s) "
+              f"through all {wl['layers']} layers on {threads} host threads")
+    line = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * tot_s / args.steps, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload=args.workload, **wl),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=threads, kind="oracle", sample=sample),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from bit_expert_layer_gb300 import _abi
+    from bit_expert_layer_gb300 import layer as ml
+    from bit_expert_layer_gb300.build import build
+
+    rank, world, local = rank_info()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    build()
+
+    hosts = make_hosts(wl)
+    Tp, Td, n_layers = wl["T_prefill"], wl["T_decode"], wl["layers"]
+    Tmax = max(Tp, Td, 1)
+    ws = ml.new_workspace(Tmax, dev)
+    layers = [ml.MoELayer(ml.DeviceWeights(h, dev), Tmax, workspace=ws) for h in hosts]
+    stack = ml.MoEStack(layers)
+    resid = n_layers > 1
+    stream = torch.cuda.current_stream(dev)
+
+    def to_dev(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    xp_src = to_dev(synth.make_x(0, Tp)) if Tp else None
+    xd_src = to_dev(synth.make_x(1, Td)) if Td else None
+    xp = torch.empty_like(xp_src) if Tp else None
+    xd = torch.empty_like(xd_src) if Td else None
+    outp = torch.empty_like(xp_src) if (Tp and not resid) else None
+    outd = torch.empty_like(xd_src) if (Td and not resid) else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if n_layers == 1 else None
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    part = {"prefill": [], "decode": []}
+
+    def step(record: bool):
+        if Tp:
+            a, b = ev(), ev()
+            xp.copy_(xp_src)
+            a.record(stream)
+            if resid:
+                stack.forward_(xp)
+            else:
+                layers[0].forward(xp, out=outp)
+            b.record(stream)
+            if record:
+                part["prefill"].append((a, b))
+        if Td:
+            a, b = ev(), ev()
+            xd.copy_(xd_src)
+            a.record(stream)
+            if resid:
+                stack.forward_(xd)
+            else:
+                layers[0].forward(xd, out=outd)
+            b.record(stream)
+            if record:
+                part["decode"].append((a, b))
+        if flush is not None:
+            flush.zero_()      # single-layer workloads: evict the weights from L2 between steps
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    assert layers[0].get_error() == 0
+
+    # ---------------- timed region (device)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    gpu_id = str(local)
+    cvd = [c.strip() for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
+    if local < len(cvd):
+        gpu_id = cvd[local]
+    else:
+        try:
+            u = str(getattr(torch.cuda.get_device_properties(dev), "uuid", ""))
+            if u:
+                gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+    clocks = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    _abi.moe_profiler_read()
+    _abi.moe_profiler_enable(True)
+    t0 = ev()
+    t1 = ev()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    _abi.moe_profiler_enable(False)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    if clk is not None:
+        clk["gpu"] = gpu_id
+    kern = _abi.moe_profiler_read()
+    # with the single-layer flush the step total excludes the flush: sum the parts
+    part_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in part.items()}
+    elapsed_ms = t0.elapsed_time(t1) if flush is None else part_ms["prefill"] + part_ms["decode"]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = layers[0].get_error()
+    assert status == 0, f"device error word {status}"
+
+    tokens_per_step = (Tp + Td) * n_layers
+    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    launches = args.steps * sum((_abi.moe_forward_launches(l.handle, Tp) if Tp else 0) +
+                                (_abi.moe_forward_launches(l.handle, Td) if Td else 0) for l in layers)
+
+    # ---------------- e2e: host buffers through the C entry, copies inside the region
+    e2e = None
+    if resid:
+        xh_p = torch.from_numpy(synth.make_x(0, Tp).view(np.int16)).pin_memory() if Tp else None
+        oh_p = torch.empty_like(xh_p).pin_memory() if Tp else None
+        xh_d = torch.from_numpy(synth.make_x(1, Td).view(np.int16)).pin_memory() if Td else None
+        oh_d = torch.empty_like(xh_d).pin_memory() if Td else None
+
+        def e2e_step():
+            if Tp:
+                stack.forward_host(xh_p, oh_p)
+            if Td:
+                stack.forward_host(xh_d, oh_d)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        nbytes = (Tp + Td) * 2048 * 2
+        e2e = dict(value=world * tokens_per_step * args.steps / (e_ms / 1e3), unit=UNIT,
+                   h2d_bytes_per_step=nbytes, d2h_bytes_per_step=nbytes, ms_per_step=e_ms / args.steps)
+
+    # ---------------- roofline of the dominant kernel
+    peaks = load_peaks()
+    roof = None
+    gu_ms, gu_n = kern.get("gateup", (0.0, 0))
+    if Tp and gu_n:
+        flop = GATEUP_FLOP_PER_ROW * 9 * Tp
+        achieved = flop / (gu_ms / gu_n / 1e3) / 1e12
+        peak = peaks["bf16_sustained"] if n_layers > 1 else peaks["bf16"]
+        tb = load_traffic(args.workload)
+        roof = dict(kernel="gateup", bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
+                    frac=achieved / peak, traffic=tb,
+                    algorithmic=f"{GATEUP_FLOP_PER_ROW} FLOP x 9T rows per launch (T={Tp})",
+                    peak_source=f"{peaks['src']} bf16 {'sustained' if n_layers > 1 else 'burst'}")
+    dec = None
+    if Td:
+        dms = part_ms["decode"] / args.steps
+        dec = dict(us_per_layer=1e3 * dms / n_layers, us_per_stack=1e3 * dms)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_pf = 6 if Tp else 0
+        n_dc = 1 if Td else 0
+        n, s, threads = oracle_sample(hosts, wl, n_pf, n_dc)
+        cpu = dict(value=n / s, unit=UNIT, cores=threads, kind="oracle",
+                   sample=f"{n_pf} prefill + {n_dc} decode tokens through all {n_layers} layers "
+                          f"({n} layer-tokens, {s:.1f} s)")
+
+    per_kernel = {k: dict(ms_avg=(v[0] / v[1]) if v[1] else None, launches=v[1], ms_total=v[0])
+                  for k, v in kern.items() if v[1]}
+    line = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=elapsed_ms / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="bf16", data="synthetic",
+        config=dict(workload=args.workload, layers=n_layers, T_prefill=Tp, T_decode=Td, skew=wl["skew"],
+                    weights="MLX affine 4-bit g64 (u4 codes, bf16 scale/bias); bf16 MMA, fp32 accumulate",
+                    l2=("weights read per step larger than L2" if n_layers > 1 else
+                        "256 MB L2 flush between steps (outside the events)"),
+                    parallelism=f"replicas x{world}"),
+        prefill_layer_tokens_per_s=(Tp * n_layers * args.steps / (part_ms["prefill"] / 1e3)) if Tp else None,
+        prefill_tflops=(FLOP_PER_TOKEN * Tp * n_layers * args.steps / (part_ms["prefill"] / 1e3) / 1e12)
+        if Tp else None,
+        decode=dec, roofline=roof, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clk,
+        kernels=per_kernel,
+    )
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

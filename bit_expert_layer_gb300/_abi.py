@@ -46,7 +46,8 @@ class MoeQMat(C.Structure):
 class MoeWeights(C.Structure):
     _fields_ = [("gate", MoeQMat), ("up", MoeQMat), ("down", MoeQMat),
                 ("sh_gate", MoeQMat), ("sh_up", MoeQMat), ("sh_down", MoeQMat),
-                ("router_w", C.c_void_p), ("router_bias", C.c_void_p), ("shared_gate_w", C.c_void_p)]
+                ("router_w", C.c_void_p), ("router_bias", C.c_void_p), ("shared_gate_w", C.c_void_p),
+                ("norm_w", C.c_void_p)]
 
 
 _lib = None
@@ -73,7 +74,7 @@ def lib() -> C.CDLL:
         L.moe_stack_forward.restype = S
         L.moe_stack_forward_host.argtypes = [P, I, P, I, P, P]
         L.moe_stack_forward_host.restype = S
-        L.moe_forward_launches.argtypes = [I]
+        L.moe_forward_launches.argtypes = [P, I]
         L.moe_forward_launches.restype = I
         L.moe_layer_get_error.argtypes = [P]
         L.moe_layer_get_error.restype = S
@@ -83,6 +84,10 @@ def lib() -> C.CDLL:
         L.moe_status_string.restype = C.c_char_p
         L.moe_last_error_detail.argtypes = []
         L.moe_last_error_detail.restype = C.c_char_p
+        L.moe_profiler_enable.argtypes = [I]
+        L.moe_profiler_enable.restype = None
+        L.moe_profiler_read.argtypes = [P, P, P, I]
+        L.moe_profiler_read.restype = I
         _lib = L
     return _lib
 
@@ -137,8 +142,8 @@ def moe_stack_forward_host(layers, x_host: int, T: int, out_host: int, stream: i
                                         stream or None), "moe_stack_forward_host")
 
 
-def moe_forward_launches(T: int) -> int:
-    return int(lib().moe_forward_launches(T))
+def moe_forward_launches(layer: int, T: int) -> int:
+    return int(lib().moe_forward_launches(layer, T))
 
 
 def moe_layer_get_error(layer: int) -> int:
@@ -151,6 +156,20 @@ def moe_layer_destroy(layer: int) -> None:
 
 def moe_status_string(status: int) -> str:
     return lib().moe_status_string(status).decode()
+
+
+def moe_profiler_enable(on: bool) -> None:
+    lib().moe_profiler_enable(1 if on else 0)
+
+
+def moe_profiler_read() -> dict:
+    """{kernel name: (total ms, launches)} since the last read."""
+    n = 32
+    names = (C.c_char_p * n)()
+    tot = (C.c_double * n)()
+    cnt = (C.c_longlong * n)()
+    k = lib().moe_profiler_read(C.cast(names, C.c_void_p), C.cast(tot, C.c_void_p), C.cast(cnt, C.c_void_p), n)
+    return {names[i].decode(): (tot[i], cnt[i]) for i in range(min(k, n))}
 
 
 def declared_functions() -> list[str]:

@@ -25,13 +25,12 @@ enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_BOUNDS = 2u };
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
 
 // ----------------------------------------------------------------- kernel geometry
-// Router (prefill): 128 tokens per CTA, 256 experts + 16 shared-gate rows on N.
+// Router (prefill): 128 tokens per CTA (M), the 256 experts on N.
 constexpr int RT_BM = 128;
 constexpr int RT_STAGES = 4;
 constexpr int RT_A_BYTES = RT_BM * 64 * 2;          // 16 KB  x tile
 constexpr int RT_B_BYTES = NEXP * 64 * 2;           // 32 KB  router tile
-constexpr int RT_G_BYTES = 16 * 64 * 2;             //  2 KB  shared-gate tile (1 real row)
-constexpr int RT_STAGE_BYTES = RT_A_BYTES + RT_B_BYTES + RT_G_BYTES;
+constexpr int RT_STAGE_BYTES = RT_A_BYTES + RT_B_BYTES;
 constexpr int RT_SMEM = RT_STAGES * RT_STAGE_BYTES + 1024 + 3072;
 constexpr int RT_THREADS = 128;
 

@@ -108,9 +108,9 @@ __global__ void __launch_bounds__(256) decode_router_kernel(DecodeParams p) {
       }
     }
   }
+  __threadfence();   // every writer publishes its logits before the ticket is taken
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
     const unsigned prev = atomicAdd(p.counter, 1u);
     s_last = (prev == gridDim.x - 1);
   }
@@ -212,10 +212,18 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeParams p) {
   __shared__ float red[8][32][8];
   const int a = blockIdx.y;
   const int n_act = __ldcg(p.n_active);
+  if (n_act < 1 || n_act > DEC_MAX_ACTIVE) {   // tables not built: record, touch nothing
+    if (threadIdx.x == 0 && blockIdx.x == 0 && a == 0) atomicOr(p.err, ERRBIT_BOUNDS);
+    return;
+  }
   if (a >= n_act) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const int e = __ldcg(p.act_expert + a);
+  if (e < 0 || e > NEXP) {
+    if (tid == 0) atomicOr(p.err, ERRBIT_BOUNDS);
+    return;
+  }
   const bool sh = e == NEXP;
   const int r0 = blockIdx.x * 16 + g, r1 = r0 + 8;
   const size_t rb0 = sh ? static_cast<size_t>(r0) : static_cast<size_t>(e) * INTER + r0;
@@ -308,7 +316,11 @@ __global__ void __launch_bounds__(512) decode_down_kernel(DecodeParams p) {
   const int g = lane >> 2, c = lane & 3;
   const int ks = warp & 3, eq = warp >> 2;
   const int r0 = blockIdx.x * 16 + g, r1 = r0 + 8;
-  const int n_act = __ldcg(p.n_active);
+  int n_act = __ldcg(p.n_active);
+  if (n_act < 1 || n_act > DEC_MAX_ACTIVE) {
+    if (tid == 0 && blockIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS);
+    n_act = 0;
+  }
   const int wo = ks * 16 + 4 * c;                  // word offset in a down row (64 words)
   const int gi = (ks * 128 + 32 * c) / GROUP;      // quantisation group (8 per row)
   float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -323,6 +335,11 @@ __global__ void __launch_bounds__(512) decode_down_kernel(DecodeParams p) {
       have[u] = a < n_act;
       if (!have[u]) continue;
       const int e = __ldcg(p.act_expert + a);
+      if (e < 0 || e > NEXP) {
+        if (lane == 0) atomicOr(p.err, ERRBIT_BOUNDS);
+        have[u] = false;
+        continue;
+      }
       const bool sh = e == NEXP;
       const size_t rw0 = sh ? static_cast<size_t>(r0) : static_cast<size_t>(e) * HID + r0;
       const size_t rw1 = rw0 + 8;
@@ -369,21 +386,25 @@ __global__ void __launch_bounds__(512) decode_down_kernel(DecodeParams p) {
       if (tok < p.T) {
         float o = s[i];
         const size_t off = static_cast<size_t>(tok) * HID + row;
-        if (p.residual) o += __bfloat162float(p.x[off]);
+        if (p.residual) o += __bfloat162float(p.x_resid[off]);
         p.out[off] = __float2bfloat16_rn(o);
       }
     }
   }
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int route_only, cudaStream_t s) {
+cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s) {
   decode_router_kernel<<<NEXP / 8 + 1, 256, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || route_only) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_gateup(const DecodeParams& p, cudaStream_t s) {
   const int ny = min(8 * p.T, NEXP) + 1;
   decode_gateup_kernel<<<dim3(INTER / 16, ny), 256, 0, s>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_down(const DecodeParams& p, cudaStream_t s) {
   decode_down_kernel<<<HID / 16, 512, 0, s>>>(p);
   return cudaGetLastError();
 }

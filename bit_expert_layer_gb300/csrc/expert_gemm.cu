@@ -42,10 +42,11 @@ constexpr int DN_P = GX_A_BYTES + GX_X_BYTES;
 
 struct TileInfo {
   int e, mb, row0, n_rows;
+  bool ok;   // tables consistent: every role skips a bad tile the same way
 };
 
 __device__ __forceinline__ TileInfo tile_info(const int* tiles, const int* offsets, const int* counts, int tile,
-                                              int mblk) {
+                                              int mblk, int T) {
   int lo = 0, hi = NEXP;   // largest e in [0, 256] with tiles[e] <= tile
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -59,6 +60,7 @@ __device__ __forceinline__ TileInfo tile_info(const int* tiles, const int* offse
   ti.mb = local - nb * mblk;
   ti.row0 = __ldg(offsets + lo) + nb * GX_BN;
   ti.n_rows = min(GX_BN, __ldg(counts + lo) - nb * GX_BN);
+  ti.ok = ti.n_rows >= 1 && ti.row0 >= 0 && ti.row0 + ti.n_rows <= 9 * T && local >= 0;
   return ti;
 }
 
@@ -129,7 +131,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       uint32_t it = 0;
       bool alive = true;
       for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, GU_MBLK);
+        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, GU_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
         const bool sh = ti.e == SHARED_E;
         const CUtensorMap* mg = sh ? &tm_sqg : &tm_qg;
         const CUtensorMap* mu = sh ? &tm_squ : &tm_qu;
@@ -157,8 +160,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       uint32_t it = 0, tc = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
-        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, GU_MBLK);
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, GU_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, N);
         if (!mbar_wait(ACCE, (tc & 1) ^ 1, p.err, abort_flag)) break;
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         }
         if (!alive) break;
         umma_commit(ACCF);
+        ++tc;
       }
       umma_commit(DRAIN);
     }
@@ -196,8 +201,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     const int half = (warp - 2) >> 2;  // which half of the token columns this warp drains
     uint32_t it = 0, tc = 0;
     bool alive = true;
-    for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x, ++tc) {
-      const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, GU_MBLK);
+    for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+      const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, GU_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
       const bool sh = ti.e == SHARED_E;
       const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + r)
                              : static_cast<size_t>(ti.e) * INTER + ti.mb * GX_BM + r;
@@ -265,6 +271,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(ACCE);
+      ++tc;
     }
   }
 
@@ -334,7 +341,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       uint32_t it = 0;
       bool alive = true;
       for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK);
+        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
         const bool sh = ti.e == SHARED_E;
         const CUtensorMap* mq = sh ? &tm_sqd : &tm_qd;
         const int wrow = (sh ? 0 : ti.e * HID) + ti.mb * GX_BM;
@@ -359,8 +367,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
-        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK);
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, N);
         const int buf = tc & 1;
@@ -385,6 +394,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         }
         if (!alive) break;
         umma_commit(ACCF(buf));
+        ++tc;
       }
       umma_commit(DRAIN);
     }
@@ -394,7 +404,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
     uint32_t it = 0;
     bool alive = true;
     for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-      const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK);
+      const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
       const bool sh = ti.e == SHARED_E;
       const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + r)
                              : static_cast<size_t>(ti.e) * HID + ti.mb * GX_BM + r;
@@ -432,8 +443,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int nrows_all = 9 * p.T;
     uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tc) {
-      const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK);
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = tile_info(p.tiles, p.offsets, p.counts, tile, DN_MBLK, p.T);
+        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
       const int buf = tc & 1;
       bool ok = mbar_wait(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -464,6 +476,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(ACCE(buf));
+      ++tc;
     }
   }
 

@@ -16,8 +16,6 @@ struct RouteParams {
   int* topk_idx;             // [T][8]
   float* topk_w;             // [T][8]
   int* hist;                 // [nblk][256] per-router-block expert histogram
-  int* row_dst;              // [9T] destination row of each permuted row (shared part written here)
-  float* row_w;              // [9T] weight of each permuted row (shared part written here)
   unsigned int* err;
 };
 
@@ -37,9 +35,10 @@ struct ScatterParams {
   const float* topk_w;
   const int* base;
   int T;
-  int* row_dst;       // [9T] (routed part) == permutation of slot ids
-  float* row_w;       // [9T]
+  int* row_dst;       // [9T] routed part: the permutation of slot ids; shared part: 8T+t
+  float* row_w;       // [9T] routing weight (routed rows) or shared-gate sigmoid (shared rows)
   const __nv_bfloat16* x;
+  const __nv_bfloat16* shared_gate_w;   // [2048]
   __nv_bfloat16* x_perm;   // [9T][2048], K-interleaved rows
   int gather;
   unsigned int* err;
@@ -54,6 +53,7 @@ struct GateUpParams {
   const uint16_t* sg_scales; const uint16_t* sg_biases;  // [512][32]
   const uint16_t* su_scales; const uint16_t* su_biases;
   __nv_bfloat16* h;      // [9T][512], K-interleaved columns
+  int T;
   unsigned int* err;
 };
 
@@ -95,13 +95,16 @@ struct DecodeParams {
   const uint32_t* sdq; const uint16_t* sds; const uint16_t* sdb;  // shared down
   __nv_bfloat16* hw;     // [65][8][512] weighted, K-interleaved
   __nv_bfloat16* out;    // [T][2048]
+  const __nv_bfloat16* x_resid;   // [T][2048] residual input (the un-normalised x)
   int residual;
   unsigned int* err;
 };
 
 // launchers (return the first launch error)
-cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const CUtensorMap& tm_gs,
-                                  const RouteParams& p, cudaStream_t s);
+cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
+                                  cudaStream_t s);
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* xn, int T,
+                           cudaStream_t s);
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
 cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s);
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
@@ -111,7 +114,9 @@ cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUt
                         const DownParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const __nv_bfloat16* y, const __nv_bfloat16* x, __nv_bfloat16* out, int T,
                            int residual, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, int route_only, cudaStream_t s);
+cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_gateup(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_down(const DecodeParams& p, cudaStream_t s);
 cudaError_t set_kernel_attributes();
 
 }  // namespace moe

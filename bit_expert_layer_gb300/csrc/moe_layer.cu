@@ -9,9 +9,11 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -33,20 +35,19 @@ struct moe_layer {
   // workspace segments
   unsigned int* err;
   unsigned int* dec_counter;
-  __nv_bfloat16* gs16;
   int *hist, *base, *counts, *offsets, *tiles_gu, *tiles_dn;
   int* topk_idx;
   float* topk_w;
   int* row_dst;
   float* row_w;
-  __nv_bfloat16 *x_perm, *h, *y, *x_io;
+  __nv_bfloat16 *x_perm, *h, *y, *x_io, *xn;
   float* dec_logits;
   int* dec_act_expert;
   float* dec_act_w;
   int* dec_n_active;
   __nv_bfloat16* dec_hw;
   // TMA descriptors of the weights and of the workspace buffers
-  CUtensorMap tm_wr, tm_gs, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_xperm, tm_h;
+  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_xperm, tm_h;
 };
 
 namespace {
@@ -55,6 +56,78 @@ thread_local char g_detail[256] = "";
 
 void set_detail(const char* what, cudaError_t e) {
   snprintf(g_detail, sizeof g_detail, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ kernel profiler
+// While enabled, every launch is bracketed by two CUDA events on its own stream; the
+// durations are resolved (and the record cleared) by moe_profiler_read.
+enum KernelId {
+  K_ROUTER, K_SCAN, K_SCATTER, K_GATEUP, K_DOWN, K_COMBINE, K_DEC_ROUTER, K_DEC_GATEUP, K_DEC_DOWN, K_NORM,
+  K_COUNT
+};
+const char* const kKernelNames[K_COUNT] = {"router_prefill", "route_scan",    "route_scatter",
+                                           "gateup",         "down",          "combine",
+                                           "decode_router",  "decode_gateup", "decode_down",
+                                           "rmsnorm"};
+struct ProfRec {
+  int id;
+  cudaEvent_t a, b;
+};
+struct Profiler {
+  bool on = false;
+  std::mutex m;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> pool;
+} g_prof;
+
+cudaEvent_t prof_event() {
+  if (!g_prof.pool.empty()) {
+    cudaEvent_t e = g_prof.pool.back();
+    g_prof.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// MOE_DEBUG_SYNC=1 (read once): synchronise after every launch, and turn a CUDA error
+// or a bit in the device error word into cudaErrorUnknown naming the kernel.
+bool debug_sync() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_DEBUG_SYNC");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+template <typename F>
+cudaError_t timed(int id, cudaStream_t s, const unsigned int* err_word, F&& launch) {
+  cudaError_t e;
+  if (!g_prof.on) {
+    e = launch();
+  } else {
+    std::lock_guard<std::mutex> lk(g_prof.m);
+    ProfRec r{id, prof_event(), prof_event()};
+    cudaEventRecord(r.a, s);
+    e = launch();
+    cudaEventRecord(r.b, s);
+    g_prof.recs.push_back(r);
+  }
+  if (e == cudaSuccess && debug_sync()) {
+    e = cudaStreamSynchronize(s);
+    unsigned int w = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&w, err_word, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      snprintf(g_detail, sizeof g_detail, "kernel %s: %s", kKernelNames[id], cudaGetErrorString(e));
+      fprintf(stderr, "[moe debug] %s\n", g_detail);
+    } else if (w) {
+      snprintf(g_detail, sizeof g_detail, "kernel %s set device error bits 0x%x", kKernelNames[id], w);
+      fprintf(stderr, "[moe debug] %s\n", g_detail);
+      e = cudaErrorUnknown;
+    }
+  }
+  return e;
 }
 
 constexpr int MAX_TOKENS = 65536;
@@ -80,7 +153,6 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   const size_t rows = 9ull * Tm;
   d->err = c.take<unsigned int>(256);
   d->dec_counter = c.take<unsigned int>(256);
-  d->gs16 = c.take<__nv_bfloat16>(16ull * HID * 2);
   d->hist = c.take<int>(nblk * NEXP * 4);
   d->base = c.take<int>(nblk * NEXP * 4);
   d->counts = c.take<int>((NEXP + 1) * 4);
@@ -95,6 +167,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->h = c.take<__nv_bfloat16>(rows * INTER * 2);
   d->y = c.take<__nv_bfloat16>(rows * HID * 2);
   d->x_io = c.take<__nv_bfloat16>(static_cast<size_t>(Tm) * HID * 2);
+  d->xn = c.take<__nv_bfloat16>(static_cast<size_t>(Tm) * HID * 2);
   d->dec_logits = c.take<float>(DEC_MAX_T * (NEXP + 1) * 4);
   d->dec_act_expert = c.take<int>(DEC_MAX_ACTIVE * 4);
   d->dec_act_w = c.take<float>(DEC_MAX_ACTIVE * DEC_MAX_T * 4);
@@ -175,14 +248,14 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   const int nblk = (T + RT_BM - 1) / RT_BM;
   CUtensorMap tm_x;
   if (!encode_bf16_rows(&tm_x, x, HID, T, RT_BM)) return MOE_ERR_CUDA;
-  RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist,
-                 L->row_dst, L->row_w, L->err};
-  MOE_TRY(launch_router_prefill(tm_x, L->tm_wr, L->tm_gs, rp, s), "router launch");
+  RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist, L->err};
+  MOE_TRY(timed(K_ROUTER, s, L->err, [&] { return launch_router_prefill(tm_x, L->tm_wr, rp, s); }), "router launch");
   ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->tiles_gu, L->tiles_dn};
-  MOE_TRY(launch_scan(sp, s), "scan launch");
+  MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
   ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->row_w,
-                    static_cast<const __nv_bfloat16*>(x), L->x_perm, gather, L->err};
-  MOE_TRY(launch_scatter(scp, nblk, s), "scatter launch");
+                    static_cast<const __nv_bfloat16*>(x),
+                    static_cast<const __nv_bfloat16*>(L->w.shared_gate_w), L->x_perm, gather, L->err};
+  MOE_TRY(timed(K_SCATTER, s, L->err, [&] { return launch_scatter(scp, nblk, s); }), "scatter launch");
   return MOE_OK;
 }
 
@@ -222,10 +295,30 @@ DecodeParams decode_params(moe_layer* L, const void* x, int T, void* out, int re
   return p;
 }
 
-moe_status_t forward_impl(moe_layer* L, const void* x, int T, void* out, int residual, cudaStream_t s) {
+// The layer's input to routing and experts: x itself, or its RMSNorm when the layer has one.
+moe_status_t layer_input(moe_layer* L, const void* x, int T, cudaStream_t s, const void** xin) {
+  *xin = x;
+  if (!L->w.norm_w) return MOE_OK;
+  MOE_TRY(timed(K_NORM, s, L->err,
+                [&] {
+                  return launch_rmsnorm(static_cast<const __nv_bfloat16*>(x),
+                                        static_cast<const __nv_bfloat16*>(L->w.norm_w), L->xn, T, s);
+                }),
+          "rmsnorm launch");
+  *xin = L->xn;
+  return MOE_OK;
+}
+
+moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, int residual, cudaStream_t s) {
+  const void* x = nullptr;
+  const moe_status_t sn = layer_input(L, x_orig, T, s, &x);
+  if (sn != MOE_OK) return sn;
   if (T <= DEC_MAX_T) {
-    const DecodeParams p = decode_params(L, x, T, out, residual);
-    MOE_TRY(launch_decode(p, 0, s), "decode launch");
+    DecodeParams p = decode_params(L, x, T, out, residual);
+    p.x_resid = static_cast<const __nv_bfloat16*>(x_orig);
+    MOE_TRY(timed(K_DEC_ROUTER, s, L->err, [&] { return launch_decode_router(p, s); }), "decode router launch");
+    MOE_TRY(timed(K_DEC_GATEUP, s, L->err, [&] { return launch_decode_gateup(p, s); }), "decode gate/up launch");
+    MOE_TRY(timed(K_DEC_DOWN, s, L->err, [&] { return launch_decode_down(p, s); }), "decode down launch");
     return MOE_OK;
   }
   const moe_status_t st = route_prefill(L, x, T, 1, s);
@@ -235,18 +328,23 @@ moe_status_t forward_impl(moe_layer* L, const void* x, int T, void* out, int res
   GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                  L->h, L->err};
+                  L->h, T, L->err};
   // upper bound of the tile count: every touched expert adds at most one partial token block
   const long long tok_blocks = (8ll * T + GX_BN - 1) / GX_BN + (8ll * T < NEXP ? 8ll * T : NEXP) +
                                (T + GX_BN - 1) / GX_BN;
   const int grid_gu = static_cast<int>(tok_blocks * GU_MBLK < L->num_sms ? tok_blocks * GU_MBLK : L->num_sms);
   const int grid_dn = static_cast<int>(tok_blocks * DN_MBLK < L->num_sms ? tok_blocks * DN_MBLK : L->num_sms);
-  MOE_TRY(launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_xperm, gp, grid_gu, s), "gate/up launch");
+  MOE_TRY(timed(K_GATEUP, s, L->err,
+                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_xperm, gp, grid_gu, s); }),
+          "gate/up launch");
   DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->row_dst, L->row_w, L->y, T, L->err};
-  MOE_TRY(launch_down(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_dn, s), "down launch");
-  MOE_TRY(launch_combine(L->y, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(out), T,
-                         residual, s),
+  MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_dn, s); }), "down launch");
+  MOE_TRY(timed(K_COMBINE, s, L->err,
+                [&] {
+                  return launch_combine(L->y, static_cast<const __nv_bfloat16*>(x_orig),
+                                        static_cast<__nv_bfloat16*>(out), T, residual, s);
+                }),
           "combine launch");
   return MOE_OK;
 }
@@ -280,7 +378,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
     if (!qmat_ok(*m, &st)) return st;
   if (!weights->router_w || !weights->shared_gate_w || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(weights->router_w, 16) || !aligned(weights->shared_gate_w, 16) ||
-      (weights->router_bias && !aligned(weights->router_bias, 16)) || !aligned(workspace, 256))
+      (weights->router_bias && !aligned(weights->router_bias, 16)) ||
+      (weights->norm_w && !aligned(weights->norm_w, 16)) || !aligned(workspace, 256))
     return MOE_ERR_ALIGNMENT;
   const size_t need = carve(cfg->max_tokens, nullptr, nullptr);
   if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
@@ -305,16 +404,14 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
   }
   if ((e = set_router_attributes()) != cudaSuccess || (e = set_gemm_attributes()) != cudaSuccess)
     return fail(cuda_fail("kernel attributes", e));
-  // workspace constants: the error word, the decode ticket, the 16-row shared-gate tile
+  // workspace state shared by every layer bound to it: the error word and the decode
+  // ticket (nothing layer-specific may live in the workspace)
   if ((e = cudaMemset(L->err, 0, 256)) != cudaSuccess || (e = cudaMemset(L->dec_counter, 0, 256)) != cudaSuccess ||
-      (e = cudaMemset(L->gs16, 0, 16ull * HID * 2)) != cudaSuccess ||
-      (e = cudaMemcpy(L->gs16, weights->shared_gate_w, HID * 2, cudaMemcpyDeviceToDevice)) != cudaSuccess ||
       (e = cudaDeviceSynchronize()) != cudaSuccess)
     return fail(cuda_fail("workspace init", e));
 
   const int Tm = cfg->max_tokens;
   bool ok = encode_bf16_rows(&L->tm_wr, weights->router_w, HID, NEXP, NEXP) &&
-            encode_bf16_rows(&L->tm_gs, L->gs16, HID, 16, 16) &&
             encode_packed(&L->tm_qg, weights->gate.q, HID / 8, static_cast<uint64_t>(NEXP) * INTER) &&
             encode_packed(&L->tm_qu, weights->up.q, HID / 8, static_cast<uint64_t>(NEXP) * INTER) &&
             encode_packed(&L->tm_sqg, weights->sh_gate.q, HID / 8, SH_INTER) &&
@@ -334,9 +431,13 @@ moe_status_t moe_route(moe_layer_t* L, const void* x, int T, int32_t* topk_idx, 
   if (T < 1 || T > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16)) return MOE_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const void* xin = nullptr;
+  const moe_status_t sn = layer_input(L, x, T, s, &xin);
+  if (sn != MOE_OK) return sn;
+  x = xin;
   if (T <= DEC_MAX_T) {
     const DecodeParams p = decode_params(L, x, T, nullptr, 0);
-    MOE_TRY(launch_decode(p, 1, s), "decode router launch");
+    MOE_TRY(timed(K_DEC_ROUTER, s, L->err, [&] { return launch_decode_router(p, s); }), "decode router launch");
   } else {
     const moe_status_t st = route_prefill(L, x, T, 0, s);
     if (st != MOE_OK) return st;
@@ -392,7 +493,10 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
   return MOE_OK;
 }
 
-int moe_forward_launches(int T) { return T <= DEC_MAX_T ? 3 : 6; }
+int moe_forward_launches(const moe_layer_t* L, int T) {
+  if (!L || T < 1 || T > L->cfg.max_tokens) return 0;
+  return (T <= DEC_MAX_T ? 3 : 6) + (L->w.norm_w ? 1 : 0);
+}
 
 moe_status_t moe_layer_get_error(moe_layer_t* L) {
   if (!L) return MOE_ERR_INVALID_ARG;
@@ -424,5 +528,32 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 const char* moe_last_error_detail(void) { return g_detail; }
+
+void moe_profiler_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof.m);
+  g_prof.on = on != 0;
+}
+
+int moe_profiler_read(const char** names, double* total_ms, long long* launches, int max) {
+  std::lock_guard<std::mutex> lk(g_prof.m);
+  double tot[K_COUNT] = {0};
+  long long cnt[K_COUNT] = {0};
+  for (const ProfRec& r : g_prof.recs) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      tot[r.id] += ms;
+      cnt[r.id] += 1;
+    }
+    g_prof.pool.push_back(r.a);
+    g_prof.pool.push_back(r.b);
+  }
+  g_prof.recs.clear();
+  for (int i = 0; i < K_COUNT && i < max; ++i) {
+    if (names) names[i] = kKernelNames[i];
+    if (total_ms) total_ms[i] = tot[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return K_COUNT;
+}
 
 }  // extern "C"

@@ -5,17 +5,17 @@
 // "Perplexity opened the Lily engine", section "Where the speed-up comes from").
 //
 //   router_prefill_kernel  logits = x W_r^T on tcgen05 (bf16 in, fp32 accumulate in
-//                          TMEM), plus the shared-expert gate g_s . x as 16 extra
-//                          N columns; per token: top-8 by logit with lowest-index
-//                          ties, weights exp(l_k - l_1) / sum (equal to softmax over
-//                          all 256 followed by renormalisation over the 8), the
-//                          shared gate sigmoid, and a per-CTA expert histogram.
+//                          TMEM); per token: top-8 by logit with lowest-index ties,
+//                          weights exp(l_k - l_1) / sum (equal to softmax over all 256
+//                          followed by renormalisation over the 8), and a per-CTA
+//                          expert histogram.
 //   route_scan_kernel      per-expert counts, exclusive-scan offsets, the first
 //                          permuted row of every (router block, expert), and the
 //                          tile tables of both grouped GEMMs.
 //   route_scatter_kernel   stable permutation of the slots t*8+k into expert order,
-//                          the per-row weight, and the gather of x into x_perm
-//                          (8 routed copies + 1 shared copy per token).
+//                          the per-row weight, the gather of x into x_perm (8 routed
+//                          copies + 1 shared copy per token) and, on the same read of
+//                          x, the shared-expert gate sigmoid(g_s . x).
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,7 +23,7 @@ namespace moe {
 
 __global__ void __launch_bounds__(RT_THREADS, 1)
     router_prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wr,
-                          const __grid_constant__ CUtensorMap tm_gs, RouteParams p) {
+                          RouteParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RT_STAGES * RT_STAGE_BYTES);  // full[4] empty[4] done
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     bias_s[i] = p.router_bias ? p.router_bias[i] : 0.0f;
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     // ---- TMA producer
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_wr);
-    tma_prefetch_desc(&tm_gs);
     int issued = 0;
     for (int kb = 0; kb < NKB; ++kb) {
       const int s = kb % RT_STAGES;
@@ -73,7 +72,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
       tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kb * 64, m0);
       tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kb * 64, 0);
-      tma_load_2d(smem_u32(st + RT_A_BYTES + RT_B_BYTES), &tm_gs, full0 + 8 * s, kb * 64, 0);
       issued = kb + 1;
     }
     if (*abort_flag) {
@@ -87,21 +85,17 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
-    const uint32_t id_r = idesc_bf16(128, 256), id_g = idesc_bf16(128, 16);
+    const uint32_t id_r = idesc_bf16(128, 256);
     for (int kb = 0; kb < NKB; ++kb) {
       const int s = kb % RT_STAGES;
       const uint32_t ph = (kb / RT_STAGES) & 1;
       if (!mbar_wait(full0 + 8 * s, ph, p.err, abort_flag)) break;
       tc_fence_after();
       const uint32_t a = smem_u32(smem + s * RT_STAGE_BYTES);
-      const uint32_t b = a + RT_A_BYTES, g = b + RT_B_BYTES;
+      const uint32_t b = a + RT_A_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = sdesc_sw128(a + kk * 32);
-        const uint32_t acc = (kb | kk) != 0;
-        umma_bf16(tmem, ad, sdesc_sw128(b + kk * 32), id_r, acc);
-        umma_bf16(tmem + 256, ad, sdesc_sw128(g + kk * 32), id_g, acc);
-      }
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem, sdesc_sw128(a + kk * 32), sdesc_sw128(b + kk * 32), id_r, (kb | kk) != 0);
       umma_commit(empty0 + 8 * s);
     }
     umma_commit(done);   // also covers an early exit: all issued MMAs complete first
@@ -141,10 +135,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         }
       }
     }
-    uint32_t gr;
-    tmem_ld1(lane_base + 256, gr);
-    tmem_ld_wait();
     if (t < p.T) {
+      // fewer than 8 ordered logits (NaN input): record it and route to expert 0
+      if (ti[TOPK - 1] >= NEXP) {
+        atomicOr(p.err, ERRBIT_BOUNDS);
+#pragma unroll
+        for (int k = 0; k < TOPK; ++k)
+          if (ti[k] >= NEXP) { ti[k] = k; tv[k] = tv[0]; }
+      }
       float ex[TOPK], sum = 0.0f;
 #pragma unroll
       for (int k = 0; k < TOPK; ++k) { ex[k] = expf(tv[k] - tv[0]); sum += ex[k]; }
@@ -155,11 +153,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
         p.topk_w[t * TOPK + k] = ex[k] * inv;
         atomicAdd(&hist_s[ti[k]], 1);
       }
-      const float z = __uint_as_float(gr);
-      const float sg = 1.0f / (1.0f + expf(-z));
-      const int srow = 8 * p.T + t;
-      p.row_dst[srow] = srow;
-      p.row_w[srow] = sg;
     }
   }
   tc_fence_before();
@@ -174,7 +167,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       }
     }
     __syncwarp();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -248,7 +241,14 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slot0 = b * SLOTS;
   const int nslots = min(SLOTS, p.T * TOPK - slot0);
-  for (int i = tid; i < SLOTS; i += SC_THREADS) idx_s[i] = (i < nslots) ? p.topk_idx[slot0 + i] : -1;
+  for (int i = tid; i < SLOTS; i += SC_THREADS) {
+    int e = (i < nslots) ? p.topk_idx[slot0 + i] : -1;
+    if (e >= NEXP || e < -1) {   // never index shared memory with a bad expert id
+      atomicOr(p.err, ERRBIT_BOUNDS);
+      e = -1;
+    }
+    idx_s[i] = e;
+  }
   for (int i = tid; i < 8 * NEXP; i += SC_THREADS) (&wh[0][0])[i] = 0;
   __syncthreads();
   // pass 1: histogram of each warp's 128 consecutive slots
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
     __syncwarp();
     if (e >= 0 && rank == 0) wh[warp][e] += __popc(peers);
     __syncwarp();
-    if (e >= 0 && (e >= NEXP || pos < 0 || pos >= n8)) {
+    if (e >= 0 && (pos < 0 || pos >= n8)) {
       atomicOr(p.err, ERRBIT_BOUNDS);
       pos = -1;
     }
@@ -295,15 +295,37 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   }
   __syncthreads();
   if (!p.gather) return;
-  // gather: one warp per token; one read of x, nine interleaved copies
+  // gather: one warp per token; one read of x, nine interleaved copies, and the
+  // shared-expert gate on the same read
   const int t0 = b * RT_BM;
+  const uint4* gsv = reinterpret_cast<const uint4*>(p.shared_gate_w);
   for (int tl = warp; tl < RT_BM; tl += SC_THREADS / 32) {
     const int t = t0 + tl;
     if (t >= p.T) break;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * HID);
     uint4 v[8];
+    float dot = 0.0f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) v[c] = interleave8(ldg_nc_v4(src + lane + 32 * c));
+    for (int c = 0; c < 8; ++c) {
+      const uint4 raw = ldg_nc_v4(src + lane + 32 * c);
+      const uint4 g = ldg_nc_v4(gsv + lane + 32 * c);
+      dot = fmaf(bf16lo(raw.x), bf16lo(g.x), dot);
+      dot = fmaf(bf16hi(raw.x), bf16hi(g.x), dot);
+      dot = fmaf(bf16lo(raw.y), bf16lo(g.y), dot);
+      dot = fmaf(bf16hi(raw.y), bf16hi(g.y), dot);
+      dot = fmaf(bf16lo(raw.z), bf16lo(g.z), dot);
+      dot = fmaf(bf16hi(raw.z), bf16hi(g.z), dot);
+      dot = fmaf(bf16lo(raw.w), bf16lo(g.w), dot);
+      dot = fmaf(bf16hi(raw.w), bf16hi(g.w), dot);
+      v[c] = interleave8(raw);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) {
+      const int srow = n8 + t;
+      p.row_dst[srow] = srow;
+      p.row_w[srow] = 1.0f / (1.0f + expf(-dot));
+    }
 #pragma unroll 1
     for (int k = 0; k <= TOPK; ++k) {
       const int pos = (k < TOPK) ? pos_s[tl * TOPK + k] : n8 + t;
@@ -315,10 +337,58 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   }
 }
 
-cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const CUtensorMap& tm_gs,
-                                  const RouteParams& p, cudaStream_t s) {
+// Input RMSNorm of a stacked layer: xn = bf16(x / sqrt(mean(x^2) + 1e-6) * w), one warp
+// per token row, fp32 sum of squares in a fixed order (lane partials, xor tree).
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                      const __nv_bfloat16* __restrict__ w,
+                                                      __nv_bfloat16* __restrict__ xn, int T) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= T) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * HID);
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+  uint4 v[8];
+  float ss = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = ldg_nc_v4(src + lane + 32 * j);
+    const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ss = fmaf(bf16lo(u[i]), bf16lo(u[i]), ss);
+      ss = fmaf(bf16hi(u[i]), bf16hi(u[i]), ss);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float r = 1.0f / sqrtf(ss / static_cast<float>(HID) + 1e-6f);
+  uint4* dst = reinterpret_cast<uint4*>(xn + static_cast<size_t>(row) * HID);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 g = ldg_nc_v4(wv + lane + 32 * j);
+    const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(bf16lo(u[i]) * r * bf16lo(gw[i]),
+                                                      bf16hi(u[i]) * r * bf16hi(gw[i]));
+      o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    dst[lane + 32 * j] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* xn, int T,
+                           cudaStream_t s) {
+  rmsnorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, w, xn, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
+                                  cudaStream_t s) {
   const int nblk = (p.T + RT_BM - 1) / RT_BM;
-  router_prefill_kernel<<<nblk, RT_THREADS, RT_SMEM, s>>>(tm_x, tm_wr, tm_gs, p);
+  router_prefill_kernel<<<nblk, RT_THREADS, RT_SMEM, s>>>(tm_x, tm_wr, p);
   return cudaGetLastError();
 }
 

@@ -56,13 +56,16 @@ class DeviceWeights:
         self.shared_gate_w = _dev(host.shared_gate_w, device)
         rb = getattr(host, "router_bias", None)
         self.router_bias = None if rb is None else _dev(np.asarray(rb, np.float32), device)
+        nw = getattr(host, "norm_w", None)
+        self.norm_w = None if nw is None else _dev(np.asarray(nw, np.uint16), device)
 
     def c(self) -> MoeWeights:
         m = self.mats
         return MoeWeights(m["gate"].c(), m["up"].c(), m["down"].c(), m["sh_gate"].c(), m["sh_up"].c(),
                           m["sh_down"].c(), self.router_w.data_ptr(),
                           None if self.router_bias is None else self.router_bias.data_ptr(),
-                          self.shared_gate_w.data_ptr())
+                          self.shared_gate_w.data_ptr(),
+                          None if self.norm_w is None else self.norm_w.data_ptr())
 
     @property
     def nbytes(self) -> int:

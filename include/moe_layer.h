@@ -82,6 +82,10 @@ typedef struct {
     const void* router_w;               /* bf16 [256][2048] */
     const float* router_bias;           /* fp32 [256] added to the logits before softmax, or NULL */
     const void* shared_gate_w;          /* bf16 [2048] */
+    const void* norm_w;                 /* bf16 [2048]: the layer's input RMSNorm weight, or NULL.
+                                         * With it the layer computes MoE(x_n), x_n = bf16(x /
+                                         * sqrt(mean(x^2) + 1e-6) * norm_w), and the residual forms
+                                         * add the un-normalised x (the form stacked layers need). */
 } moe_weights_t;
 
 /* Bytes of device workspace a layer with this config needs (0 if the config is refused). */
@@ -128,8 +132,9 @@ moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x
 moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, const void* x_host, int T,
                                     void* out_host, moe_stream_t stream);
 
-/* Number of kernel launches one moe_forward of T tokens enqueues (for accounting). */
-int moe_forward_launches(int T);
+/* Number of kernel launches one moe_forward of T tokens on this layer enqueues
+ * (for accounting); 0 for a NULL layer or T out of range. */
+int moe_forward_launches(const moe_layer_t* layer, int T);
 
 /* Synchronise the device, read and clear the layer's device error word.
  * MOE_OK if nothing was recorded. */
@@ -144,6 +149,15 @@ const char* moe_status_string(moe_status_t status);
 /* The calling thread's description of the last CUDA/driver failure behind an
  * MOE_ERR_CUDA status (empty if none).  Valid until the thread's next call. */
 const char* moe_last_error_detail(void);
+
+/* Kernel timing (tracing for benchmarks).  While enabled, every kernel this library
+ * launches is bracketed by two CUDA events recorded on the launch's own stream. */
+void moe_profiler_enable(int on);
+
+/* Resolve the recorded events (waits for each one), add up the duration per kernel
+ * kind and clear the record.  Fills up to `max` entries of names (static strings),
+ * total_ms and launches (any may be NULL); returns the number of kernel kinds. */
+int moe_profiler_read(const char** names, double* total_ms, long long* launches, int max);
 
 #ifdef __cplusplus
 }

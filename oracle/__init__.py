@@ -60,7 +60,8 @@ class QMat(C.Structure):
 class Weights(C.Structure):
     _fields_ = [("gate", QMat), ("up", QMat), ("down", QMat),
                 ("sh_gate", QMat), ("sh_up", QMat), ("sh_down", QMat),
-                ("router_w", C.c_void_p), ("router_bias", C.c_void_p), ("shared_gate_w", C.c_void_p)]
+                ("router_w", C.c_void_p), ("router_bias", C.c_void_p), ("shared_gate_w", C.c_void_p),
+                ("norm_w", C.c_void_p)]
 
 
 def _p(a):
@@ -81,6 +82,8 @@ def load(mutant: int = 0) -> C.CDLL:
         lib.oracle_dequant_row.argtypes = [P, P, P, C.c_int, C.c_int, P]
         lib.oracle_qmatvec.argtypes = [C.POINTER(QMat), C.c_long, C.c_int, C.c_int, C.c_int, P, P]
         lib.oracle_router_logits.argtypes = [C.POINTER(Dims), P, P, P, P]
+        lib.oracle_layer_logits.argtypes = [C.POINTER(Dims), C.POINTER(Weights), P, P]
+        lib.oracle_rmsnorm.argtypes = [C.c_int, P, P, P]
         lib.oracle_route_logits.argtypes = [C.POINTER(Dims), P, P, P, P, P, P]
         lib.oracle_expert.argtypes = [C.POINTER(Dims), C.POINTER(QMat), C.POINTER(QMat), C.POINTER(QMat),
                                       C.c_long, C.c_int, P, P]
@@ -139,13 +142,21 @@ class Oracle:
         for m in L.qmats():
             assert m.q.flags.c_contiguous and m.scales.flags.c_contiguous and m.biases.flags.c_contiguous
         return Weights(*(self._qmat(m) for m in L.qmats()), _p(L.router_w), _p(L.router_bias),
-                       _p(L.shared_gate_w))
+                       _p(L.shared_gate_w), _p(getattr(L, "norm_w", None)))
 
     def router_logits(self, L, x_row) -> np.ndarray:
+        """The layer's fp32 router logits for one token (after the layer's input norm, if any)."""
         x_row = np.ascontiguousarray(x_row, np.uint16)
         out = np.zeros(L.dims.n_experts, np.float32)
-        d = self._dims(L.dims)
-        self.lib.oracle_router_logits(C.byref(d), _p(L.router_w), _p(L.router_bias), _p(x_row), _p(out))
+        d, W = self._dims(L.dims), self._weights(L)
+        self.lib.oracle_layer_logits(C.byref(d), C.byref(W), _p(x_row), _p(out))
+        return out
+
+    def rmsnorm(self, x_row, norm_w) -> np.ndarray:
+        x_row = np.ascontiguousarray(x_row, np.uint16)
+        norm_w = np.ascontiguousarray(norm_w, np.uint16)
+        out = np.zeros_like(x_row)
+        self.lib.oracle_rmsnorm(x_row.size, _p(x_row), _p(norm_w), _p(out))
         return out
 
     def route_logits(self, dims, logits):

@@ -29,6 +29,14 @@
  *   shared   s = sigmoid(g_s . x) multiplies the shared expert's y
  *   output   o = sum_k w_k y_k + s * y_shared (+ x when the residual is asked for),
  *            rounded once to bf16 (nearest, ties to even).
+ *   norm     (stacked layers only) the layer's input is first RMS-normalised,
+ *            x_n = bf16( x / sqrt(mean(x^2) + 1e-6) * norm_w ), and the residual adds
+ *            the un-normalised x.  Without it a stack of these layers diverges: the
+ *            SwiGLU output grows with the square of its input, so the residual stream
+ *            grows doubly exponentially (it reaches inf within about 7 layers).  A norm
+ *            before the mixture-of-experts block is how the real model keeps the scale;
+ *            the pages name the 40-layer hybrid stack (p1, section "Qwen3.6's 256
+ *            experts and two layer kinds make the MLX/Lily gap") but print no formula.
  * Router logits are fp32 values (the one place where the precision decides an
  * integer result, the chosen experts); they are the exact dot product rounded
  * once to fp32.  Everything else is double.
@@ -196,6 +204,23 @@ void oracle_route_logits(const oracle_dims_t* d, const float* logits, int32_t* i
     free(taken);
 }
 
+/* ---------------------------------------------------------------- input norm */
+
+void oracle_rmsnorm(int hidden, const uint16_t* x_row, const uint16_t* norm_w, uint16_t* out) {
+    double ss = 0.0;
+    for (int i = 0; i < hidden; ++i) {
+        const double v = oracle_bf16_to_double(x_row[i]);
+        ss += v * v;
+    }
+#if ORACLE_MUTANT == 9
+    const double r = 1.0 / sqrt(ss / hidden);                  /* planted: epsilon dropped */
+#else
+    const double r = 1.0 / sqrt(ss / hidden + ORACLE_RMS_EPS);
+#endif
+    for (int i = 0; i < hidden; ++i)
+        out[i] = oracle_double_to_bf16(oracle_bf16_to_double(x_row[i]) * r * oracle_bf16_to_double(norm_w[i]));
+}
+
 /* ---------------------------------------------------------------- experts */
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
@@ -236,12 +261,15 @@ void oracle_token_forward(const oracle_dims_t* d, const oracle_weights_t* W, con
     const int H = d->hidden;
     double* x = (double*)malloc(sizeof(double) * (size_t)H);
     double* y = (double*)malloc(sizeof(double) * (size_t)H);
-    for (int i = 0; i < H; ++i) { x[i] = oracle_bf16_to_double(x_row[i]); out[i] = 0.0; }
+    uint16_t* xn_row = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+    if (W->norm_w) oracle_rmsnorm(H, x_row, W->norm_w, xn_row);
+    else memcpy(xn_row, x_row, sizeof(uint16_t) * (size_t)H);
+    for (int i = 0; i < H; ++i) { x[i] = oracle_bf16_to_double(xn_row[i]); out[i] = 0.0; }
     for (int k = 0; k < d->top_k; ++k) {
         oracle_expert(d, &W->gate, &W->up, &W->down, experts[k], d->inter, x, y);
         for (int i = 0; i < H; ++i) out[i] += wts[k] * y[i];
     }
-    double s = oracle_shared_gate(d, W->shared_gate_w, x_row);
+    double s = oracle_shared_gate(d, W->shared_gate_w, xn_row);
     oracle_expert(d, &W->sh_gate, &W->sh_up, &W->sh_down, 0, d->shared_inter, x, y);
 #if ORACLE_MUTANT != 8
     for (int i = 0; i < H; ++i) out[i] += s * y[i];   /* (mutant 8 drops the shared expert) */
@@ -249,12 +277,29 @@ void oracle_token_forward(const oracle_dims_t* d, const oracle_weights_t* W, con
     (void)s;
 #endif
     if (residual)
-        for (int i = 0; i < H; ++i) out[i] += x[i];
+#if ORACLE_MUTANT == 10
+        for (int i = 0; i < H; ++i) out[i] += x[i];                              /* planted: normalised input */
+#else
+        for (int i = 0; i < H; ++i) out[i] += oracle_bf16_to_double(x_row[i]);   /* the un-normalised input */
+#endif
     free(x);
     free(y);
+    free(xn_row);
 }
 
 /* ---------------------------------------------------------------- whole layer */
+
+/* The layer's router logits for one token: on the normalised input when the layer has a norm. */
+void oracle_layer_logits(const oracle_dims_t* d, const oracle_weights_t* W, const uint16_t* x_row, float* l) {
+    if (W->norm_w) {
+        uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)d->hidden);
+        oracle_rmsnorm(d->hidden, x_row, W->norm_w, xn);
+        oracle_router_logits(d, W->router_w, W->router_bias, xn, l);
+        free(xn);
+    } else {
+        oracle_router_logits(d, W->router_w, W->router_bias, x_row, l);
+    }
+}
 
 void oracle_route(const oracle_dims_t* d, const oracle_weights_t* W, const uint16_t* x, int T, int nthreads,
                   int32_t* idx, double* wts, double* gap, int32_t* counts, int32_t* offsets, int32_t* perm) {
@@ -265,7 +310,7 @@ void oracle_route(const oracle_dims_t* d, const oracle_weights_t* W, const uint1
 #endif
     for (int t = 0; t < T; ++t) {
         float* l = (float*)malloc(sizeof(float) * (size_t)E);
-        oracle_router_logits(d, W->router_w, W->router_bias, x + (size_t)t * d->hidden, l);
+        oracle_layer_logits(d, W, x + (size_t)t * d->hidden, l);
         oracle_route_logits(d, l, idx + (size_t)t * K, wts + (size_t)t * K, gap ? gap + t : NULL, NULL, NULL);
         free(l);
     }
@@ -305,7 +350,7 @@ void oracle_layer_forward(const oracle_dims_t* d, const oracle_weights_t* W, con
         double* tw = (double*)malloc(sizeof(double) * (size_t)K);
         double* o = (double*)malloc(sizeof(double) * (size_t)H);
         double tg;
-        oracle_router_logits(d, W->router_w, W->router_bias, x + (size_t)t * H, l);
+        oracle_layer_logits(d, W, x + (size_t)t * H, l);
         oracle_route_logits(d, l, ti, tw, &tg, NULL, NULL);
         oracle_token_forward(d, W, x + (size_t)t * H, ti, tw, residual, o);
         for (int i = 0; i < H; ++i) out[(size_t)t * H + i] = oracle_double_to_bf16(o[i]);
@@ -328,7 +373,7 @@ void oracle_token_forward_choice(const oracle_dims_t* d, const oracle_weights_t*
     double* p = (double*)malloc(sizeof(double) * (size_t)E);
     double* w = (double*)malloc(sizeof(double) * (size_t)K);
     double* o = (double*)malloc(sizeof(double) * (size_t)H);
-    oracle_router_logits(d, W->router_w, W->router_bias, x_row, l);
+    oracle_layer_logits(d, W, x_row, l);
     double mx = -INFINITY, z = 0.0, sel = 0.0;
     for (int e = 0; e < E; ++e) if ((double)l[e] > mx) mx = l[e];
     for (int e = 0; e < E; ++e) { p[e] = exp((double)l[e] - mx); z += p[e]; }

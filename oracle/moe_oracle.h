@@ -29,7 +29,10 @@ typedef struct {
     const uint16_t* router_w;              /* bf16 [E][hidden] */
     const float* router_bias;              /* fp32 [E] or NULL */
     const uint16_t* shared_gate_w;         /* bf16 [hidden] */
+    const uint16_t* norm_w;                /* bf16 [hidden]: RMSNorm of the layer input, or NULL */
 } oracle_weights_t;
+
+#define ORACLE_RMS_EPS 1e-6
 
 double oracle_bf16_to_double(uint16_t b);
 uint16_t oracle_double_to_bf16(double v);
@@ -44,6 +47,8 @@ void oracle_route_logits(const oracle_dims_t* d, const float* logits, int32_t* i
                          double* gap, double* p_sorted, int32_t* order);
 void oracle_expert(const oracle_dims_t* d, const oracle_qmat_t* gate, const oracle_qmat_t* up,
                    const oracle_qmat_t* down, long e, int inter, const double* x, double* y);
+void oracle_layer_logits(const oracle_dims_t* d, const oracle_weights_t* W, const uint16_t* x_row, float* l);
+void oracle_rmsnorm(int hidden, const uint16_t* x_row, const uint16_t* norm_w, uint16_t* out);
 double oracle_shared_gate(const oracle_dims_t* d, const uint16_t* shared_gate_w, const uint16_t* x_row);
 void oracle_token_forward(const oracle_dims_t* d, const oracle_weights_t* W, const uint16_t* x_row,
                           const int32_t* experts, const double* wts, int residual, double* out);

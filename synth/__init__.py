@@ -42,7 +42,7 @@ import numpy as np
 __all__ = [
     "Dims", "QMat", "LayerWeights", "QWEN36_DIMS",
     "bf16_bits_from_f32", "f32_from_bf16_bits",
-    "make_layer", "make_x", "make_skew_bias", "make_stack",
+    "make_layer", "make_x", "make_skew_bias", "make_stack", "stack_layer",
 ]
 
 # stream ids (second element of spawn_key)
@@ -95,6 +95,7 @@ class LayerWeights:
     router_w: np.ndarray                    # uint16 bf16 bits [E, hidden]
     shared_gate_w: np.ndarray               # uint16 bf16 bits [hidden]
     router_bias: np.ndarray | None = None   # float32 [E] or None
+    norm_w: np.ndarray | None = None        # uint16 bf16 bits [hidden]: input RMSNorm, or None
     seed: int = 0
     layer: int = 0
     extra: dict = field(default_factory=dict)
@@ -172,9 +173,22 @@ def make_layer(seed: int = 0, layer: int = 0, dims: Dims = QWEN36_DIMS, skew: bo
     return LayerWeights(d, *mats, router_w=rw, shared_gate_w=gs, router_bias=bias, seed=seed, layer=layer)
 
 
+BF16_ONE = 0x3F80
+
+
+def stack_layer(l: int, dims: Dims = QWEN36_DIMS, threads: int | None = None) -> LayerWeights:
+    """Layer l of a stack: seed l, with an input RMSNorm of weight 1 (see ``make_stack``)."""
+    L = make_layer(seed=l, layer=l, dims=dims, threads=threads)
+    L.norm_w = np.full(dims.hidden, BF16_ONE, np.uint16)
+    return L
+
+
 def make_stack(n_layers: int, dims: Dims = QWEN36_DIMS, threads: int | None = None):
-    """A stack of independently seeded layers: layer l uses seed l."""
-    return [make_layer(seed=l, layer=l, dims=dims, threads=threads) for l in range(n_layers)]
+    """A stack of independently seeded layers: layer l uses seed l, and every layer
+    RMS-normalises its input (weight 1) before the mixture of experts; the residual adds
+    the un-normalised input.  Without the norm such a stack diverges within a few
+    layers (the SwiGLU output grows with the square of its input)."""
+    return [stack_layer(l, dims, threads) for l in range(n_layers)]
 
 
 def make_x(seed: int, T: int, hidden: int = 2048) -> np.ndarray:

@@ -156,7 +156,7 @@ def test_deterministic(host0, dev0):
 
 
 def test_short_stack(oracle, lib):
-    hosts = [synth.make_layer(seed=l, layer=l) for l in range(3)]
+    hosts = [synth.stack_layer(l) for l in range(3)]
     ws = lib.new_workspace(64)
     layers = [lib.MoELayer(lib.DeviceWeights(h), max_tokens=64, workspace=ws) for h in hosts]
     stack = lib.MoEStack(layers)

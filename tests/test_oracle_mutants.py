@@ -21,6 +21,8 @@ MUTANTS = {
     6: "gate and up swapped in SwiGLU",
     7: "matrix rows shifted (transposed operand)",
     8: "shared expert dropped",
+    9: "RMSNorm epsilon dropped",
+    10: "residual adds the normalised input",
 }
 
 

@@ -322,11 +322,48 @@ def check_choice_matches_forward(o):
         assert np.allclose(w, r["w"][t], rtol=1e-14)
 
 
+def check_rmsnorm_closed_forms(o):
+    H = 64
+    ones = np.full(H, BF16_ONE, np.uint16)
+    # constant input c: mean square c^2, so x_n = c / sqrt(c^2 + 1e-6) -> 1 (and -> w)
+    two = np.full(H, 0x4000, np.uint16)                     # 2.0
+    assert np.all(o.rmsnorm(two, ones) == BF16_ONE)
+    assert np.all(o.rmsnorm(two, np.full(H, 0x4040, np.uint16)) == 0x4040)   # weight 3 -> 3
+    # a single non-zero a: x_n = a / sqrt(a^2 / H + eps) ~ sqrt(H) = 8
+    e0 = np.zeros(H, np.uint16)
+    e0[0] = BF16_ONE
+    xn = o.rmsnorm(e0, ones)
+    assert xn[0] == 0x4100 and np.all(xn[1:] == 0)
+    # tiny input: the 1e-6 inside the root matters (2^-10 / sqrt(2^-20 + 1e-6) = 0.6996...)
+    tiny = np.full(H, 0x3A80, np.uint16)                    # 2^-10
+    want = 2.0**-10 / np.sqrt(2.0**-20 + 1e-6)
+    got = bf16_value(o.rmsnorm(tiny, ones))
+    assert np.all(np.abs(got - want) <= 2.0**-8 * want)
+
+
+def check_identity_experts_with_norm(o):
+    """Stacked-layer form: out = x + layer(rmsnorm(x)), identity experts, zero router."""
+    d = TINY
+    mult = [(e % 15) + 1 for e in range(d.n_experts)]
+    L = identity_layer(d, mult)
+    L.norm_w = np.full(d.hidden, BF16_ONE, np.uint16)
+    x = synth.make_x(13, 5, d.hidden)
+    r = o.forward(L, x, residual=True, nthreads=1)
+    xv = bf16_value(x)
+    xn = xv / np.sqrt(np.mean(xv * xv, axis=1, keepdims=True) + 1e-6)
+    xn = bf16_value(synth.bf16_bits_from_f32(xn.astype(np.float32)))
+    coef = sum(mult[:d.top_k]) / d.top_k + 0.5
+    ref = xv.copy()
+    ref[:, :d.inter] += coef * silu(xn[:, :d.inter]) * xn[:, :d.inter]
+    assert np.allclose(bf16_value(r["out"]), ref, rtol=2.0**-7, atol=2.0**-7)
+
+
 ALL_CHECKS = [
     check_unpack_hand_built, check_dequant_exact, check_bf16_rounding, check_router_logits_exact,
     check_router_bruteforce, check_router_ties, check_route_tables, check_identity_experts_uniform,
     check_identity_experts_biased, check_shared_gate_closed_form, check_permutation_invariance,
-    check_dense_numpy, check_choice_matches_forward,
+    check_dense_numpy, check_choice_matches_forward, check_rmsnorm_closed_forms,
+    check_identity_experts_with_norm,
 ]
 
 
