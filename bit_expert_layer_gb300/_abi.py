@@ -84,6 +84,8 @@ def lib() -> C.CDLL:
         L.moe_status_string.restype = C.c_char_p
         L.moe_last_error_detail.argtypes = []
         L.moe_last_error_detail.restype = C.c_char_p
+        L.moe_decode_forward_static.argtypes = [C.POINTER(MoeWeights), P, I, P, I, P]
+        L.moe_decode_forward_static.restype = S
         L.moe_profiler_enable.argtypes = [I]
         L.moe_profiler_enable.restype = None
         L.moe_profiler_read.argtypes = [P, P, P, I]
@@ -156,6 +158,12 @@ def moe_layer_destroy(layer: int) -> None:
 
 def moe_status_string(status: int) -> str:
     return lib().moe_status_string(status).decode()
+
+
+def moe_decode_forward_static(weights: MoeWeights, x: int, T: int, out: int, residual: bool = False,
+                              stream: int = 0) -> None:
+    _check(lib().moe_decode_forward_static(C.byref(weights), x, T, out, 1 if residual else 0, stream or None),
+           "moe_decode_forward_static")
 
 
 def moe_profiler_enable(on: bool) -> None:

@@ -1,0 +1,166 @@
+// noalloc.cu -- moe_decode_forward_static: the decode forward (T <= 8 tokens) for
+// callers that cannot allocate device memory.
+//
+// Who needs it: a host that embeds this library as a plug-in and owns every byte of
+// device memory itself (it hands out no allocation hook and no workspace), and
+// latency-critical decode loops that must never reach cudaMalloc, which can
+// synchronise the whole device.  Such a caller cannot provide the workspace that
+// moe_layer_create requires, so this entry point keeps the decode path's scratch in one
+// fixed-size array in device memory that the library owns for the life of the process.
+//
+// The scratch is the file-scope array below.  On the host its name is only a stand-in
+// symbol, not a device address, so before the first launch on a device this file asks
+// the runtime for the array's device address (cudaGetSymbolAddress, once per device,
+// with that device current) and passes that address to the kernels.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "moe_layer.h"
+
+namespace moe {
+
+namespace {
+
+// Layout of the static scratch for up to DEC_MAX_T tokens.
+struct StaticLayout {
+  size_t err, counter, logits, topk_idx, topk_w, counts, offsets, perm, act_expert, act_w, n_active, hw, xn,
+      total;
+};
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+constexpr StaticLayout make_layout() {
+  StaticLayout L{};
+  size_t o = 0;
+  L.err = o;        o = align256(o + 4);
+  L.counter = o;    o = align256(o + 4);
+  L.logits = o;     o = align256(o + DEC_MAX_T * (NEXP + 1) * 4);
+  L.topk_idx = o;   o = align256(o + DEC_MAX_T * TOPK * 4);
+  L.topk_w = o;     o = align256(o + DEC_MAX_T * TOPK * 4);
+  L.counts = o;     o = align256(o + (NEXP + 1) * 4);
+  L.offsets = o;    o = align256(o + (NEXP + 2) * 4);
+  L.perm = o;       o = align256(o + DEC_MAX_T * TOPK * 4);
+  L.act_expert = o; o = align256(o + DEC_MAX_ACTIVE * 4);
+  L.act_w = o;      o = align256(o + DEC_MAX_ACTIVE * DEC_MAX_T * 4);
+  L.n_active = o;   o = align256(o + 4);
+  L.hw = o;         o = align256(o + static_cast<size_t>(DEC_MAX_ACTIVE) * DEC_MAX_T * INTER * 2);
+  L.xn = o;         o = align256(o + static_cast<size_t>(DEC_MAX_T) * HID * 2);
+  L.total = o;
+  return L;
+}
+
+constexpr StaticLayout kLayout = make_layout();
+constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB, held by every device that loads the library
+static_assert(kLayout.total <= kStaticScratchBytes, "static scratch too small for the decode path");
+
+}  // namespace
+
+// The decode path's scratch.  Every call of moe_decode_forward_static on a device uses
+// this same array, which keeps the last call's contents between calls.
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_addr_mutex;
+unsigned char* g_addr[kMaxDevices] = {};
+thread_local char g_static_detail[200] = "";
+
+// The array's device address on the current device, looked up on the first call there.
+cudaError_t scratch_address(unsigned char** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_addr_mutex);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_addr[dev];
+  return cudaSuccess;
+}
+
+bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_decode_forward_static(const moe_weights_t* w, const void* x, int T, void* out,
+                                                  int residual, moe_stream_t stream) {
+  if (!w || !x || !out) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > DEC_MAX_T) {
+    snprintf(g_static_detail, sizeof g_static_detail,
+             "moe_decode_forward_static: T=%d is outside 1..%d, the limit of its static scratch", T, DEC_MAX_T);
+    fprintf(stderr, "%s\n", g_static_detail);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const moe_qmat_t* mats[6] = {&w->gate, &w->up, &w->down, &w->sh_gate, &w->sh_up, &w->sh_down};
+  for (const moe_qmat_t* m : mats)
+    if (!ok16(m->q) || !ok16(m->scales) || !ok16(m->biases)) return MOE_ERR_ALIGNMENT;
+  if (!ok16(w->router_w) || !ok16(w->shared_gate_w) || !ok16(x) || !ok16(out) ||
+      (w->router_bias && !ok16(w->router_bias)) || (w->norm_w && !ok16(w->norm_w)))
+    return MOE_ERR_ALIGNMENT;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), oa = reinterpret_cast<uintptr_t>(out);
+  const size_t bytes = static_cast<size_t>(T) * HID * 2;
+  if (x != out && xa < oa + bytes && oa < xa + bytes) return MOE_ERR_INVALID_ARG;
+  if (x == out && !residual) return MOE_ERR_INVALID_ARG;
+
+  unsigned char* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the error word and the router's arrival ticket must start at zero on every call
+  if (cudaMemsetAsync(base, 0, kLayout.logits, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  const __nv_bfloat16* xin = static_cast<const __nv_bfloat16*>(x);
+  if (w->norm_w) {
+    __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(base + kLayout.xn);
+    if (launch_rmsnorm(xin, static_cast<const __nv_bfloat16*>(w->norm_w), xn, T, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    xin = xn;
+  }
+  DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.x = xin;
+  p.T = T;
+  p.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
+  p.router_bias = w->router_bias;
+  p.shared_gate_w = static_cast<const __nv_bfloat16*>(w->shared_gate_w);
+  p.logits = reinterpret_cast<float*>(base + kLayout.logits);
+  p.counter = reinterpret_cast<unsigned int*>(base + kLayout.counter);
+  p.topk_idx = reinterpret_cast<int*>(base + kLayout.topk_idx);
+  p.topk_w = reinterpret_cast<float*>(base + kLayout.topk_w);
+  p.counts = reinterpret_cast<int*>(base + kLayout.counts);
+  p.offsets = reinterpret_cast<int*>(base + kLayout.offsets);
+  p.perm = reinterpret_cast<int*>(base + kLayout.perm);
+  p.act_expert = reinterpret_cast<int*>(base + kLayout.act_expert);
+  p.act_w = reinterpret_cast<float*>(base + kLayout.act_w);
+  p.n_active = reinterpret_cast<int*>(base + kLayout.n_active);
+  p.hw = reinterpret_cast<__nv_bfloat16*>(base + kLayout.hw);
+  auto Q = [](const moe_qmat_t& m, const uint32_t*& q, const uint16_t*& sc, const uint16_t*& bi) {
+    q = static_cast<const uint32_t*>(m.q);
+    sc = static_cast<const uint16_t*>(m.scales);
+    bi = static_cast<const uint16_t*>(m.biases);
+  };
+  Q(w->gate, p.gq, p.gs, p.gb);
+  Q(w->up, p.uq, p.us, p.ub);
+  Q(w->down, p.dq, p.ds, p.db);
+  Q(w->sh_gate, p.sgq, p.sgs, p.sgb);
+  Q(w->sh_up, p.suq, p.sus, p.sub);
+  Q(w->sh_down, p.sdq, p.sds, p.sdb);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.x_resid = static_cast<const __nv_bfloat16*>(x);
+  p.residual = residual ? 1 : 0;
+  p.err = reinterpret_cast<unsigned int*>(base + kLayout.err);
+  if (launch_decode_router(p, s) != cudaSuccess || launch_decode_gateup(p, s) != cudaSuccess ||
+      launch_decode_down(p, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}

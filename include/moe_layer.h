@@ -132,6 +132,27 @@ moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x
 moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, const void* x_host, int T,
                                     void* out_host, moe_stream_t stream);
 
+/* The decode forward (1 <= T <= 8) for callers that cannot allocate device memory:
+ * a plug-in whose host application owns all device memory and offers no allocator or
+ * workspace, or a latency-critical decode loop that must never reach cudaMalloc (which
+ * can synchronise the device).  No layer object and no workspace: the scratch of the
+ * decode kernels lives in a fixed 1 MiB array of device memory inside the library,
+ * held by every device that loads it until the process exits.  Nothing is allocated
+ * (no cudaMalloc, no cudaFree, no allocating library routine).  The pages describe no
+ * such entry point; it has no counterpart there.
+ *   weights  as for moe_layer_create (device pointers, borrowed for the call)
+ *   x, out   bf16 [T][2048] device pointers; out == x is allowed only with residual
+ *   residual 0: out = layer(x); 1: out = x + layer(x) (with norm_w: x + MoE(norm(x)))
+ * T above 8 (the array's limit) or below 1 returns MOE_ERR_INVALID_ARG and prints why.
+ * The first call on a device looks up the array's device address there (make that
+ * first call before any stream capture).  Every call on a device shares the one
+ * array and leaves its contents behind; the parts that must start at zero are
+ * cleared by each call on its stream.  Calls that overlap on the GPU (other streams,
+ * other threads) race on the array and corrupt each other: serialise them.  Device-side
+ * error bits of this entry stay in the array and are not reported. */
+moe_status_t moe_decode_forward_static(const moe_weights_t* weights, const void* x, int T, void* out,
+                                       int residual, moe_stream_t stream);
+
 /* Number of kernel launches one moe_forward of T tokens on this layer enqueues
  * (for accounting); 0 for a NULL layer or T out of range. */
 int moe_forward_launches(const moe_layer_t* layer, int T);
