@@ -50,6 +50,7 @@ LAYER_BYTES = 455_806_976
 WORKLOADS = {
     "stack40-T16384+T1": dict(layers=40, T_prefill=16384, T_decode=1, skew=False),
     "layer-T4096-skew": dict(layers=1, T_prefill=4096, T_decode=0, skew=True),
+    "layer-T4096": dict(layers=1, T_prefill=4096, T_decode=0, skew=False),
     "layer-T512": dict(layers=1, T_prefill=512, T_decode=0, skew=False),
     "layer-T32": dict(layers=1, T_prefill=32, T_decode=0, skew=False),
     "decode-T1": dict(layers=40, T_prefill=0, T_decode=1, skew=False),

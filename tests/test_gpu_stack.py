@@ -52,6 +52,16 @@ def test_layer_with_input_norm(oracle, lib, T):
     check_output(oracle, L, x_np, to_host(out), residual=True, alt=alt)
 
 
+def stack_tolerance(scale: float, n_layers: int) -> float:
+    """Output bound after n chained layers.  Each layer's output is the layer tolerance
+    (1e-2 of the scale) away at most, and the residual stream is rounded to bf16 once per
+    layer: where the two sides' unrounded sums straddle a rounding boundary they land one
+    bf16 unit apart, and such one-unit steps add up like a random walk over the layers,
+    about sqrt(n) units of the largest magnitude."""
+    ulp = 2.0 ** (np.floor(np.log2(scale)) - 7)
+    return 1e-2 * scale + np.sqrt(n_layers) * ulp
+
+
 def _stack_chain(oracle, hosts, x_np):
     cur = x_np.copy()
     keep = np.ones(x_np.shape[0], bool)
@@ -87,7 +97,7 @@ def test_full_stack_40_layers(oracle, lib):
     assert keep.sum() >= 12, keep.sum()
     ref_v = bf16_to_f64(ref[keep])
     err = np.max(np.abs(bf16_to_f64(got[sample][keep]) - ref_v))
-    assert err <= 1e-2 * np.max(np.abs(ref_v)), (err, np.max(np.abs(ref_v)))
+    assert err <= stack_tolerance(np.max(np.abs(ref_v)), len(hosts)), (err, np.max(np.abs(ref_v)))
     print(f"stack prefill: {int(keep.sum())}/{len(sample)} sampled tokens compared, max err {err:.3e}, "
           f"scale {np.max(np.abs(ref_v)):.3e}")
 
@@ -100,7 +110,7 @@ def test_full_stack_40_layers(oracle, lib):
     ref, keep = _stack_chain(oracle, hosts, xd_np)
     if keep[0]:
         r_v, g_v = bf16_to_f64(ref[0]), bf16_to_f64(to_host(xd)[0])
-        assert np.max(np.abs(g_v - r_v)) <= 1e-2 * np.max(np.abs(r_v))
+        assert np.max(np.abs(g_v - r_v)) <= stack_tolerance(np.max(np.abs(r_v)), len(hosts))
 
     # the first layer alone, routing tables exact on the full T
     r = layers[0].route(to_dev(x_np))
