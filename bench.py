@@ -51,6 +51,9 @@ WORKLOADS = {
     "stack40-T16384+T1": dict(layers=40, T_prefill=16384, T_decode=1, skew=False),
     "layer-T4096-skew": dict(layers=1, T_prefill=4096, T_decode=0, skew=True),
     "layer-T4096": dict(layers=1, T_prefill=4096, T_decode=0, skew=False),
+    "layer-T16384": dict(layers=1, T_prefill=16384, T_decode=0, skew=False),
+    "layer-decode-T1": dict(layers=1, T_prefill=0, T_decode=1, skew=False),
+    "layer-decode-T8": dict(layers=1, T_prefill=0, T_decode=8, skew=False),
     "layer-T512": dict(layers=1, T_prefill=512, T_decode=0, skew=False),
     "layer-T32": dict(layers=1, T_prefill=32, T_decode=0, skew=False),
     "decode-T1": dict(layers=40, T_prefill=0, T_decode=1, skew=False),

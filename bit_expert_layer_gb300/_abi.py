@@ -86,6 +86,8 @@ def lib() -> C.CDLL:
         L.moe_last_error_detail.restype = C.c_char_p
         L.moe_decode_forward_static.argtypes = [C.POINTER(MoeWeights), P, I, P, I, P]
         L.moe_decode_forward_static.restype = S
+        L.moe_pipeline_counters.argtypes = [P, P]
+        L.moe_pipeline_counters.restype = S
         L.moe_profiler_enable.argtypes = [I]
         L.moe_profiler_enable.restype = None
         L.moe_profiler_read.argtypes = [P, P, P, I]
@@ -164,6 +166,18 @@ def moe_decode_forward_static(weights: MoeWeights, x: int, T: int, out: int, res
                               stream: int = 0) -> None:
     _check(lib().moe_decode_forward_static(C.byref(weights), x, T, out, 1 if residual else 0, stream or None),
            "moe_decode_forward_static")
+
+
+PIPE_SLOTS = ["mma_wait_acc_drain", "mma_wait_dequant", "mma_wait_tma", "mma_total", "producer_wait_stage",
+              "producer_total", "dequant_wait_tma", "dequant_total", "epilogue_wait_acc", "epilogue_total",
+              "tiles"]
+
+
+def moe_pipeline_counters(layer: int) -> dict:
+    """{'gateup': {slot: cycles}, 'down': {...}} since the last read (MOE_PIPE_PROF=1)."""
+    buf = (C.c_ulonglong * 32)()
+    _check(lib().moe_pipeline_counters(layer, C.cast(buf, C.c_void_p)), "moe_pipeline_counters")
+    return {k: {n: int(buf[16 * j + i]) for i, n in enumerate(PIPE_SLOTS)} for j, k in enumerate(("gateup", "down"))}
 
 
 def moe_profiler_enable(on: bool) -> None:

@@ -45,14 +45,19 @@ constexpr int GX_P_BYTES = GX_BM * 32;              //  4 KB packed 4-bit tile (
 // gate/up: two A tiles + X + two packed tiles per stage
 constexpr int GU_STAGES = 3;
 constexpr int GU_STAGE_BYTES = 2 * GX_A_BYTES + GX_X_BYTES + 2 * GX_P_BYTES;
-constexpr int GU_SMEM = GU_STAGES * GU_STAGE_BYTES + 1024 + 512;
-constexpr int GU_THREADS = 320;                     // producer, MMA, 8 dequant/epilogue warps
+constexpr int GX_TAB_BYTES = 3 * (NEXP + 2) * 4 + 128;   // tile tables staged in shared memory
+// + alignment slack, barriers (256 B), tile tables
+constexpr int GU_SMEM = GU_STAGES * GU_STAGE_BYTES + 1024 + 512 + GX_TAB_BYTES;
+constexpr int GU_THREADS = 448;                     // producer, MMA, 8 dequant warps, 4 epilogue warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
 constexpr int DN_STAGES = 4;
 constexpr int DN_STAGE_BYTES = GX_A_BYTES + GX_X_BYTES + GX_P_BYTES;
-constexpr int DN_SMEM = DN_STAGES * DN_STAGE_BYTES + 1024 + 512;
-constexpr int DN_THREADS = 320;                     // producer, MMA, 4 dequant, 4 epilogue warps
+// + barriers, and per epilogue warp a 256-row table of (destination row, weight)
+// + alignment slack, barriers (256 B), row tables (2 KB), 32-row staging (8 KB), tile tables
+constexpr int DN_SMEM = DN_STAGES * DN_STAGE_BYTES + 1024 + 256 + GX_BN * 8 + 32 * GX_BM * 2 + GX_TAB_BYTES;
+static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
+constexpr int DN_THREADS = 448;                     // producer, MMA, 8 dequant, 4 epilogue warps
 constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
 
 // scatter: one CTA per router block of 128 tokens (1024 slots)

@@ -1,0 +1,310 @@
+// down.cu -- the grouped down GEMM of the prefill path: y[row_dst] = W_down h' for every
+// permuted row (8 routed slots and 1 shared row per token), where h' already carries the
+// row's weight (applied by the gate/up epilogue), with the 4-bit weights dequantised
+// inside the kernel (Lily restores the 4-bit weights inside its
+// grouped GEMM: aimanavo.com, "Why is Perplexity's local AI Lily faster than MLX",
+// section "Prefill and decode are not treated as the same job").
+//
+// A tile is 128 output features (M) x up to 256 permuted rows (N); K = 512 is only 8
+// steps of 64, so one tile's MMAs take ~2 us and the dequant and epilogue have to keep
+// pace with that.  Warp roles (14 warps):
+//   warp 0      TMA producer (packed 4-bit tile + activation rows h)
+//   warp 1      TMEM allocator and MMA issuer (double-buffered 128 x 256 accumulator)
+//   warps 2-9   dequant: two threads per weight row, four packed words each
+//   warps 10-13 epilogue: per 32-row chunk, round to bf16, transpose through shared
+//               memory and write each destination row's 128 features (256 B) with
+//               16-byte stores
+#include "common.cuh"
+#include "gemm_common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+constexpr int DN_A = 0;                              // dequantised weight tile
+constexpr int DN_X = GX_A_BYTES;                     // activation rows
+constexpr int DN_P = GX_A_BYTES + GX_X_BYTES;        // packed 4-bit tile
+constexpr int EPI_BAR = 1;                           // named barrier of the epilogue warps
+constexpr int STG_ROW = GX_BM * 2;                   // bytes of one staged row (128 bf16)
+
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(EPI_BAR), "n"(128) : "memory");
+}
+}  // namespace
+
+__global__ void __launch_bounds__(DN_THREADS, 1)
+    down_kernel(const __grid_constant__ CUtensorMap tm_qd, const __grid_constant__ CUtensorMap tm_sqd,
+                const __grid_constant__ CUtensorMap tm_h, DownParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* misc = smem + DN_STAGES * DN_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                       // 256 B
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
+  int* md_dst = reinterpret_cast<int*>(misc + 256);                          // [256] destination rows
+  uint8_t* stg = misc + 256 + GX_BN * 8;                                     // [32][128] bf16 staging
+  int* s_tiles = reinterpret_cast<int*>(stg + 32 * STG_ROW);
+  int* s_off = s_tiles + (NEXP + 2);
+  int* s_cnt = s_off + (NEXP + 2);
+  stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  // full 0..3, afull 4..7, empty 8..11, accf 12..13, acce 14..15, drain 16
+#define FULL(s) (bar0 + 8u * (s))
+#define AFULL(s) (bar0 + 8u * (4 + (s)))
+#define EMPTY(s) (bar0 + 8u * (8 + (s)))
+#define ACCF(b) (bar0 + 8u * (12 + (b)))
+#define ACCE(b) (bar0 + 8u * (14 + (b)))
+  const uint32_t DRAIN = bar0 + 8u * 16;
+
+  if (tid == 0) {
+    for (int s = 0; s < DN_STAGES; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(AFULL(s), 256);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(ACCF(b), 1);
+      mbar_init(ACCE(b), 128);
+    }
+    mbar_init(DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int total = s_tiles[NEXP + 1];
+  constexpr int NKB = INTER / 64;   // 8
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const bool pp = p.pipe != nullptr;
+      unsigned long long pc[1] = {0};
+      const unsigned long long t_role = pp ? clock64() : 0;
+      tma_prefetch_desc(&tm_qd);
+      tma_prefetch_desc(&tm_h);
+      uint32_t it = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+        if (!ti.ok) { atomicOr(p.err, ERRBIT_BOUNDS); continue; }
+        const bool sh = ti.e == SHARED_E;
+        const CUtensorMap* mq = sh ? &tm_sqd : &tm_qd;
+        const int wrow = (sh ? 0 : ti.e * HID) + ti.mb * GX_BM;
+        const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
+        const uint32_t bytes = GX_P_BYTES + nbox * GX_XBOX * 128;
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % DN_STAGES;
+          const uint32_t ph = (it / DN_STAGES) & 1;
+          if (!mbar_wait_t(EMPTY(s), ph ^ 1, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
+          const uint32_t st = smem_u32(smem + s * DN_STAGE_BYTES);
+          mbar_arrive_expect_tx(FULL(s), bytes);
+          tma_load_2d(st + DN_P, mq, FULL(s), kb * 8, wrow);
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d(st + DN_X + j * GX_XBOX * 128, &tm_h, FULL(s), kb * 64, ti.row0 + j * GX_XBOX);
+        }
+      }
+      if (!alive) {
+        for (uint32_t i = (it > DN_STAGES ? it - DN_STAGES : 0); i < it; ++i)
+          drain_wait(FULL(i % DN_STAGES), (i / DN_STAGES) & 1);
+      }
+      if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const bool pp = p.pipe != nullptr;
+      unsigned long long pc[3] = {0, 0, 0};
+      const unsigned long long t_role = pp ? clock64() : 0;
+      uint32_t it = 0, tc = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+        if (!ti.ok) continue;
+        const int N = max(16, (ti.n_rows + 15) & ~15);
+        const uint32_t idesc = idesc_bf16(128, N);
+        const int buf = tc & 1;
+        if (!mbar_wait_t(ACCE(buf), ((tc >> 1) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * 256;
+        bool alive = true;
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % DN_STAGES;
+          const uint32_t ph = (it / DN_STAGES) & 1;
+          if (!mbar_wait_t(AFULL(s), ph, p.err, abort_flag, pc[1], pp) ||
+              !mbar_wait_t(FULL(s), ph, p.err, abort_flag, pc[2], pp)) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * DN_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, sdesc_sw128(st + DN_A + kk * 32), sdesc_sw128(st + DN_X + kk * 32), idesc,
+                      (kb | kk) != 0);
+          umma_commit(EMPTY(s));
+        }
+        if (!alive) break;
+        umma_commit(ACCF(buf));
+        ++tc;
+      }
+      umma_commit(DRAIN);
+      if (pp) {
+        pipe_flush(p.pipe, 0, pc, 3, clock64() - t_role, 3);
+        atomicAdd(p.pipe + 10, static_cast<unsigned long long>(tc));
+      }
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------ dequant (8 warps, 2 threads per row)
+    const int dt = tid - 64;       // 0..255
+    const int r = dt & 127;        // row inside the tile
+    const int hw = dt >> 7;        // which four of the row's eight packed words
+    const bool pp = p.pipe != nullptr;
+    unsigned long long pc[1] = {0};
+    const unsigned long long t_role = pp ? clock64() : 0;
+    uint32_t it = 0;
+    bool alive = true;
+    // a row's 8 scales and 8 biases (one per K step) are loaded one tile ahead
+    TileInfo ti;
+    ti.ok = false;
+    uint4 nsv = make_uint4(0, 0, 0, 0), nbv = nsv;
+    auto load_next = [&](int t) {
+      if (t >= total) return;
+      ti = tile_info(s_tiles, s_off, s_cnt, t, DN_MBLK, p.T);
+      if (!ti.ok) return;
+      const bool sh = ti.e == SHARED_E;
+      const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + r)
+                             : static_cast<size_t>(ti.e) * HID + ti.mb * GX_BM + r;
+      nsv = ldg_nc_v4((sh ? p.sd_scales : p.d_scales) + srow * (INTER / GROUP));
+      nbv = ldg_nc_v4((sh ? p.sd_biases : p.d_biases) + srow * (INTER / GROUP));
+    };
+    load_next(blockIdx.x);
+    for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+      const bool cur_ok = ti.ok;
+      const uint4 sv = nsv, bv = nbv;
+      load_next(tile + gridDim.x);
+      if (!cur_ok) continue;
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        const int s = it % DN_STAGES;
+        const uint32_t ph = (it / DN_STAGES) & 1;
+        if (!mbar_wait_t(FULL(s), ph, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
+        ++it;
+        const __nv_bfloat162 ms = bf2((kb & 1) ? (sw[kb >> 1] >> 16) : sw[kb >> 1]);
+        const __nv_bfloat162 mbv = bf2((kb & 1) ? (bw[kb >> 1] >> 16) : bw[kb >> 1]);
+        uint8_t* st = smem + s * DN_STAGE_BYTES;
+        const uint4 w = *reinterpret_cast<const uint4*>(st + DN_P + r * 32 + hw * 16);
+        uint8_t* A = st + DN_A;
+        st_shared_v4(A + sw128_off(r, 4 * hw + 0), dequant8(w.x, ms, mbv));
+        st_shared_v4(A + sw128_off(r, 4 * hw + 1), dequant8(w.y, ms, mbv));
+        st_shared_v4(A + sw128_off(r, 4 * hw + 2), dequant8(w.z, ms, mbv));
+        st_shared_v4(A + sw128_off(r, 4 * hw + 3), dequant8(w.w, ms, mbv));
+        fence_proxy_async_smem();
+        mbar_arrive(AFULL(s));
+      }
+    }
+    if (pp && dt == 0) pipe_flush(p.pipe, 6, pc, 1, clock64() - t_role, 7);
+  } else {
+    // ------------------------------------------------ epilogue (4 warps)
+    const int q = warp & 3;                       // TMEM lane quarter = features q*32..q*32+31
+    const int te = tid - 320;                     // 0..127
+    const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int nrows_all = 9 * p.T;
+    const bool pp = p.pipe != nullptr;
+    unsigned long long pc[1] = {0};
+    const unsigned long long t_role = pp ? clock64() : 0;
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+      if (!ti.ok) continue;
+      // the rows' destinations, fetched before waiting for the accumulator (each row's
+      // weight was already applied to its h row by the gate/up epilogue)
+      int dv[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int j = c * 128 + te;
+        const bool valid = j < ti.n_rows;
+        dv[c] = valid ? __ldg(p.row_dst + ti.row0 + j) : -1;
+        if (valid && (dv[c] < 0 || dv[c] >= nrows_all)) {
+          atomicOr(p.err, ERRBIT_BOUNDS);
+          dv[c] = -1;
+        }
+      }
+      const int buf = tc & 1;
+      // the wait is bounded; all four warps then meet and leave together on an abort
+      mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, pc[0], pp);
+      epi_sync();                                 // also: the previous tile's tables are consumed
+      if (*abort_flag) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) md_dst[c * 128 + te] = dv[c];
+      epi_sync();
+      const int f = q * 32 + lane;                // feature inside the tile
+      const size_t fcol = static_cast<size_t>(ti.mb) * GX_BM;
+#pragma unroll 1
+      for (int cc = 0; cc < GX_BN / 32; ++cc) {
+        const int col0 = cc * 32;
+        if (col0 >= ti.n_rows) break;
+        uint32_t d[32];
+        tmem_ld32(tl + buf * 256 + col0, d);
+        tmem_ld_wait();
+        // round and transpose: staged row j holds the chunk's row col0 + j
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<__nv_bfloat16*>(stg + j * STG_ROW + f * 2) = __float2bfloat16_rn(__uint_as_float(d[j]));
+        epi_sync();
+        // each staged row is 128 features = 16 segments of 16 bytes; 512 segments per chunk
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int item = te + 128 * i;
+          const int j = item >> 4, seg = item & 15;
+          const int dst = md_dst[col0 + j];
+          if (col0 + j < ti.n_rows && dst >= 0) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + j * STG_ROW + seg * 16);
+            *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(dst) * HID + fcol + seg * 8) = v;
+          }
+        }
+        epi_sync();                               // the staging rows are free again
+      }
+      tc_fence_before();
+      mbar_arrive(ACCE(buf));
+      ++tc;
+    }
+    if (pp && te == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    if (lane == 0) drain_wait(DRAIN, 0);
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+#undef FULL
+#undef AFULL
+#undef EMPTY
+#undef ACCF
+#undef ACCE
+}
+
+cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
+                        const DownParams& p, int grid, cudaStream_t s) {
+  down_kernel<<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, p);
+  return cudaGetLastError();
+}
+
+cudaError_t set_down_attributes() {
+  return cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DN_SMEM);
+}
+
+}  // namespace moe

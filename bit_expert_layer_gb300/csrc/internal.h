@@ -52,9 +52,11 @@ struct GateUpParams {
   const uint16_t* u_scales; const uint16_t* u_biases;
   const uint16_t* sg_scales; const uint16_t* sg_biases;  // [512][32]
   const uint16_t* su_scales; const uint16_t* su_biases;
-  __nv_bfloat16* h;      // [9T][512], K-interleaved columns
+  __nv_bfloat16* h;      // [9T][512], K-interleaved columns, each row scaled by its row_w
   int T;
   unsigned int* err;
+  unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
+  const float* row_w;         // [9T] weight of each permuted row
 };
 
 struct DownParams {
@@ -68,6 +70,7 @@ struct DownParams {
   __nv_bfloat16* y;      // [9T][2048]
   int T;
   unsigned int* err;
+  unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
 };
 
 struct DecodeParams {
@@ -118,5 +121,6 @@ cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_gateup(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_down(const DecodeParams& p, cudaStream_t s);
 cudaError_t set_kernel_attributes();
+cudaError_t set_down_attributes();
 
 }  // namespace moe

@@ -46,6 +46,7 @@ struct moe_layer {
   float* dec_act_w;
   int* dec_n_active;
   __nv_bfloat16* dec_hw;
+  unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
   CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_xperm, tm_h;
 };
@@ -96,6 +97,16 @@ cudaEvent_t prof_event() {
 bool debug_sync() {
   static const bool on = [] {
     const char* v = getenv("MOE_DEBUG_SYNC");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+// MOE_PIPE_PROF=1 (read once): the grouped GEMMs add their barrier-wait cycles to the
+// layer's pipeline counters (moe_pipeline_counters).
+bool pipe_trace() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PIPE_PROF");
     return v && v[0] == '1';
   }();
   return on;
@@ -173,6 +184,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->dec_act_w = c.take<float>(DEC_MAX_ACTIVE * DEC_MAX_T * 4);
   d->dec_n_active = c.take<int>(4);
   d->dec_hw = c.take<__nv_bfloat16>(static_cast<size_t>(DEC_MAX_ACTIVE) * DEC_MAX_T * INTER * 2);
+  d->pipe = c.take<unsigned long long>(32 * 8);
   return (c.off + 255) & ~size_t(255);
 }
 
@@ -328,7 +340,7 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                  L->h, T, L->err};
+                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->row_w};
   // upper bound of the tile count: every touched expert adds at most one partial token block
   const long long tok_blocks = (8ll * T + GX_BN - 1) / GX_BN + (8ll * T < NEXP ? 8ll * T : NEXP) +
                                (T + GX_BN - 1) / GX_BN;
@@ -338,7 +350,8 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
                 [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_xperm, gp, grid_gu, s); }),
           "gate/up launch");
   DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
-                U16(w.sh_down.scales), U16(w.sh_down.biases), L->row_dst, L->row_w, L->y, T, L->err};
+                U16(w.sh_down.scales), U16(w.sh_down.biases), L->row_dst, L->row_w, L->y, T, L->err,
+                pipe_trace() ? L->pipe + 16 : nullptr};
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
@@ -407,6 +420,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
   // workspace state shared by every layer bound to it: the error word and the decode
   // ticket (nothing layer-specific may live in the workspace)
   if ((e = cudaMemset(L->err, 0, 256)) != cudaSuccess || (e = cudaMemset(L->dec_counter, 0, 256)) != cudaSuccess ||
+      (e = cudaMemset(L->pipe, 0, 32 * 8)) != cudaSuccess ||
       (e = cudaDeviceSynchronize()) != cudaSuccess)
     return fail(cuda_fail("workspace init", e));
 
@@ -528,6 +542,15 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 const char* moe_last_error_detail(void) { return g_detail; }
+
+moe_status_t moe_pipeline_counters(moe_layer_t* L, unsigned long long* out) {
+  if (!L || !out) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(out, L->pipe, 32 * 8, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(L->pipe, 0, 32 * 8);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e == cudaSuccess ? MOE_OK : cuda_fail("pipeline counters", e);
+}
 
 void moe_profiler_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof.m);

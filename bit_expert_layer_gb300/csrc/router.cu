@@ -175,12 +175,14 @@ __global__ void __launch_bounds__(256) route_scan_kernel(ScanParams p) {
   __shared__ int sc[NEXP];
   __shared__ int s_tot[2];
   const int e = threadIdx.x;
+  constexpr int CH = 16;   // histogram entries loaded together (independent loads in flight)
   int c = 0;
-#pragma unroll 4
-  for (int b = 0; b < p.nblk; ++b) {
-    const int h = p.hist[b * NEXP + e];
-    p.base[b * NEXP + e] = c;
-    c += h;
+  for (int b0 = 0; b0 < p.nblk; b0 += CH) {
+    int h[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) h[i] = (b0 + i < p.nblk) ? __ldg(p.hist + (b0 + i) * NEXP + e) : 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c += h[i];
   }
   // block-wide inclusive scan (Hillis-Steele) of the counts
   sc[e] = c;
@@ -192,7 +194,18 @@ __global__ void __launch_bounds__(256) route_scan_kernel(ScanParams p) {
     __syncthreads();
   }
   const int excl = sc[e] - c;
-  for (int b = 0; b < p.nblk; ++b) p.base[b * NEXP + e] += excl;
+  // first permuted row of (block, expert): the expert's offset plus earlier blocks' counts
+  int run = excl;
+  for (int b0 = 0; b0 < p.nblk; b0 += CH) {
+    int h[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) h[i] = (b0 + i < p.nblk) ? __ldg(p.hist + (b0 + i) * NEXP + e) : 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      if (b0 + i < p.nblk) p.base[(b0 + i) * NEXP + e] = run;
+      run += h[i];
+    }
+  }
   p.counts[e] = c;
   p.offsets[e] = excl;
   __syncthreads();

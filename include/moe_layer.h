@@ -171,6 +171,17 @@ const char* moe_status_string(moe_status_t status);
  * MOE_ERR_CUDA status (empty if none).  Valid until the thread's next call. */
 const char* moe_last_error_detail(void);
 
+/* Pipeline tracing of the grouped GEMMs (only when the environment variable
+ * MOE_PIPE_PROF=1 is set before the first forward): clock cycles that each warp role
+ * spent waiting on its barriers, summed over all CTAs and launches since the last read.
+ * out receives 32 counters, 16 for the gate/up kernel then 16 for the down kernel, each:
+ * [0] MMA issuer waiting for the accumulator to drain, [1] for dequantised tiles, [2] for
+ * TMA data, [3] MMA issuer total; [4] TMA producer waiting for a free stage, [5] its
+ * total; [6] one dequant thread waiting for TMA data, [7] its total; [8] one epilogue
+ * thread waiting for the accumulator, [9] its total; [10] tiles processed.
+ * Synchronises the device, then zeroes the counters. */
+moe_status_t moe_pipeline_counters(moe_layer_t* layer, unsigned long long* out);
+
 /* Kernel timing (tracing for benchmarks).  While enabled, every kernel this library
  * launches is bracketed by two CUDA events recorded on the launch's own stream. */
 void moe_profiler_enable(int on);

@@ -22,6 +22,11 @@ from oracle import Oracle, valid_choices
 
 GAP_TOL = 1e-4
 W_TOL = 1e-5
+# A layer with an input RMSNorm routes on bf16(x * r): the GPU's fp32 r and the oracle's
+# double r differ by ~1e-7, so about one element in 2e4 rounds to the neighbouring bf16
+# value, which moves a logit by up to 2^-8 * |x_i| * |W_r| (~1e-4) and a weight by a few
+# 1e-5; the bound keeps a decade of headroom.
+W_TOL_NORM = 1e-3
 OUT_REL_TOL = 1e-2
 
 
@@ -33,6 +38,7 @@ def check_routing(o: Oracle, L, x: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.nd
     """Returns (report dict, alt dict token -> oracle-valid expert list the GPU chose)."""
     T, K = idx_gpu.shape
     ref = ref if ref is not None else o.route(L, x)
+    w_tol = W_TOL_NORM if getattr(L, "norm_w", None) is not None else W_TOL
     near = ref["gap"] <= GAP_TOL
     alt = {}
     flips = 0
@@ -51,7 +57,7 @@ def check_routing(o: Oracle, L, x: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.nd
                     assert idx_gpu[t, k] == order[k], f"token {t} rank {k}"
             wmap = dict(zip(ref["idx"][t].tolist(), ref["w"][t].tolist()))
             for k in range(K):
-                assert abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])]) <= W_TOL, f"token {t} weight {k}"
+                assert abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])]) <= w_tol, f"token {t} weight {k}"
         else:
             logits = o.router_logits(L, x[t])
             choices = valid_choices(o, L.dims, logits, GAP_TOL)
@@ -63,7 +69,7 @@ def check_routing(o: Oracle, L, x: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.nd
             else:
                 wmap = dict(zip(ref["idx"][t].tolist(), ref["w"][t].tolist()))
                 for k in range(K):
-                    assert abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])]) <= W_TOL
+                    assert abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])]) <= w_tol
     return dict(tokens=T, near_ties=int(near.sum()), flips=flips), alt
 
 
