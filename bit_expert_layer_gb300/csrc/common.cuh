@@ -42,13 +42,19 @@ constexpr int GX_XBOX = 32;                         // token rows per TMA box
 constexpr int GX_A_BYTES = GX_BM * 64 * 2;          // 16 KB dequantised tile
 constexpr int GX_X_BYTES = GX_BN * 64 * 2;          // 32 KB activation tile
 constexpr int GX_P_BYTES = GX_BM * 32;              //  4 KB packed 4-bit tile (8 words/row)
-// gate/up: two A tiles + X + two packed tiles per stage
-constexpr int GU_STAGES = 3;
-constexpr int GU_STAGE_BYTES = 2 * GX_A_BYTES + GX_X_BYTES + 2 * GX_P_BYTES;
+// gate/up: three rings of different depth -- packed 4-bit tiles (gate + up, 8 KB, fetched
+// from HBM, deepest), activation tiles (32 KB, mostly from L2), dequantised tiles (gate +
+// up, 32 KB, only between dequant and MMA)
+constexpr int GU_NP = 6;
+constexpr int GU_NX = 3;
+constexpr int GU_NA = 2;
+constexpr int GU_P_STAGE = 2 * GX_P_BYTES;
+constexpr int GU_A_STAGE = 2 * GX_A_BYTES;
+constexpr int GU_RINGS = GU_NA * GU_A_STAGE + GU_NX * GX_X_BYTES + GU_NP * GU_P_STAGE;
 constexpr int GX_TAB_BYTES = 3 * (NEXP + 2) * 4 + 128;   // tile tables staged in shared memory
-// + alignment slack, barriers (256 B), tile tables
-constexpr int GU_SMEM = GU_STAGES * GU_STAGE_BYTES + 1024 + 512 + GX_TAB_BYTES;
-constexpr int GU_THREADS = 448;                     // producer, MMA, 8 dequant warps, 4 epilogue warps
+// + alignment slack, barriers (512 B), tile tables
+constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES;
+constexpr int GU_THREADS = 480;   // packed producer, MMA, 8 dequant, 4 epilogue, activation producer
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
 constexpr int DN_STAGES = 4;

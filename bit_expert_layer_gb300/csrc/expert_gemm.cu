@@ -1,8 +1,8 @@
-// expert_gemm.cu -- the grouped expert GEMMs of the prefill path, with the 4-bit
-// dequantisation fused into the GEMM: packed weights go from HBM to shared memory by
-// TMA, dequant warps expand them to bf16 tiles in shared memory, and tcgen05 MMAs
-// accumulate into TMEM; the dequantised weights never touch device memory (Lily fuses
-// the 4-bit restore into its grouped GEMM and keeps the result in on-chip memory:
+// expert_gemm.cu -- the grouped gate/up GEMM of the prefill path with the 4-bit
+// dequantisation fused into it, and the combine.  Packed weights go from HBM to shared
+// memory by TMA, dequant warps expand them to bf16 tiles in shared memory, and tcgen05
+// MMAs accumulate into TMEM; the dequantised weights never touch device memory (Lily
+// fuses the 4-bit restore into its grouped GEMM and keeps the result in on-chip memory:
 // aimanavo.com, "Why is Perplexity's local AI Lily faster than MLX", section "Prefill
 // and decode are not treated as the same job"; dzen.guru, "Perplexity opened the Lily
 // engine", section "Where the speed-up comes from").
@@ -11,16 +11,22 @@
 // to 256 per tile, rounded up to 16), K steps of 64 = one quantisation group, so each
 // dequantised row needs exactly one scale and one bias per K step.
 //
-//   gateup_kernel  h = silu(W_gate x) * (W_up x) for every (expert, token) pair of the
-//                  permuted activations; the shared expert is expert 256 over all T
-//                  tokens.  Two TMEM accumulators (gate, up), SwiGLU in the epilogue.
-//   down_kernel    y[row_dst] = row_w * (W_down h): each routed row is scaled by its
-//                  renormalised routing weight, each shared row by sigmoid(g_s . x).
-//                  Double-buffered TMEM accumulator so the epilogue overlaps the next
-//                  tile's MMAs.
+//   gateup_kernel  h' = w * silu(W_gate x) * (W_up x) for every (expert, token) pair of
+//                  the permuted activations, w = the row's routing weight (the shared
+//                  expert, expert 256 over all T tokens, uses sigmoid(g_s . x)).  Two
+//                  TMEM accumulators (gate, up), SwiGLU in the epilogue.
 //   combine_kernel out[t] = sum_k y[8t+k] + y[8T+t] (+ x[t]) in a fixed order.
 //
-// Persistent kernels: grid = number of SMs, tiles taken in a static stride from the
+// Warp roles of gateup_kernel (15 warps):
+//   warp 0      TMA producer of the packed 4-bit tiles (ring of GU_NP)
+//   warp 1      TMEM allocator and MMA issuer
+//   warps 2-9   dequant: packed tile -> 128-byte-swizzled bf16 tiles (ring of GU_NA)
+//   warps 10-13 epilogue: SwiGLU and row weight, bf16 h' rows
+//   warp 14     TMA producer of the activation tiles (ring of GU_NX)
+// The rings are separate so the HBM-bound packed tiles can be fetched further ahead than
+// the large activation tiles fit.
+//
+// Persistent kernel: grid = number of SMs, tiles taken in a static stride from the
 // device-side tile tables built by route_scan_kernel (no host readback).
 #include "common.cuh"
 #include "gemm_common.cuh"
@@ -29,44 +35,52 @@
 namespace moe {
 
 namespace {
-
-// gate/up stage layout
-constexpr int GU_AG = 0;
-constexpr int GU_AU = GX_A_BYTES;
-constexpr int GU_X = 2 * GX_A_BYTES;
-constexpr int GU_PG = GU_X + GX_X_BYTES;
-constexpr int GU_PU = GU_PG + GX_P_BYTES;
-
+// shared-memory layout (1024-byte aligned base)
+constexpr int OFF_A = 0;                                     // [GU_NA][gate 16 KB | up 16 KB]
+constexpr int OFF_X = OFF_A + GU_NA * GU_A_STAGE;            // [GU_NX][32 KB]
+constexpr int OFF_P = OFF_X + GU_NX * GX_X_BYTES;            // [GU_NP][gate 4 KB | up 4 KB]
+constexpr int OFF_MISC = OFF_P + GU_NP * GU_P_STAGE;
+static_assert(OFF_X % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 }  // namespace
 
-// ============================================================================ gate/up
 __global__ void __launch_bounds__(GU_THREADS, 1)
     gateup_kernel(const __grid_constant__ CUtensorMap tm_qg, const __grid_constant__ CUtensorMap tm_qu,
                   const __grid_constant__ CUtensorMap tm_sqg, const __grid_constant__ CUtensorMap tm_squ,
                   const __grid_constant__ CUtensorMap tm_x, GateUpParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GU_STAGES * GU_STAGE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_tiles = reinterpret_cast<int*>(bars + 32);
+  uint8_t* misc = smem + OFF_MISC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                   // 32 barriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  int* s_tiles = reinterpret_cast<int*>(misc + 512);
   int* s_off = s_tiles + (NEXP + 2);
   int* s_cnt = s_off + (NEXP + 2);
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
-  // full[s] = 0..2, afull[s] = 3..5, empty[s] = 6..8, accf 9, acce 10, drain 11
-#define FULL(s) (bar0 + 8u * (s))
-#define AFULL(s) (bar0 + 8u * (3 + (s)))
-#define EMPTY(s) (bar0 + 8u * (6 + (s)))
-  const uint32_t ACCF = bar0 + 72, ACCE = bar0 + 80, DRAIN = bar0 + 88;
+#define PFULL(s) (bar0 + 8u * (s))
+#define PEMPTY(s) (bar0 + 8u * (GU_NP + (s)))
+#define XFULL(s) (bar0 + 8u * (2 * GU_NP + (s)))
+#define XEMPTY(s) (bar0 + 8u * (2 * GU_NP + GU_NX + (s)))
+#define AFULL(s) (bar0 + 8u * (2 * GU_NP + 2 * GU_NX + (s)))
+#define AEMPTY(s) (bar0 + 8u * (2 * GU_NP + 2 * GU_NX + GU_NA + (s)))
+  constexpr int NB = 2 * GU_NP + 2 * GU_NX + 2 * GU_NA;
+  const uint32_t ACCF = bar0 + 8u * NB, ACCE = bar0 + 8u * (NB + 1), DRAIN = bar0 + 8u * (NB + 2);
 
   if (tid == 0) {
-    for (int s = 0; s < GU_STAGES; ++s) {
-      mbar_init(FULL(s), 1);
+    for (int s = 0; s < GU_NP; ++s) {
+      mbar_init(PFULL(s), 1);
+      mbar_init(PEMPTY(s), 256);
+    }
+    for (int s = 0; s < GU_NX; ++s) {
+      mbar_init(XFULL(s), 1);
+      mbar_init(XEMPTY(s), 1);
+    }
+    for (int s = 0; s < GU_NA; ++s) {
       mbar_init(AFULL(s), 256);
-      mbar_init(EMPTY(s), 1);
+      mbar_init(AEMPTY(s), 1);
     }
     mbar_init(ACCF, 1);
     mbar_init(ACCE, 128);
@@ -84,78 +98,97 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const int total = s_tiles[NEXP + 1];
   constexpr int NKB = HID / 64;
+  const bool pp = p.pipe != nullptr;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
-      const bool pp = p.pipe != nullptr;
+      // ------------------------------------------------ packed-tile producer
       unsigned long long pc[1] = {0};
       const unsigned long long t_role = pp ? clock64() : 0;
       tma_prefetch_desc(&tm_qg);
       tma_prefetch_desc(&tm_qu);
+      uint32_t it = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+        if (!ti.ok) { atomicOr(p.err, ERRBIT_BOUNDS); continue; }
+        const bool sh = ti.e == SHARED_E;
+        const CUtensorMap* mg = sh ? &tm_sqg : &tm_qg;
+        const CUtensorMap* mu = sh ? &tm_squ : &tm_qu;
+        const int wrow = (sh ? 0 : ti.e * INTER) + ti.mb * GX_BM;
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % GU_NP;
+          if (!mbar_wait_t(PEMPTY(s), ((it / GU_NP) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) {
+            alive = false;
+            break;
+          }
+          const uint32_t st = smem_u32(smem + OFF_P + s * GU_P_STAGE);
+          mbar_arrive_expect_tx(PFULL(s), GU_P_STAGE);
+          tma_load_2d(st, mg, PFULL(s), kb * 8, wrow);
+          tma_load_2d(st + GX_P_BYTES, mu, PFULL(s), kb * 8, wrow);
+        }
+      }
+      if (!alive) {
+        for (uint32_t i = (it > GU_NP ? it - GU_NP : 0); i < it; ++i) drain_wait(PFULL(i % GU_NP), (i / GU_NP) & 1);
+      }
+      if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
+    }
+  } else if (warp == 14) {
+    if (lane == 0) {
+      // ------------------------------------------------ activation-tile producer
       tma_prefetch_desc(&tm_x);
       uint32_t it = 0;
       bool alive = true;
       for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
         const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
-        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
-        const bool sh = ti.e == SHARED_E;
-        const CUtensorMap* mg = sh ? &tm_sqg : &tm_qg;
-        const CUtensorMap* mu = sh ? &tm_squ : &tm_qu;
-        const int wrow = (sh ? 0 : ti.e * INTER) + ti.mb * GX_BM;
+        if (!ti.ok) continue;
         const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
-        const uint32_t bytes = 2 * GX_P_BYTES + nbox * GX_XBOX * 128;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % GU_STAGES;
-          const uint32_t ph = (it / GU_STAGES) & 1;
-          if (!mbar_wait_t(EMPTY(s), ph ^ 1, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
-          const uint32_t st = smem_u32(smem + s * GU_STAGE_BYTES);
-          mbar_arrive_expect_tx(FULL(s), bytes);
-          tma_load_2d(st + GU_PG, mg, FULL(s), kb * 8, wrow);
-          tma_load_2d(st + GU_PU, mu, FULL(s), kb * 8, wrow);
+          const int s = it % GU_NX;
+          if (!mbar_wait(XEMPTY(s), ((it / GU_NX) & 1) ^ 1, p.err, abort_flag)) { alive = false; break; }
+          const uint32_t st = smem_u32(smem + OFF_X + s * GX_X_BYTES);
+          mbar_arrive_expect_tx(XFULL(s), nbox * GX_XBOX * 128);
           for (int j = 0; j < nbox; ++j)
-            tma_load_2d(st + GU_X + j * GX_XBOX * 128, &tm_x, FULL(s), kb * 64, ti.row0 + j * GX_XBOX);
+            tma_load_2d(st + j * GX_XBOX * 128, &tm_x, XFULL(s), kb * 64, ti.row0 + j * GX_XBOX);
         }
       }
       if (!alive) {
-        for (uint32_t i = (it > GU_STAGES ? it - GU_STAGES : 0); i < it; ++i)
-          drain_wait(FULL(i % GU_STAGES), (i / GU_STAGES) & 1);
+        for (uint32_t i = (it > GU_NX ? it - GU_NX : 0); i < it; ++i) drain_wait(XFULL(i % GU_NX), (i / GU_NX) & 1);
       }
-      if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      const bool pp = p.pipe != nullptr;
       unsigned long long pc[3] = {0, 0, 0};
       const unsigned long long t_role = pp ? clock64() : 0;
       uint32_t it = 0, tc = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
         const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
-        if (!ti.ok) { if (threadIdx.x == 0) atomicOr(p.err, ERRBIT_BOUNDS); continue; }
+        if (!ti.ok) continue;
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, N);
         if (!mbar_wait_t(ACCE, (tc & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
         tc_fence_after();
         bool alive = true;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % GU_STAGES;
-          const uint32_t ph = (it / GU_STAGES) & 1;
-          if (!mbar_wait_t(AFULL(s), ph, p.err, abort_flag, pc[1], pp) ||
-              !mbar_wait_t(FULL(s), ph, p.err, abort_flag, pc[2], pp)) {
+          const int sa = it % GU_NA, sx = it % GU_NX;
+          if (!mbar_wait_t(AFULL(sa), (it / GU_NA) & 1, p.err, abort_flag, pc[1], pp) ||
+              !mbar_wait_t(XFULL(sx), (it / GU_NX) & 1, p.err, abort_flag, pc[2], pp)) {
             alive = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * GU_STAGE_BYTES);
+          const uint32_t a = smem_u32(smem + OFF_A + sa * GU_A_STAGE);
+          const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(st + GU_X + kk * 32);
+            const uint64_t bd = sdesc_sw128(x + kk * 32);
             const uint32_t acc = (kb | kk) != 0;
-            umma_bf16(tmem, sdesc_sw128(st + GU_AG + kk * 32), bd, idesc, acc);
-            umma_bf16(tmem + 256, sdesc_sw128(st + GU_AU + kk * 32), bd, idesc, acc);
+            umma_bf16(tmem, sdesc_sw128(a + kk * 32), bd, idesc, acc);
+            umma_bf16(tmem + 256, sdesc_sw128(a + GX_A_BYTES + kk * 32), bd, idesc, acc);
           }
-          umma_commit(EMPTY(s));
+          umma_commit(AEMPTY(sa));
+          umma_commit(XEMPTY(sx));
         }
         if (!alive) break;
         umma_commit(ACCF);
@@ -170,13 +203,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   } else if (warp < 10) {
     // ------------------------------------------------ dequant (8 warps)
     const int dt = tid - 64;           // 0..255
-    const bool pp = p.pipe != nullptr;
-    unsigned long long pc[1] = {0};
-    const unsigned long long t_role = pp ? clock64() : 0;
     const int mat = dt >> 7;           // 0: gate rows, 1: up rows
     const int r = dt & 127;            // row inside the tile
-    const int p_off = mat ? GU_PU : GU_PG;
-    const int a_off = mat ? GU_AU : GU_AG;
+    unsigned long long pc[1] = {0};
+    const unsigned long long t_role = pp ? clock64() : 0;
     uint32_t it = 0;
     bool alive = true;
     // The scales and biases of 8 K steps (16 bytes each) are loaded one chunk ahead,
@@ -203,7 +233,6 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       const uint16_t* csc = sc;
       const uint16_t* cbi = bi;
       if (!cur.ok) {
-        if (threadIdx.x == 64) atomicOr(p.err, ERRBIT_BOUNDS);
         load_next(tile + gridDim.x);
         continue;
       }
@@ -219,16 +248,22 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int s = it % GU_STAGES;
-          const uint32_t ph = (it / GU_STAGES) & 1;
-          if (!mbar_wait_t(FULL(s), ph, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
+          const int sp = it % GU_NP, sa = it % GU_NA;
+          if (!mbar_wait_t(PFULL(sp), (it / GU_NP) & 1, p.err, abort_flag, pc[0], pp) ||
+              !mbar_wait(AEMPTY(sa), ((it / GU_NA) & 1) ^ 1, p.err, abort_flag)) {
+            alive = false;
+            break;
+          }
           ++it;
           const __nv_bfloat162 ms = bf2((j & 1) ? (sw[j >> 1] >> 16) : sw[j >> 1]);
           const __nv_bfloat162 mbv = bf2((j & 1) ? (bw[j >> 1] >> 16) : bw[j >> 1]);
-          uint8_t* st = smem + s * GU_STAGE_BYTES;
-          const uint4* P = reinterpret_cast<const uint4*>(st + p_off + r * 32);
+          const uint4* P = reinterpret_cast<const uint4*>(smem + OFF_P + sp * GU_P_STAGE + mat * GX_P_BYTES + r * 32);
           const uint4 w0 = P[0], w1 = P[1];
-          uint8_t* A = st + a_off;
+          // the packed words are in registers; the next TMA write into this stage is an
+          // async-proxy access, so the generic reads are fenced before the release
+          fence_proxy_async_smem();
+          mbar_arrive(PEMPTY(sp));
+          uint8_t* A = smem + OFF_A + sa * GU_A_STAGE + mat * GX_A_BYTES;
           st_shared_v4(A + sw128_off(r, 0), dequant8(w0.x, ms, mbv));
           st_shared_v4(A + sw128_off(r, 1), dequant8(w0.y, ms, mbv));
           st_shared_v4(A + sw128_off(r, 2), dequant8(w0.z, ms, mbv));
@@ -238,7 +273,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           st_shared_v4(A + sw128_off(r, 6), dequant8(w1.z, ms, mbv));
           st_shared_v4(A + sw128_off(r, 7), dequant8(w1.w, ms, mbv));
           fence_proxy_async_smem();
-          mbar_arrive(AFULL(s));
+          mbar_arrive(AFULL(sa));
         }
       }
     }
@@ -248,7 +283,6 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     // While these warps drain TMEM, the dequant warps already fill the next tile's stages.
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const bool pp = p.pipe != nullptr;
     unsigned long long pc[1] = {0};
     const unsigned long long t_role = pp ? clock64() : 0;
     uint32_t tc = 0;
@@ -309,9 +343,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
-#undef FULL
+#undef PFULL
+#undef PEMPTY
+#undef XFULL
+#undef XEMPTY
 #undef AFULL
-#undef EMPTY
+#undef AEMPTY
 }
 
 // ============================================================================ combine
