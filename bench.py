@@ -315,8 +315,13 @@ def run_ours(args, wl):
 
     tokens_per_step = (Tp + Td) * n_layers
     value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
-    launches = args.steps * sum((_abi.moe_forward_launches(l.handle, Tp) if Tp else 0) +
-                                (_abi.moe_forward_launches(l.handle, Td) if Td else 0) for l in layers)
+    def call_launches(T):
+        if not T:
+            return 0
+        if resid:
+            return _abi.moe_stack_forward_launches([l.handle for l in layers], T)
+        return _abi.moe_forward_launches(layers[0].handle, T)
+    launches = args.steps * (call_launches(Tp) + call_launches(Td))
 
     # ---------------- e2e: host buffers through the C entry, copies inside the region
     e2e = None

@@ -76,6 +76,8 @@ def lib() -> C.CDLL:
         L.moe_stack_forward_host.restype = S
         L.moe_forward_launches.argtypes = [P, I]
         L.moe_forward_launches.restype = I
+        L.moe_stack_forward_launches.argtypes = [P, I, I]
+        L.moe_stack_forward_launches.restype = I
         L.moe_layer_get_error.argtypes = [P]
         L.moe_layer_get_error.restype = S
         L.moe_layer_destroy.argtypes = [P]
@@ -148,6 +150,11 @@ def moe_stack_forward_host(layers, x_host: int, T: int, out_host: int, stream: i
 
 def moe_forward_launches(layer: int, T: int) -> int:
     return int(lib().moe_forward_launches(layer, T))
+
+
+def moe_stack_forward_launches(layers, T: int) -> int:
+    arr = (C.c_void_p * len(layers))(*layers)
+    return int(lib().moe_stack_forward_launches(arr, len(layers), T))
 
 
 def moe_layer_get_error(layer: int) -> int:

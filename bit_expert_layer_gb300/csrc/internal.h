@@ -103,6 +103,42 @@ struct DecodeParams {
   unsigned int* err;
 };
 
+// One layer of the fused decode kernel: the layer's weights and its error word.
+struct DecLayer {
+  const __nv_bfloat16* router_w;      // [256][2048]
+  const float* router_bias;           // [256] or nullptr
+  const __nv_bfloat16* shared_gate_w; // [2048]
+  const __nv_bfloat16* norm_w;        // [2048] input RMSNorm weights, or nullptr (no norm)
+  const uint32_t* gq; const uint16_t* gs; const uint16_t* gb;     // routed gate
+  const uint32_t* uq; const uint16_t* us; const uint16_t* ub;     // routed up
+  const uint32_t* dq; const uint16_t* ds; const uint16_t* db;     // routed down
+  const uint32_t* sgq; const uint16_t* sgs; const uint16_t* sgb;  // shared gate
+  const uint32_t* suq; const uint16_t* sus; const uint16_t* sub;  // shared up
+  const uint32_t* sdq; const uint16_t* sds; const uint16_t* sdb;  // shared down
+  unsigned int* err;
+};
+
+constexpr int DEC_MAX_LAYERS = 48;   // layers per launch of the fused decode kernel
+constexpr size_t DEC_LT_WORDS = 2ull * 8 * 257;
+constexpr size_t DEC_HT_WORDS = 2ull * 65 * 8 * 256;
+constexpr size_t DEC_XT_WORDS = 2ull * 8 * 1024;
+
+struct DecLayersParams {
+  const __nv_bfloat16* x;   // [T][2048] input of the first layer
+  __nv_bfloat16* out;       // [T][2048] output of every layer (may alias x)
+  int T;                    // 1..8
+  int n_layers;             // 1..DEC_MAX_LAYERS
+  int residual;             // out = x + MoE(x) when set
+  // scratch, zeroed once when the workspace is bound; tagged words {payload, tag}
+  unsigned long long* lt;   // [2][8][257] router and shared-gate logits
+  unsigned long long* ht;   // [2][65][8][256] weighted h' (pairs of interleaved features)
+  unsigned long long* xt;   // [2][8][1024] layer outputs between layers (pairs of features)
+  unsigned int* sync;       // [4]: [1] exit count, [2] abort flag, [3] launch epoch
+  int* topk_idx;            // [T][8] routing of the last layer, or nullptr
+  float* topk_w;
+  DecLayer layer[DEC_MAX_LAYERS];
+};
+
 // launchers (return the first launch error)
 cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
                                   cudaStream_t s);
@@ -118,8 +154,7 @@ cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUt
 cudaError_t launch_combine(const __nv_bfloat16* y, const __nv_bfloat16* x, __nv_bfloat16* out, int T,
                            int residual, cudaStream_t s);
 cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
-cudaError_t launch_decode_gateup(const DecodeParams& p, cudaStream_t s);
-cudaError_t launch_decode_down(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s);
 cudaError_t set_kernel_attributes();
 cudaError_t set_down_attributes();
 

@@ -46,6 +46,10 @@ struct moe_layer {
   float* dec_act_w;
   int* dec_n_active;
   __nv_bfloat16* dec_hw;
+  unsigned int* dec_sync;          // fused decode: exit count, abort flag, launch epoch
+  unsigned long long* dec_lt;      // fused decode: tagged logits, h', layer outputs
+  unsigned long long* dec_ht;
+  unsigned long long* dec_xt;
   unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
   CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_xperm, tm_h;
@@ -63,12 +67,12 @@ void set_detail(const char* what, cudaError_t e) {
 // While enabled, every launch is bracketed by two CUDA events on its own stream; the
 // durations are resolved (and the record cleared) by moe_profiler_read.
 enum KernelId {
-  K_ROUTER, K_SCAN, K_SCATTER, K_GATEUP, K_DOWN, K_COMBINE, K_DEC_ROUTER, K_DEC_GATEUP, K_DEC_DOWN, K_NORM,
+  K_ROUTER, K_SCAN, K_SCATTER, K_GATEUP, K_DOWN, K_COMBINE, K_DEC_ROUTER, K_DEC_LAYERS, K_NORM,
   K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"router_prefill", "route_scan",    "route_scatter",
                                            "gateup",         "down",          "combine",
-                                           "decode_router",  "decode_gateup", "decode_down",
+                                           "decode_router",  "decode_layers",
                                            "rmsnorm"};
 struct ProfRec {
   int id;
@@ -185,6 +189,10 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->dec_n_active = c.take<int>(4);
   d->dec_hw = c.take<__nv_bfloat16>(static_cast<size_t>(DEC_MAX_ACTIVE) * DEC_MAX_T * INTER * 2);
   d->pipe = c.take<unsigned long long>(32 * 8);
+  d->dec_sync = c.take<unsigned int>(256);
+  d->dec_lt = c.take<unsigned long long>(DEC_LT_WORDS * 8);
+  d->dec_ht = c.take<unsigned long long>(DEC_HT_WORDS * 8);
+  d->dec_xt = c.take<unsigned long long>(DEC_XT_WORDS * 8);
   return (c.off + 255) & ~size_t(255);
 }
 
@@ -307,6 +315,55 @@ DecodeParams decode_params(moe_layer* L, const void* x, int T, void* out, int re
   return p;
 }
 
+DecLayer dec_layer(const moe_layer* L) {
+  DecLayer d;
+  std::memset(&d, 0, sizeof d);
+  d.router_w = static_cast<const __nv_bfloat16*>(L->w.router_w);
+  d.router_bias = L->w.router_bias;
+  d.shared_gate_w = static_cast<const __nv_bfloat16*>(L->w.shared_gate_w);
+  d.norm_w = static_cast<const __nv_bfloat16*>(L->w.norm_w);
+  auto Q = [](const moe_qmat_t& m, const uint32_t*& q, const uint16_t*& sc, const uint16_t*& bi) {
+    q = static_cast<const uint32_t*>(m.q);
+    sc = static_cast<const uint16_t*>(m.scales);
+    bi = static_cast<const uint16_t*>(m.biases);
+  };
+  Q(L->w.gate, d.gq, d.gs, d.gb);
+  Q(L->w.up, d.uq, d.us, d.ub);
+  Q(L->w.down, d.dq, d.ds, d.db);
+  Q(L->w.sh_gate, d.sgq, d.sgs, d.sgb);
+  Q(L->w.sh_up, d.suq, d.sus, d.sub);
+  Q(L->w.sh_down, d.sdq, d.sds, d.sdb);
+  d.err = L->err;
+  return d;
+}
+
+// Decode forward (T <= 8) of n consecutive layers in one cooperative launch per
+// DEC_MAX_LAYERS layers; the scratch (logits, h', barrier words) is the first layer's.
+moe_status_t decode_forward(moe_layer* const* layers, int n, const void* x, int T, void* out, int residual,
+                            cudaStream_t s) {
+  static DecLayersParams p;   // large (about 9 KB): kept off the stack, filled under the lock
+  static std::mutex m;
+  std::lock_guard<std::mutex> lk(m);
+  moe_layer* L0 = layers[0];
+  for (int base = 0; base < n; base += DEC_MAX_LAYERS) {
+    const int cnt = n - base < DEC_MAX_LAYERS ? n - base : DEC_MAX_LAYERS;
+    p.x = static_cast<const __nv_bfloat16*>(base == 0 ? x : out);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.T = T;
+    p.n_layers = cnt;
+    p.residual = residual;
+    p.lt = L0->dec_lt;
+    p.ht = L0->dec_ht;
+    p.xt = L0->dec_xt;
+    p.sync = L0->dec_sync;
+    p.topk_idx = nullptr;
+    p.topk_w = nullptr;
+    for (int i = 0; i < cnt; ++i) p.layer[i] = dec_layer(layers[base + i]);
+    MOE_TRY(timed(K_DEC_LAYERS, s, L0->err, [&] { return launch_decode_layers(p, s); }), "decode launch");
+  }
+  return MOE_OK;
+}
+
 // The layer's input to routing and experts: x itself, or its RMSNorm when the layer has one.
 moe_status_t layer_input(moe_layer* L, const void* x, int T, cudaStream_t s, const void** xin) {
   *xin = x;
@@ -322,17 +379,10 @@ moe_status_t layer_input(moe_layer* L, const void* x, int T, cudaStream_t s, con
 }
 
 moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, int residual, cudaStream_t s) {
+  if (T <= DEC_MAX_T) return decode_forward(&L, 1, x_orig, T, out, residual, s);
   const void* x = nullptr;
   const moe_status_t sn = layer_input(L, x_orig, T, s, &x);
   if (sn != MOE_OK) return sn;
-  if (T <= DEC_MAX_T) {
-    DecodeParams p = decode_params(L, x, T, out, residual);
-    p.x_resid = static_cast<const __nv_bfloat16*>(x_orig);
-    MOE_TRY(timed(K_DEC_ROUTER, s, L->err, [&] { return launch_decode_router(p, s); }), "decode router launch");
-    MOE_TRY(timed(K_DEC_GATEUP, s, L->err, [&] { return launch_decode_gateup(p, s); }), "decode gate/up launch");
-    MOE_TRY(timed(K_DEC_DOWN, s, L->err, [&] { return launch_decode_down(p, s); }), "decode down launch");
-    return MOE_OK;
-  }
   const moe_status_t st = route_prefill(L, x, T, 1, s);
   if (st != MOE_OK) return st;
   auto U16 = [](const void* p) { return static_cast<const uint16_t*>(p); };
@@ -417,10 +467,15 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
   }
   if ((e = set_router_attributes()) != cudaSuccess || (e = set_gemm_attributes()) != cudaSuccess)
     return fail(cuda_fail("kernel attributes", e));
-  // workspace state shared by every layer bound to it: the error word and the decode
-  // ticket (nothing layer-specific may live in the workspace)
+  // workspace state shared by every layer bound to it: the error word, the decode
+  // ticket and the fused decode kernel's tagged tables and epoch, which start at zero
+  // (no tag is zero) -- nothing layer-specific may live in the workspace
   if ((e = cudaMemset(L->err, 0, 256)) != cudaSuccess || (e = cudaMemset(L->dec_counter, 0, 256)) != cudaSuccess ||
       (e = cudaMemset(L->pipe, 0, 32 * 8)) != cudaSuccess ||
+      (e = cudaMemset(L->dec_sync, 0, 256)) != cudaSuccess ||
+      (e = cudaMemset(L->dec_lt, 0, DEC_LT_WORDS * 8)) != cudaSuccess ||
+      (e = cudaMemset(L->dec_ht, 0, DEC_HT_WORDS * 8)) != cudaSuccess ||
+      (e = cudaMemset(L->dec_xt, 0, DEC_XT_WORDS * 8)) != cudaSuccess ||
       (e = cudaDeviceSynchronize()) != cudaSuccess)
     return fail(cuda_fail("workspace init", e));
 
@@ -486,6 +541,7 @@ moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x
     const moe_status_t st = check_call(layers[l], x_io, T, x_io);
     if (st != MOE_OK) return st;
   }
+  if (T <= DEC_MAX_T) return decode_forward(layers, n_layers, x_io, T, x_io, 1, reinterpret_cast<cudaStream_t>(stream));
   for (int l = 0; l < n_layers; ++l) {
     const moe_status_t st = forward_impl(layers[l], x_io, T, x_io, 1, reinterpret_cast<cudaStream_t>(stream));
     if (st != MOE_OK) return st;
@@ -509,7 +565,17 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
 
 int moe_forward_launches(const moe_layer_t* L, int T) {
   if (!L || T < 1 || T > L->cfg.max_tokens) return 0;
-  return (T <= DEC_MAX_T ? 3 : 6) + (L->w.norm_w ? 1 : 0);
+  return T <= DEC_MAX_T ? 1 : 6 + (L->w.norm_w ? 1 : 0);
+}
+
+int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, int T) {
+  if (!layers || n_layers < 1) return 0;
+  for (int l = 0; l < n_layers; ++l)
+    if (!layers[l] || T < 1 || T > layers[l]->cfg.max_tokens) return 0;
+  if (T <= DEC_MAX_T) return (n_layers + DEC_MAX_LAYERS - 1) / DEC_MAX_LAYERS;
+  int n = 0;
+  for (int l = 0; l < n_layers; ++l) n += moe_forward_launches(layers[l], T);
+  return n;
 }
 
 moe_status_t moe_layer_get_error(moe_layer_t* L) {

@@ -26,8 +26,7 @@ namespace {
 
 // Layout of the static scratch for up to DEC_MAX_T tokens.
 struct StaticLayout {
-  size_t err, counter, logits, topk_idx, topk_w, counts, offsets, perm, act_expert, act_w, n_active, hw, xn,
-      total;
+  size_t err, sync, lt, ht, xt, topk_idx, topk_w, total;
 };
 
 constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -36,24 +35,18 @@ constexpr StaticLayout make_layout() {
   StaticLayout L{};
   size_t o = 0;
   L.err = o;        o = align256(o + 4);
-  L.counter = o;    o = align256(o + 4);
-  L.logits = o;     o = align256(o + DEC_MAX_T * (NEXP + 1) * 4);
+  L.sync = o;       o = align256(o + 16);
+  L.lt = o;         o = align256(o + DEC_LT_WORDS * 8);
+  L.ht = o;         o = align256(o + DEC_HT_WORDS * 8);
+  L.xt = o;         o = align256(o + DEC_XT_WORDS * 8);
   L.topk_idx = o;   o = align256(o + DEC_MAX_T * TOPK * 4);
   L.topk_w = o;     o = align256(o + DEC_MAX_T * TOPK * 4);
-  L.counts = o;     o = align256(o + (NEXP + 1) * 4);
-  L.offsets = o;    o = align256(o + (NEXP + 2) * 4);
-  L.perm = o;       o = align256(o + DEC_MAX_T * TOPK * 4);
-  L.act_expert = o; o = align256(o + DEC_MAX_ACTIVE * 4);
-  L.act_w = o;      o = align256(o + DEC_MAX_ACTIVE * DEC_MAX_T * 4);
-  L.n_active = o;   o = align256(o + 4);
-  L.hw = o;         o = align256(o + static_cast<size_t>(DEC_MAX_ACTIVE) * DEC_MAX_T * INTER * 2);
-  L.xn = o;         o = align256(o + static_cast<size_t>(DEC_MAX_T) * HID * 2);
   L.total = o;
   return L;
 }
 
 constexpr StaticLayout kLayout = make_layout();
-constexpr size_t kStaticScratchBytes = 1u << 20;   // 1 MiB, held by every device that loads the library
+constexpr size_t kStaticScratchBytes = 3u << 20;   // 3 MiB, held by every device that loads the library
 static_assert(kLayout.total <= kStaticScratchBytes, "static scratch too small for the decode path");
 
 }  // namespace
@@ -116,51 +109,42 @@ extern "C" moe_status_t moe_decode_forward_static(const moe_weights_t* w, const 
   unsigned char* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the error word and the router's arrival ticket must start at zero on every call
-  if (cudaMemsetAsync(base, 0, kLayout.logits, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the error word starts at zero on every call; the tagged tables and the epoch word
+  // start at zero with the array and are left to the kernel, which keeps them valid
+  if (cudaMemsetAsync(base + kLayout.err, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  const __nv_bfloat16* xin = static_cast<const __nv_bfloat16*>(x);
-  if (w->norm_w) {
-    __nv_bfloat16* xn = reinterpret_cast<__nv_bfloat16*>(base + kLayout.xn);
-    if (launch_rmsnorm(xin, static_cast<const __nv_bfloat16*>(w->norm_w), xn, T, s) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    xin = xn;
-  }
-  DecodeParams p;
+  static DecLayersParams p;   // about 9 KB: kept off the stack, filled under the lock
+  static std::mutex m;
+  std::lock_guard<std::mutex> lk(m);
   std::memset(&p, 0, sizeof p);
-  p.x = xin;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.out = static_cast<__nv_bfloat16*>(out);
   p.T = T;
-  p.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
-  p.router_bias = w->router_bias;
-  p.shared_gate_w = static_cast<const __nv_bfloat16*>(w->shared_gate_w);
-  p.logits = reinterpret_cast<float*>(base + kLayout.logits);
-  p.counter = reinterpret_cast<unsigned int*>(base + kLayout.counter);
+  p.n_layers = 1;
+  p.residual = residual ? 1 : 0;
+  p.lt = reinterpret_cast<unsigned long long*>(base + kLayout.lt);
+  p.ht = reinterpret_cast<unsigned long long*>(base + kLayout.ht);
+  p.xt = reinterpret_cast<unsigned long long*>(base + kLayout.xt);
+  p.sync = reinterpret_cast<unsigned int*>(base + kLayout.sync);
   p.topk_idx = reinterpret_cast<int*>(base + kLayout.topk_idx);
   p.topk_w = reinterpret_cast<float*>(base + kLayout.topk_w);
-  p.counts = reinterpret_cast<int*>(base + kLayout.counts);
-  p.offsets = reinterpret_cast<int*>(base + kLayout.offsets);
-  p.perm = reinterpret_cast<int*>(base + kLayout.perm);
-  p.act_expert = reinterpret_cast<int*>(base + kLayout.act_expert);
-  p.act_w = reinterpret_cast<float*>(base + kLayout.act_w);
-  p.n_active = reinterpret_cast<int*>(base + kLayout.n_active);
-  p.hw = reinterpret_cast<__nv_bfloat16*>(base + kLayout.hw);
-  auto Q = [](const moe_qmat_t& m, const uint32_t*& q, const uint16_t*& sc, const uint16_t*& bi) {
-    q = static_cast<const uint32_t*>(m.q);
-    sc = static_cast<const uint16_t*>(m.scales);
-    bi = static_cast<const uint16_t*>(m.biases);
+  DecLayer& d = p.layer[0];
+  d.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
+  d.router_bias = w->router_bias;
+  d.shared_gate_w = static_cast<const __nv_bfloat16*>(w->shared_gate_w);
+  d.norm_w = static_cast<const __nv_bfloat16*>(w->norm_w);
+  auto Q = [](const moe_qmat_t& mq, const uint32_t*& q, const uint16_t*& sc, const uint16_t*& bi) {
+    q = static_cast<const uint32_t*>(mq.q);
+    sc = static_cast<const uint16_t*>(mq.scales);
+    bi = static_cast<const uint16_t*>(mq.biases);
   };
-  Q(w->gate, p.gq, p.gs, p.gb);
-  Q(w->up, p.uq, p.us, p.ub);
-  Q(w->down, p.dq, p.ds, p.db);
-  Q(w->sh_gate, p.sgq, p.sgs, p.sgb);
-  Q(w->sh_up, p.suq, p.sus, p.sub);
-  Q(w->sh_down, p.sdq, p.sds, p.sdb);
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.x_resid = static_cast<const __nv_bfloat16*>(x);
-  p.residual = residual ? 1 : 0;
-  p.err = reinterpret_cast<unsigned int*>(base + kLayout.err);
-  if (launch_decode_router(p, s) != cudaSuccess || launch_decode_gateup(p, s) != cudaSuccess ||
-      launch_decode_down(p, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  Q(w->gate, d.gq, d.gs, d.gb);
+  Q(w->up, d.uq, d.us, d.ub);
+  Q(w->down, d.dq, d.ds, d.db);
+  Q(w->sh_gate, d.sgq, d.sgs, d.sgb);
+  Q(w->sh_up, d.suq, d.sus, d.sub);
+  Q(w->sh_down, d.sdq, d.sds, d.sdb);
+  d.err = reinterpret_cast<unsigned int*>(base + kLayout.err);
+  if (launch_decode_layers(p, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -136,7 +136,7 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
  * a plug-in whose host application owns all device memory and offers no allocator or
  * workspace, or a latency-critical decode loop that must never reach cudaMalloc (which
  * can synchronise the device).  No layer object and no workspace: the scratch of the
- * decode kernels lives in a fixed 1 MiB array of device memory inside the library,
+ * decode kernel lives in a fixed 3 MiB array of device memory inside the library,
  * held by every device that loads it until the process exits.  Nothing is allocated
  * (no cudaMalloc, no cudaFree, no allocating library routine).  The pages describe no
  * such entry point; it has no counterpart there.
@@ -156,6 +156,11 @@ moe_status_t moe_decode_forward_static(const moe_weights_t* weights, const void*
 /* Number of kernel launches one moe_forward of T tokens on this layer enqueues
  * (for accounting); 0 for a NULL layer or T out of range. */
 int moe_forward_launches(const moe_layer_t* layer, int T);
+
+/* Number of kernel launches one moe_stack_forward of T tokens over these layers
+ * enqueues (for T <= 8 the whole stack runs in one launch per 48 layers); 0 for a NULL
+ * array or layer, n_layers < 1 or T out of range. */
+int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, int T);
 
 /* Synchronise the device, read and clear the layer's device error word.
  * MOE_OK if nothing was recorded. */

@@ -71,6 +71,9 @@ def test_call_argument_checks_need_no_gpu(lib):
     assert lib.moe_route(None, None, 1, None, None, None, None, None, None) == _abi.MOE_ERR_INVALID_ARG
     assert lib.moe_stack_forward(None, 0, None, 1, None) == _abi.MOE_ERR_INVALID_ARG
     assert lib.moe_forward_launches(None, 1) == 0
+    assert lib.moe_stack_forward_launches(None, 1, 1) == 0
+    null_layers = (C.c_void_p * 2)(None, None)
+    assert lib.moe_stack_forward_launches(null_layers, 2, 1) == 0
 
 
 def test_status_strings(lib):
