@@ -67,6 +67,23 @@ def rank_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time; every rank receives it."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank_step: int, steps: int, elapsed_ms: float) -> float:
+    """Units all ranks processed (each rank its own replica's work) / the slowest rank's
+    time: weak scaling, no data-path collective."""
+    return world * units_per_rank_step * steps / (elapsed_ms / 1e3)
+
+
 def make_hosts(wl):
     import synth
     n = wl["layers"]
@@ -306,15 +323,12 @@ def run_ours(args, wl):
     # with the single-layer flush the step total excludes the flush: sum the parts
     part_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in part.items()}
     elapsed_ms = t0.elapsed_time(t1) if flush is None else part_ms["prefill"] + part_ms["decode"]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     status = layers[0].get_error()
     assert status == 0, f"device error word {status}"
 
     tokens_per_step = (Tp + Td) * n_layers
-    value = world * tokens_per_step * args.steps / (elapsed_ms / 1e3)
+    value = job_throughput(world, tokens_per_step, args.steps, elapsed_ms)
     def call_launches(T):
         if not T:
             return 0
@@ -347,13 +361,9 @@ def run_ours(args, wl):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
         nbytes = (Tp + Td) * 2048 * 2
-        e2e = dict(value=world * tokens_per_step * args.steps / (e_ms / 1e3), unit=UNIT,
+        e2e = dict(value=job_throughput(world, tokens_per_step, args.steps, e_ms), unit=UNIT,
                    h2d_bytes_per_step=nbytes, d2h_bytes_per_step=nbytes, ms_per_step=e_ms / args.steps)
 
     # ---------------- roofline of the dominant kernel
