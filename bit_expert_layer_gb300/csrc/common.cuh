@@ -53,8 +53,10 @@ constexpr int GU_A_STAGE = 2 * GX_A_BYTES;
 constexpr int GU_RINGS = GU_NA * GU_A_STAGE + GU_NX * GX_X_BYTES + GU_NP * GU_P_STAGE;
 constexpr int GX_TAB_BYTES = 3 * (NEXP + 2) * 4 + 128;   // tile tables staged in shared memory
 // + alignment slack, barriers (512 B), tile tables
-constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES;
-constexpr int GU_THREADS = 480;   // packed producer, MMA, 8 dequant, 4 epilogue, activation producer
+constexpr int GU_GW = 6;                            // activation gather warps
+constexpr int GU_GROWS = (GX_BN + GU_GW - 1) / GU_GW + 4;   // token ids per gather warp and tile
+constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4;
+constexpr int GU_THREADS = (14 + GU_GW) * 32;   // packed producer, MMA, 8 dequant, 4 epilogue, gather warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
 constexpr int DN_STAGES = 4;
@@ -66,8 +68,10 @@ static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exc
 constexpr int DN_THREADS = 448;                     // producer, MMA, 8 dequant, 4 epilogue warps
 constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
 
-// scatter: one CTA per router block of 128 tokens (1024 slots)
+// scatter: per router block of 128 tokens (1024 slots), SC_SPLIT CTAs; the first also
+// places the slots, all of them copy their share of the tokens
 constexpr int SC_THREADS = 256;
+constexpr int SC_SPLIT = 4;
 
 // decode path (T <= 8)
 constexpr int DEC_MAX_T = 8;
@@ -152,6 +156,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same load with an L2 eviction-priority policy (from l2_policy_*).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                 int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+// L2 policies: data read once (streamed weights) and data read again soon (activations)
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // ----------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -201,6 +226,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
         "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {

@@ -17,12 +17,17 @@
 //                  TMEM accumulators (gate, up), SwiGLU in the epilogue.
 //   combine_kernel out[t] = sum_k y[8t+k] + y[8T+t] (+ x[t]) in a fixed order.
 //
-// Warp roles of gateup_kernel (15 warps):
+// Warp roles of gateup_kernel (20 warps, one role per warpgroup but the first):
 //   warp 0      TMA producer of the packed 4-bit tiles (ring of GU_NP)
 //   warp 1      TMEM allocator and MMA issuer
-//   warps 2-9   dequant: packed tile -> 128-byte-swizzled bf16 tiles (ring of GU_NA)
-//   warps 10-13 epilogue: SwiGLU and row weight, bf16 h' rows
-//   warp 14     TMA producer of the activation tiles (ring of GU_NX)
+//   warps 2-7   activation gather (GU_GW warps, ring of GU_NX): the tile's rows are tokens in expert
+//               order; each row is copied from the K-interleaved copy of x by token id
+//               with 16-byte cp.async into the 128-byte-swizzled layout the MMA reads,
+//               so the nine permuted copies of x are never written to memory; the
+//               activation rows are kept in L2 (evict-last), the weights streamed
+//               through it (evict-first)
+//   warps 8-15  dequant: packed tile -> 128-byte-swizzled bf16 tiles (ring of GU_NA)
+//   warps 16-19 epilogue: SwiGLU and row weight, bf16 h' rows
 // The rings are separate so the HBM-bound packed tiles can be fetched further ahead than
 // the large activation tiles fit.
 //
@@ -46,7 +51,7 @@ static_assert(OFF_X % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-
 __global__ void __launch_bounds__(GU_THREADS, 1)
     gateup_kernel(const __grid_constant__ CUtensorMap tm_qg, const __grid_constant__ CUtensorMap tm_qu,
                   const __grid_constant__ CUtensorMap tm_sqg, const __grid_constant__ CUtensorMap tm_squ,
-                  const __grid_constant__ CUtensorMap tm_x, GateUpParams p) {
+                  GateUpParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* misc = smem + OFF_MISC;
@@ -56,6 +61,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   int* s_tiles = reinterpret_cast<int*>(misc + 512);
   int* s_off = s_tiles + (NEXP + 2);
   int* s_cnt = s_off + (NEXP + 2);
+  int* s_tok = reinterpret_cast<int*>(misc + 512 + GX_TAB_BYTES);   // [GU_GW][GU_GROWS] token ids
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -75,7 +81,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       mbar_init(PEMPTY(s), 256);
     }
     for (int s = 0; s < GU_NX; ++s) {
-      mbar_init(XFULL(s), 1);
+      mbar_init(XFULL(s), GU_GW * 32);   // one arrival per gather thread, after its copies landed
       mbar_init(XEMPTY(s), 1);
     }
     for (int s = 0; s < GU_NA; ++s) {
@@ -100,109 +106,141 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   constexpr int NKB = HID / 64;
   const bool pp = p.pipe != nullptr;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ packed-tile producer
-      unsigned long long pc[1] = {0};
-      const unsigned long long t_role = pp ? clock64() : 0;
-      tma_prefetch_desc(&tm_qg);
-      tma_prefetch_desc(&tm_qu);
-      uint32_t it = 0;
-      bool alive = true;
-      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
-        if (!ti.ok) { atomicOr(p.err, ERRBIT_BOUNDS); continue; }
-        const bool sh = ti.e == SHARED_E;
-        const CUtensorMap* mg = sh ? &tm_sqg : &tm_qg;
-        const CUtensorMap* mu = sh ? &tm_squ : &tm_qu;
-        const int wrow = (sh ? 0 : ti.e * INTER) + ti.mb * GX_BM;
-        for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % GU_NP;
-          if (!mbar_wait_t(PEMPTY(s), ((it / GU_NP) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) {
-            alive = false;
-            break;
+  // Registers by warpgroup (setmaxnreg, executed by all four warps of a group at the
+  // top of its branch): the copy and MMA-issue warpgroups 0-1 hand theirs to the dequant
+  // and epilogue warpgroups 2-4.  Launch: 640 x 96 = 61,440; after: 128 x (64 + 64 +
+  // 112 + 112 + 112) = 59,392.
+  static_assert(GU_THREADS == 640 && GU_GW == 6, "register split assumes 5 warpgroups");
+  if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;");
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------ packed-tile producer
+        unsigned long long pc[1] = {0};
+        const unsigned long long t_role = pp ? clock64() : 0;
+        tma_prefetch_desc(&tm_qg);
+        tma_prefetch_desc(&tm_qu);
+        const uint64_t pol = l2_policy_evict_first();   // each weight tile is read by one CTA once
+        uint32_t it = 0;
+        bool alive = true;
+        for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+          const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+          if (!ti.ok) { atomicOr(p.err, ERRBIT_BOUNDS); continue; }
+          const bool sh = ti.e == SHARED_E;
+          const CUtensorMap* mg = sh ? &tm_sqg : &tm_qg;
+          const CUtensorMap* mu = sh ? &tm_squ : &tm_qu;
+          const int wrow = (sh ? 0 : ti.e * INTER) + ti.mb * GX_BM;
+          for (int kb = 0; kb < NKB; ++kb, ++it) {
+            const int s = it % GU_NP;
+            if (!mbar_wait_t(PEMPTY(s), ((it / GU_NP) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) {
+              alive = false;
+              break;
+            }
+            const uint32_t st = smem_u32(smem + OFF_P + s * GU_P_STAGE);
+            mbar_arrive_expect_tx(PFULL(s), GU_P_STAGE);
+            tma_load_2d_hint(st, mg, PFULL(s), kb * 8, wrow, pol);
+            tma_load_2d_hint(st + GX_P_BYTES, mu, PFULL(s), kb * 8, wrow, pol);
           }
-          const uint32_t st = smem_u32(smem + OFF_P + s * GU_P_STAGE);
-          mbar_arrive_expect_tx(PFULL(s), GU_P_STAGE);
-          tma_load_2d(st, mg, PFULL(s), kb * 8, wrow);
-          tma_load_2d(st + GX_P_BYTES, mu, PFULL(s), kb * 8, wrow);
+        }
+        if (!alive) {
+          for (uint32_t i = (it > GU_NP ? it - GU_NP : 0); i < it; ++i) drain_wait(PFULL(i % GU_NP), (i / GU_NP) & 1);
+        }
+        if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        unsigned long long pc[3] = {0, 0, 0};
+        const unsigned long long t_role = pp ? clock64() : 0;
+        uint32_t it = 0, tc = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+          const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+          if (!ti.ok) continue;
+          const int N = max(16, (ti.n_rows + 15) & ~15);
+          const uint32_t idesc = idesc_bf16(128, N);
+          if (!mbar_wait_t(ACCE, (tc & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
+          tc_fence_after();
+          bool alive = true;
+          for (int kb = 0; kb < NKB; ++kb, ++it) {
+            const int sa = it % GU_NA, sx = it % GU_NX;
+            if (!mbar_wait_t(AFULL(sa), (it / GU_NA) & 1, p.err, abort_flag, pc[1], pp) ||
+                !mbar_wait_t(XFULL(sx), (it / GU_NX) & 1, p.err, abort_flag, pc[2], pp)) {
+              alive = false;
+              break;
+            }
+            fence_proxy_async_smem();   // the activation stage was written by cp.async (generic proxy)
+            tc_fence_after();
+            const uint32_t a = smem_u32(smem + OFF_A + sa * GU_A_STAGE);
+            const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = sdesc_sw128(x + kk * 32);
+              const uint32_t acc = (kb | kk) != 0;
+              umma_bf16(tmem, sdesc_sw128(a + kk * 32), bd, idesc, acc);
+              umma_bf16(tmem + 256, sdesc_sw128(a + GX_A_BYTES + kk * 32), bd, idesc, acc);
+            }
+            umma_commit(AEMPTY(sa));
+            umma_commit(XEMPTY(sx));
+          }
+          if (!alive) break;
+          umma_commit(ACCF);
+          ++tc;
+        }
+        umma_commit(DRAIN);
+        if (pp) {
+          pipe_flush(p.pipe, 0, pc, 3, clock64() - t_role, 3);
+          atomicAdd(p.pipe + 10, static_cast<unsigned long long>(tc));
         }
       }
-      if (!alive) {
-        for (uint32_t i = (it > GU_NP ? it - GU_NP : 0); i < it; ++i) drain_wait(PFULL(i % GU_NP), (i / GU_NP) & 1);
-      }
-      if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
-    }
-  } else if (warp == 14) {
-    if (lane == 0) {
-      // ------------------------------------------------ activation-tile producer
-      tma_prefetch_desc(&tm_x);
+    } else {
+      // ------------------------------------------------ activation gather (GU_GW warps)
+      // Warp g copies rows g, g + GU_GW, g + 2 GU_GW, ... of every tile, so the gather
+      // warps never wait on each other (each decides alone to stop on an abort).
+      const int gw = warp - 2;
+      int* tok = s_tok + gw * GU_GROWS;
+      const int n8 = 8 * p.T;
+      const uint64_t pol = l2_policy_evict_last();   // every token row is read by about nine tiles
       uint32_t it = 0;
       bool alive = true;
       for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
-        if (!ti.ok) continue;
-        const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
-        for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % GU_NX;
-          if (!mbar_wait(XEMPTY(s), ((it / GU_NX) & 1) ^ 1, p.err, abort_flag)) { alive = false; break; }
-          const uint32_t st = smem_u32(smem + OFF_X + s * GX_X_BYTES);
-          mbar_arrive_expect_tx(XFULL(s), nbox * GX_XBOX * 128);
-          for (int j = 0; j < nbox; ++j)
-            tma_load_2d(st + j * GX_XBOX * 128, &tm_x, XFULL(s), kb * 64, ti.row0 + j * GX_XBOX);
-        }
-      }
-      if (!alive) {
-        for (uint32_t i = (it > GU_NX ? it - GU_NX : 0); i < it; ++i) drain_wait(XFULL(i % GU_NX), (i / GU_NX) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      unsigned long long pc[3] = {0, 0, 0};
-      const unsigned long long t_role = pp ? clock64() : 0;
-      uint32_t it = 0, tc = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
         const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
         if (!ti.ok) continue;
         const int N = max(16, (ti.n_rows + 15) & ~15);
-        const uint32_t idesc = idesc_bf16(128, N);
-        if (!mbar_wait_t(ACCE, (tc & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
-        tc_fence_after();
-        bool alive = true;
-        for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int sa = it % GU_NA, sx = it % GU_NX;
-          if (!mbar_wait_t(AFULL(sa), (it / GU_NA) & 1, p.err, abort_flag, pc[1], pp) ||
-              !mbar_wait_t(XFULL(sx), (it / GU_NX) & 1, p.err, abort_flag, pc[2], pp)) {
-            alive = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a = smem_u32(smem + OFF_A + sa * GU_A_STAGE);
-          const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(x + kk * 32);
-            const uint32_t acc = (kb | kk) != 0;
-            umma_bf16(tmem, sdesc_sw128(a + kk * 32), bd, idesc, acc);
-            umma_bf16(tmem + 256, sdesc_sw128(a + GX_A_BYTES + kk * 32), bd, idesc, acc);
-          }
-          umma_commit(AEMPTY(sa));
-          umma_commit(XEMPTY(sx));
+        const int nr = (N - gw + GU_GW - 1) / GU_GW;   // this warp's rows
+        // token of each of this warp's rows (rows past n_rows repeat the first, unused)
+        __syncwarp();   // the previous tile's reads of tok are done
+        for (int i = lane; i < nr; i += 32) {
+          const int r = gw + GU_GW * i;
+          const int row = ti.row0 + (r < ti.n_rows ? r : 0);
+          int t = row >= n8 ? row - n8 : (__ldg(p.row_dst + row) >> 3);
+          if (t < 0 || t >= p.T) { atomicOr(p.err, ERRBIT_BOUNDS); t = 0; }
+          tok[i] = t;
         }
-        if (!alive) break;
-        umma_commit(ACCF);
-        ++tc;
+        __syncwarp();
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % GU_NX;
+          alive = __all_sync(0xffffffffu, mbar_wait(XEMPTY(s), ((it / GU_NX) & 1) ^ 1, p.err, abort_flag));
+          if (!alive) break;
+          uint8_t* st = smem + OFF_X + s * GX_X_BYTES;
+          for (int q = lane; q < nr * 8; q += 32) {
+            const int i = q >> 3, c = q & 7;
+            const __nv_bfloat16* src = p.x_ilv + static_cast<size_t>(tok[i]) * HID + kb * 64 + c * 8;
+            asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                             smem_u32(st + sw128_off(gw + GU_GW * i, c))),
+                         "l"(src), "l"(pol)
+                         : "memory");
+          }
+          // one arrival per thread once its copies into the stage have landed; the MMA
+          // issuer fences them into the async proxy after its wait
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(XFULL(s)) : "memory");
+        }
       }
-      umma_commit(DRAIN);
-      if (pp) {
-        pipe_flush(p.pipe, 0, pc, 3, clock64() - t_role, 3);
-        atomicAdd(p.pipe + 10, static_cast<unsigned long long>(tc));
-      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
-  } else if (warp < 10) {
+  } else if (warp < 16) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 112;");
     // ------------------------------------------------ dequant (8 warps)
-    const int dt = tid - 64;           // 0..255
+    const int dt = tid - (2 + GU_GW) * 32;   // 0..255
     const int mat = dt >> 7;           // 0: gate rows, 1: up rows
     const int r = dt & 127;            // row inside the tile
     unsigned long long pc[1] = {0};
@@ -279,6 +317,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     }
     if (pp && dt == 0) pipe_flush(p.pipe, 6, pc, 1, clock64() - t_role, 7);
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 112;");
     // ------------------------------------------------ epilogue (4 warps): SwiGLU
     // While these warps drain TMEM, the dequant warps already fill the next tile's stages.
     const int q = warp & 3;            // TMEM lane quarter this warp may access
@@ -305,17 +344,17 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       const int f = ti.mb * GX_BM + q * 32 + lane;   // intermediate feature of this lane
       const int hcol = ilv_pos(f);
 #pragma unroll
-      for (int cc = 0; cc < GX_BN / 32; ++cc) {
-        const int col0 = cc * 32;
+      for (int cc = 0; cc < GX_BN / 16; ++cc) {
+        const int col0 = cc * 16;
         if (col0 >= ti.n_rows) break;
-        uint32_t g[32], u[32];
-        tmem_ld32(tl + col0, g);
-        tmem_ld32(tl + 256 + col0, u);
+        uint32_t g[16], u[16];
+        tmem_ld16(tl + col0, g);
+        tmem_ld16(tl + 256 + col0, u);
         tmem_ld_wait();
         __nv_bfloat16* hp = p.h + static_cast<size_t>(ti.row0 + col0) * INTER + hcol;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, wv[cc], j);
+        for (int j = 0; j < 16; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, wv[cc >> 1], (cc & 1) * 16 + j);
           if (col0 + j < ti.n_rows) {
             const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
             // silu(g) = g * sigmoid(g), sigmoid(g) = (1 + tanh(g/2)) / 2 with the hardware
@@ -331,7 +370,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       mbar_arrive(ACCE);
       ++tc;
     }
-    if (pp && warp == 10 && lane == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
+    if (pp && warp == 2 + GU_GW + 8 && lane == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
   }
 
   // ------------------------------------------------ teardown
@@ -389,9 +428,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 }
 
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
-                          const CUtensorMap& squ, const CUtensorMap& xperm, const GateUpParams& p, int grid,
-                          cudaStream_t s) {
-  gateup_kernel<<<grid, GU_THREADS, GU_SMEM, s>>>(qg, qu, sqg, squ, xperm, p);
+                          const CUtensorMap& squ, const GateUpParams& p, int grid, cudaStream_t s) {
+  gateup_kernel<<<grid, GU_THREADS, GU_SMEM, s>>>(qg, qu, sqg, squ, p);
   return cudaGetLastError();
 }
 

@@ -39,8 +39,8 @@ struct ScatterParams {
   float* row_w;       // [9T] routing weight (routed rows) or shared-gate sigmoid (shared rows)
   const __nv_bfloat16* x;
   const __nv_bfloat16* shared_gate_w;   // [2048]
-  __nv_bfloat16* x_perm;   // [9T][2048], K-interleaved rows
-  int gather;
+  __nv_bfloat16* x_ilv;    // [T][2048] copy of x with K-interleaved rows (read by the gate/up gather)
+  int gather;              // 0: routing tables only (moe_route)
   unsigned int* err;
 };
 
@@ -57,6 +57,8 @@ struct GateUpParams {
   unsigned int* err;
   unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
   const float* row_w;         // [9T] weight of each permuted row
+  const __nv_bfloat16* x_ilv; // [T][2048] K-interleaved activations, gathered by token
+  const int* row_dst;         // [9T] slot id (t*8+k) of each routed permuted row
 };
 
 struct DownParams {
@@ -147,8 +149,7 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
 cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s);
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
-                          const CUtensorMap& squ, const CUtensorMap& xperm, const GateUpParams& p, int grid,
-                          cudaStream_t s);
+                          const CUtensorMap& squ, const GateUpParams& p, int grid, cudaStream_t s);
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const DownParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const __nv_bfloat16* y, const __nv_bfloat16* x, __nv_bfloat16* out, int T,

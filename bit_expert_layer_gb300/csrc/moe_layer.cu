@@ -40,7 +40,7 @@ struct moe_layer {
   float* topk_w;
   int* row_dst;
   float* row_w;
-  __nv_bfloat16 *x_perm, *h, *y, *x_io, *xn;
+  __nv_bfloat16 *x_ilv, *h, *y, *x_io, *xn;
   float* dec_logits;
   int* dec_act_expert;
   float* dec_act_w;
@@ -52,7 +52,7 @@ struct moe_layer {
   unsigned long long* dec_xt;
   unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
-  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_xperm, tm_h;
+  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h;
 };
 
 namespace {
@@ -178,7 +178,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->topk_w = c.take<float>(static_cast<size_t>(Tm) * TOPK * 4);
   d->row_dst = c.take<int>(rows * 4);
   d->row_w = c.take<float>(rows * 4);
-  d->x_perm = c.take<__nv_bfloat16>(rows * HID * 2);
+  d->x_ilv = c.take<__nv_bfloat16>(static_cast<size_t>(Tm) * HID * 2);
   d->h = c.take<__nv_bfloat16>(rows * INTER * 2);
   d->y = c.take<__nv_bfloat16>(rows * HID * 2);
   d->x_io = c.take<__nv_bfloat16>(static_cast<size_t>(Tm) * HID * 2);
@@ -274,7 +274,7 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
   ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->row_w,
                     static_cast<const __nv_bfloat16*>(x),
-                    static_cast<const __nv_bfloat16*>(L->w.shared_gate_w), L->x_perm, gather, L->err};
+                    static_cast<const __nv_bfloat16*>(L->w.shared_gate_w), L->x_ilv, gather, L->err};
   MOE_TRY(timed(K_SCATTER, s, L->err, [&] { return launch_scatter(scp, nblk, s); }), "scatter launch");
   return MOE_OK;
 }
@@ -390,14 +390,14 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->row_w};
+                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->row_w, L->x_ilv, L->row_dst};
   // upper bound of the tile count: every touched expert adds at most one partial token block
   const long long tok_blocks = (8ll * T + GX_BN - 1) / GX_BN + (8ll * T < NEXP ? 8ll * T : NEXP) +
                                (T + GX_BN - 1) / GX_BN;
   const int grid_gu = static_cast<int>(tok_blocks * GU_MBLK < L->num_sms ? tok_blocks * GU_MBLK : L->num_sms);
   const int grid_dn = static_cast<int>(tok_blocks * DN_MBLK < L->num_sms ? tok_blocks * DN_MBLK : L->num_sms);
   MOE_TRY(timed(K_GATEUP, s, L->err,
-                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_xperm, gp, grid_gu, s); }),
+                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, gp, grid_gu, s); }),
           "gate/up launch");
   DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->row_dst, L->row_w, L->y, T, L->err,
@@ -487,7 +487,6 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
             encode_packed(&L->tm_squ, weights->sh_up.q, HID / 8, SH_INTER) &&
             encode_packed(&L->tm_qd, weights->down.q, INTER / 8, static_cast<uint64_t>(NEXP) * HID) &&
             encode_packed(&L->tm_sqd, weights->sh_down.q, SH_INTER / 8, HID) &&
-            encode_bf16_rows(&L->tm_xperm, L->x_perm, HID, 9ull * Tm, GX_XBOX) &&
             encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX);
   if (!ok) return fail(MOE_ERR_CUDA);
   *out = L;

@@ -12,10 +12,11 @@
 //   route_scan_kernel      per-expert counts, exclusive-scan offsets, the first
 //                          permuted row of every (router block, expert), and the
 //                          tile tables of both grouped GEMMs.
-//   route_scatter_kernel   stable permutation of the slots t*8+k into expert order,
-//                          the per-row weight, the gather of x into x_perm (8 routed
-//                          copies + 1 shared copy per token) and, on the same read of
-//                          x, the shared-expert gate sigmoid(g_s . x).
+//   route_scatter_kernel   stable permutation of the slots t*8+k into expert order and
+//                          the per-row weight (first CTA of each router block), one
+//                          K-interleaved copy of x per token (the gate/up GEMM gathers
+//                          its rows from it by token) and, on the same read of x, the
+//                          shared-expert gate sigmoid(g_s . x).
 #include "common.cuh"
 #include "internal.h"
 
@@ -249,11 +250,12 @@ __global__ void __launch_bounds__(256) route_scan_kernel(ScanParams p) {
 __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams p) {
   constexpr int SLOTS = RT_BM * TOPK;   // 1024 slots per router block
   __shared__ int idx_s[SLOTS];
-  __shared__ int pos_s[SLOTS];
   __shared__ int wh[8][NEXP];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slot0 = b * SLOTS;
   const int nslots = min(SLOTS, p.T * TOPK - slot0);
+  const int n8 = 8 * p.T;
+  if (blockIdx.y == 0) {
   for (int i = tid; i < SLOTS; i += SC_THREADS) {
     int e = (i < nslots) ? p.topk_idx[slot0 + i] : -1;
     if (e >= NEXP || e < -1) {   // never index shared memory with a bad expert id
@@ -284,7 +286,6 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   }
   __syncthreads();
   // pass 3: stable ranks, slot order inside each warp's range
-  const int n8 = 8 * p.T;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int s = warp * 128 + j * 32 + lane;
@@ -300,19 +301,19 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
       atomicOr(p.err, ERRBIT_BOUNDS);
       pos = -1;
     }
-    pos_s[s] = pos;
     if (pos >= 0) {
       p.row_dst[pos] = slot0 + s;
       p.row_w[pos] = p.topk_w[slot0 + s];
     }
   }
-  __syncthreads();
+  }   // blockIdx.y == 0
   if (!p.gather) return;
-  // gather: one warp per token; one read of x, nine interleaved copies, and the
-  // shared-expert gate on the same read
-  const int t0 = b * RT_BM;
+  // one warp per token: one read of x, one K-interleaved copy (the gate/up GEMM gathers
+  // its rows from it by token), and the shared-expert gate on the same read
+  constexpr int TPC = RT_BM / SC_SPLIT;   // tokens of this CTA
+  const int t0 = b * RT_BM + blockIdx.y * TPC;
   const uint4* gsv = reinterpret_cast<const uint4*>(p.shared_gate_w);
-  for (int tl = warp; tl < RT_BM; tl += SC_THREADS / 32) {
+  for (int tl = warp; tl < TPC; tl += SC_THREADS / 32) {
     const int t = t0 + tl;
     if (t >= p.T) break;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * HID);
@@ -339,14 +340,9 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
       p.row_dst[srow] = srow;
       p.row_w[srow] = 1.0f / (1.0f + expf(-dot));
     }
-#pragma unroll 1
-    for (int k = 0; k <= TOPK; ++k) {
-      const int pos = (k < TOPK) ? pos_s[tl * TOPK + k] : n8 + t;
-      if (pos < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(p.x_perm + static_cast<size_t>(pos) * HID);
+    uint4* dst = reinterpret_cast<uint4*>(p.x_ilv + static_cast<size_t>(t) * HID);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) dst[lane + 32 * c] = v[c];
-    }
+    for (int c = 0; c < 8; ++c) dst[lane + 32 * c] = v[c];
   }
 }
 
@@ -411,7 +407,7 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
-  route_scatter_kernel<<<nblk, SC_THREADS, 0, s>>>(p);
+  route_scatter_kernel<<<dim3(nblk, SC_SPLIT), SC_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 
