@@ -59,13 +59,16 @@ constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS 
 constexpr int GU_THREADS = (14 + GU_GW) * 32;   // packed producer, MMA, 8 dequant, 4 epilogue, gather warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
-constexpr int DN_STAGES = 4;
-constexpr int DN_STAGE_BYTES = GX_A_BYTES + GX_X_BYTES + GX_P_BYTES;
-// + barriers, and per epilogue warp a 256-row table of (destination row, weight)
-// + alignment slack, barriers (256 B), row tables (2 KB), 32-row staging (8 KB), tile tables
-constexpr int DN_SMEM = DN_STAGES * DN_STAGE_BYTES + 1024 + 256 + GX_BN * 8 + 32 * GX_BM * 2 + GX_TAB_BYTES;
+// down: rings of packed tiles (4 KB), activation tiles (32 KB) and dequantised tiles (16 KB)
+constexpr int DN_NP = 8;
+constexpr int DN_NX = 3;
+constexpr int DN_NA = 3;
+constexpr int DN_RINGS = DN_NP * GX_P_BYTES + DN_NX * GX_X_BYTES + DN_NA * GX_A_BYTES;
+// + alignment slack, barriers and words (1 KB), destination rows (1 KB), 32-row staging
+// (8 KB), tile tables
+constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + GX_BN * 4 + 32 * GX_BM * 2 + GX_TAB_BYTES;
 static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
-constexpr int DN_THREADS = 448;                     // producer, MMA, 8 dequant, 4 epilogue warps
+constexpr int DN_THREADS = 480;   // packed producer, MMA, 8 dequant, 4 epilogue, activation producer
 constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
 
 // scatter: per router block of 128 tokens (1024 slots), SC_SPLIT CTAs; the first also

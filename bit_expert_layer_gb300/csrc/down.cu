@@ -7,13 +7,18 @@
 //
 // A tile is 128 output features (M) x up to 256 permuted rows (N); K = 512 is only 8
 // steps of 64, so one tile's MMAs take ~2 us and the dequant and epilogue have to keep
-// pace with that.  Warp roles (14 warps):
-//   warp 0      TMA producer (packed 4-bit tile + activation rows h)
+// pace with that.  Warp roles (15 warps):
+//   warp 0      TMA producer of the packed 4-bit tiles (ring of DN_NP, 4 KB stages)
 //   warp 1      TMEM allocator and MMA issuer (double-buffered 128 x 256 accumulator)
-//   warps 2-9   dequant: two threads per weight row, four packed words each
+//   warps 2-9   dequant: two threads per weight row, four packed words each (ring of
+//               DN_NA dequantised 16 KB tiles)
 //   warps 10-13 epilogue: per 32-row chunk, round to bf16, transpose through shared
 //               memory and write each destination row's 128 features (256 B) with
 //               16-byte stores
+//   warp 14     TMA producer of the activation rows h' (ring of DN_NX, 32 KB stages)
+// The rings are separate so the small packed tiles, which come from HBM, run further
+// ahead than the activation tiles, which each expert's 16 row blocks re-read from L2
+// (evict-last) while the weights stream through it (evict-first).
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "internal.h"
@@ -21,9 +26,12 @@
 namespace moe {
 
 namespace {
-constexpr int DN_A = 0;                              // dequantised weight tile
-constexpr int DN_X = GX_A_BYTES;                     // activation rows
-constexpr int DN_P = GX_A_BYTES + GX_X_BYTES;        // packed 4-bit tile
+// shared-memory layout (1024-byte aligned base)
+constexpr int OFF_A = 0;                                   // [DN_NA][16 KB]
+constexpr int OFF_X = OFF_A + DN_NA * GX_A_BYTES;          // [DN_NX][32 KB]
+constexpr int OFF_P = OFF_X + DN_NX * GX_X_BYTES;          // [DN_NP][4 KB]
+constexpr int OFF_MISC = OFF_P + DN_NP * GX_P_BYTES;
+static_assert(OFF_X % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 constexpr int EPI_BAR = 1;                           // named barrier of the epilogue warps
 constexpr int STG_ROW = GX_BM * 2;                   // bytes of one staged row (128 bf16)
 
@@ -37,12 +45,12 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
                 const __grid_constant__ CUtensorMap tm_h, DownParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* misc = smem + DN_STAGES * DN_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                       // 256 B
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 196);
-  int* md_dst = reinterpret_cast<int*>(misc + 256);                          // [256] destination rows
-  uint8_t* stg = misc + 256 + GX_BN * 8;                                     // [32][128] bf16 staging
+  uint8_t* misc = smem + OFF_MISC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                       // 40 barriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
+  int* md_dst = reinterpret_cast<int*>(misc + 1024);                         // [256] destination rows
+  uint8_t* stg = misc + 1024 + GX_BN * 4;                                    // [32][128] bf16 staging
   int* s_tiles = reinterpret_cast<int*>(stg + 32 * STG_ROW);
   int* s_off = s_tiles + (NEXP + 2);
   int* s_cnt = s_off + (NEXP + 2);
@@ -50,19 +58,30 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
-  // full 0..3, afull 4..7, empty 8..11, accf 12..13, acce 14..15, drain 16
-#define FULL(s) (bar0 + 8u * (s))
-#define AFULL(s) (bar0 + 8u * (4 + (s)))
-#define EMPTY(s) (bar0 + 8u * (8 + (s)))
-#define ACCF(b) (bar0 + 8u * (12 + (b)))
-#define ACCE(b) (bar0 + 8u * (14 + (b)))
-  const uint32_t DRAIN = bar0 + 8u * 16;
+#define PFULL(s) (bar0 + 8u * (s))
+#define PEMPTY(s) (bar0 + 8u * (DN_NP + (s)))
+#define XFULL(s) (bar0 + 8u * (2 * DN_NP + (s)))
+#define XEMPTY(s) (bar0 + 8u * (2 * DN_NP + DN_NX + (s)))
+#define AFULL(s) (bar0 + 8u * (2 * DN_NP + 2 * DN_NX + (s)))
+#define AEMPTY(s) (bar0 + 8u * (2 * DN_NP + 2 * DN_NX + DN_NA + (s)))
+  constexpr int NB = 2 * DN_NP + 2 * DN_NX + 2 * DN_NA;
+  static_assert(NB + 5 <= 64, "barrier space");
+#define ACCF(b) (bar0 + 8u * (NB + (b)))
+#define ACCE(b) (bar0 + 8u * (NB + 2 + (b)))
+  const uint32_t DRAIN = bar0 + 8u * (NB + 4);
 
   if (tid == 0) {
-    for (int s = 0; s < DN_STAGES; ++s) {
-      mbar_init(FULL(s), 1);
+    for (int s = 0; s < DN_NP; ++s) {
+      mbar_init(PFULL(s), 1);
+      mbar_init(PEMPTY(s), 256);
+    }
+    for (int s = 0; s < DN_NX; ++s) {
+      mbar_init(XFULL(s), 1);
+      mbar_init(XEMPTY(s), 1);
+    }
+    for (int s = 0; s < DN_NA; ++s) {
       mbar_init(AFULL(s), 256);
-      mbar_init(EMPTY(s), 1);
+      mbar_init(AEMPTY(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(ACCF(b), 1);
@@ -85,12 +104,13 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
+      // ------------------------------------------------ packed-tile producer
       const bool pp = p.pipe != nullptr;
       unsigned long long pc[1] = {0};
       const unsigned long long t_role = pp ? clock64() : 0;
       tma_prefetch_desc(&tm_qd);
-      tma_prefetch_desc(&tm_h);
+      tma_prefetch_desc(&tm_sqd);
+      const uint64_t pol = l2_policy_evict_first();   // each weight tile is read once
       uint32_t it = 0;
       bool alive = true;
       for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
@@ -99,24 +119,41 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const bool sh = ti.e == SHARED_E;
         const CUtensorMap* mq = sh ? &tm_sqd : &tm_qd;
         const int wrow = (sh ? 0 : ti.e * HID) + ti.mb * GX_BM;
-        const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
-        const uint32_t bytes = GX_P_BYTES + nbox * GX_XBOX * 128;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % DN_STAGES;
-          const uint32_t ph = (it / DN_STAGES) & 1;
-          if (!mbar_wait_t(EMPTY(s), ph ^ 1, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
-          const uint32_t st = smem_u32(smem + s * DN_STAGE_BYTES);
-          mbar_arrive_expect_tx(FULL(s), bytes);
-          tma_load_2d(st + DN_P, mq, FULL(s), kb * 8, wrow);
-          for (int j = 0; j < nbox; ++j)
-            tma_load_2d(st + DN_X + j * GX_XBOX * 128, &tm_h, FULL(s), kb * 64, ti.row0 + j * GX_XBOX);
+          const int s = it % DN_NP;
+          if (!mbar_wait_t(PEMPTY(s), ((it / DN_NP) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
+          mbar_arrive_expect_tx(PFULL(s), GX_P_BYTES);
+          tma_load_2d_hint(smem_u32(smem + OFF_P + s * GX_P_BYTES), mq, PFULL(s), kb * 8, wrow, pol);
         }
       }
       if (!alive) {
-        for (uint32_t i = (it > DN_STAGES ? it - DN_STAGES : 0); i < it; ++i)
-          drain_wait(FULL(i % DN_STAGES), (i / DN_STAGES) & 1);
+        for (uint32_t i = (it > DN_NP ? it - DN_NP : 0); i < it; ++i) drain_wait(PFULL(i % DN_NP), (i / DN_NP) & 1);
       }
       if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
+    }
+  } else if (warp == 14) {
+    if (lane == 0) {
+      // ------------------------------------------------ activation-tile producer
+      tma_prefetch_desc(&tm_h);
+      const uint64_t pol = l2_policy_evict_last();    // each h' block is read by 16 row blocks
+      uint32_t it = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+        if (!ti.ok) continue;
+        const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % DN_NX;
+          if (!mbar_wait(XEMPTY(s), ((it / DN_NX) & 1) ^ 1, p.err, abort_flag)) { alive = false; break; }
+          const uint32_t st = smem_u32(smem + OFF_X + s * GX_X_BYTES);
+          mbar_arrive_expect_tx(XFULL(s), nbox * GX_XBOX * 128);
+          for (int j = 0; j < nbox; ++j)
+            tma_load_2d_hint(st + j * GX_XBOX * 128, &tm_h, XFULL(s), kb * 64, ti.row0 + j * GX_XBOX, pol);
+        }
+      }
+      if (!alive) {
+        for (uint32_t i = (it > DN_NX ? it - DN_NX : 0); i < it; ++i) drain_wait(XFULL(i % DN_NX), (i / DN_NX) & 1);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -136,20 +173,20 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const uint32_t d = tmem + buf * 256;
         bool alive = true;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % DN_STAGES;
-          const uint32_t ph = (it / DN_STAGES) & 1;
-          if (!mbar_wait_t(AFULL(s), ph, p.err, abort_flag, pc[1], pp) ||
-              !mbar_wait_t(FULL(s), ph, p.err, abort_flag, pc[2], pp)) {
+          const int sa = it % DN_NA, sx = it % DN_NX;
+          if (!mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, pc[1], pp) ||
+              !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, pc[2], pp)) {
             alive = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * DN_STAGE_BYTES);
+          const uint32_t a = smem_u32(smem + OFF_A + sa * GX_A_BYTES);
+          const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, sdesc_sw128(st + DN_A + kk * 32), sdesc_sw128(st + DN_X + kk * 32), idesc,
-                      (kb | kk) != 0);
-          umma_commit(EMPTY(s));
+            umma_bf16(d, sdesc_sw128(a + kk * 32), sdesc_sw128(x + kk * 32), idesc, (kb | kk) != 0);
+          umma_commit(AEMPTY(sa));
+          umma_commit(XEMPTY(sx));
         }
         if (!alive) break;
         umma_commit(ACCF(buf));
@@ -195,21 +232,27 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
       for (int kb = 0; kb < NKB; ++kb) {
-        const int s = it % DN_STAGES;
-        const uint32_t ph = (it / DN_STAGES) & 1;
-        if (!mbar_wait_t(FULL(s), ph, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
+        const int sp = it % DN_NP, sa = it % DN_NA;
+        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, pc[0], pp) ||
+            !mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag)) {
+          alive = false;
+          break;
+        }
         ++it;
         const __nv_bfloat162 ms = bf2((kb & 1) ? (sw[kb >> 1] >> 16) : sw[kb >> 1]);
         const __nv_bfloat162 mbv = bf2((kb & 1) ? (bw[kb >> 1] >> 16) : bw[kb >> 1]);
-        uint8_t* st = smem + s * DN_STAGE_BYTES;
-        const uint4 w = *reinterpret_cast<const uint4*>(st + DN_P + r * 32 + hw * 16);
-        uint8_t* A = st + DN_A;
+        const uint4 w = *reinterpret_cast<const uint4*>(smem + OFF_P + sp * GX_P_BYTES + r * 32 + hw * 16);
+        // the packed words are in registers; the next TMA write into this stage is an
+        // async-proxy access, so the generic reads are fenced before the release
+        fence_proxy_async_smem();
+        mbar_arrive(PEMPTY(sp));
+        uint8_t* A = smem + OFF_A + sa * GX_A_BYTES;
         st_shared_v4(A + sw128_off(r, 4 * hw + 0), dequant8(w.x, ms, mbv));
         st_shared_v4(A + sw128_off(r, 4 * hw + 1), dequant8(w.y, ms, mbv));
         st_shared_v4(A + sw128_off(r, 4 * hw + 2), dequant8(w.z, ms, mbv));
         st_shared_v4(A + sw128_off(r, 4 * hw + 3), dequant8(w.w, ms, mbv));
         fence_proxy_async_smem();
-        mbar_arrive(AFULL(s));
+        mbar_arrive(AFULL(sa));
       }
     }
     if (pp && dt == 0) pipe_flush(p.pipe, 6, pc, 1, clock64() - t_role, 7);
@@ -290,9 +333,12 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
-#undef FULL
+#undef PFULL
+#undef PEMPTY
+#undef XFULL
+#undef XEMPTY
 #undef AFULL
-#undef EMPTY
+#undef AEMPTY
 #undef ACCF
 #undef ACCE
 }
