@@ -344,17 +344,21 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       const int f = ti.mb * GX_BM + q * 32 + lane;   // intermediate feature of this lane
       const int hcol = ilv_pos(f);
 #pragma unroll
-      for (int cc = 0; cc < GX_BN / 16; ++cc) {
-        const int col0 = cc * 16;
+      for (int cc = 0; cc < GX_BN / 32; ++cc) {
+        const int col0 = cc * 32;
         if (col0 >= ti.n_rows) break;
-        uint32_t g[16], u[16];
-        tmem_ld16(tl + col0, g);
-        tmem_ld16(tl + 256 + col0, u);
+        uint32_t g[32], u[32];
+        tmem_ld32(tl + col0, g);
+        tmem_ld32(tl + 256 + col0, u);
         tmem_ld_wait();
+        if (col0 + 32 >= ti.n_rows) {   // last chunk read: the MMA may overwrite the accumulator
+          tc_fence_before();
+          mbar_arrive(ACCE);
+        }
         __nv_bfloat16* hp = p.h + static_cast<size_t>(ti.row0 + col0) * INTER + hcol;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, wv[cc >> 1], (cc & 1) * 16 + j);
+        for (int j = 0; j < 32; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, wv[cc], j);
           if (col0 + j < ti.n_rows) {
             const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
             // silu(g) = g * sigmoid(g), sigmoid(g) = (1 + tanh(g/2)) / 2 with the hardware
@@ -366,8 +370,6 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(ACCE);
       ++tc;
     }
     if (pp && warp == 2 + GU_GW + 8 && lane == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
