@@ -64,9 +64,8 @@ constexpr int DN_NP = 8;
 constexpr int DN_NX = 3;
 constexpr int DN_NA = 3;
 constexpr int DN_RINGS = DN_NP * GX_P_BYTES + DN_NX * GX_X_BYTES + DN_NA * GX_A_BYTES;
-// + alignment slack, barriers and words (1 KB), destination rows (1 KB), 32-row staging
-// (8 KB), tile tables
-constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + GX_BN * 4 + 32 * GX_BM * 2 + GX_TAB_BYTES;
+// + alignment slack, barriers and words (1 KB), two 32-row staging buffers (16 KB), tile tables
+constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + 2 * 32 * GX_BM * 2 + GX_TAB_BYTES;
 static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
 constexpr int DN_THREADS = 480;   // packed producer, MMA, 8 dequant, 4 epilogue, activation producer
 constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
@@ -168,6 +167,20 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+// Shared -> global 2D tile store (bulk group); the smem source must stay untouched until
+// tma_store_wait_read says the copy has read it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // L2 policies: data read once (streamed weights) and data read again soon (activations)
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

@@ -1,4 +1,4 @@
-// down.cu -- the grouped down GEMM of the prefill path: y[row_dst] = W_down h' for every
+// down.cu -- the grouped down GEMM of the prefill path: y[row] = W_down h'[row] for every
 // permuted row (8 routed slots and 1 shared row per token), where h' already carries the
 // row's weight (applied by the gate/up epilogue), with the 4-bit weights dequantised
 // inside the kernel (Lily restores the 4-bit weights inside its
@@ -12,9 +12,11 @@
 //   warp 1      TMEM allocator and MMA issuer (double-buffered 128 x 256 accumulator)
 //   warps 2-9   dequant: two threads per weight row, four packed words each (ring of
 //               DN_NA dequantised 16 KB tiles)
-//   warps 10-13 epilogue: per 32-row chunk, round to bf16, transpose through shared
-//               memory and write each destination row's 128 features (256 B) with
-//               16-byte stores
+//   warps 10-13 epilogue: per 32-row chunk, round to bf16 into a shared-memory tile
+//               of 32 rows x 128 features and write it with one TMA store (y is kept in
+//               permuted-row order, so a chunk is one box; the combine reads each
+//               token's nine rows through the slot -> row map); two staging buffers
+//               alternate; a ragged last chunk is written with 16-byte stores
 //   warp 14     TMA producer of the activation rows h' (ring of DN_NX, 32 KB stages)
 // The rings are separate so the small packed tiles, which come from HBM, run further
 // ahead than the activation tiles, which each expert's 16 row blocks re-read from L2
@@ -38,20 +40,33 @@ constexpr int STG_ROW = GX_BM * 2;                   // bytes of one staged row 
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(EPI_BAR), "n"(128) : "memory");
 }
+// the epilogue barrier with a vote: true in every epilogue thread if any passed true
+__device__ __forceinline__ bool epi_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(EPI_BAR), "n"(128)
+      : "memory");
+  return r != 0;
+}
 }  // namespace
 
 __global__ void __launch_bounds__(DN_THREADS, 1)
     down_kernel(const __grid_constant__ CUtensorMap tm_qd, const __grid_constant__ CUtensorMap tm_sqd,
-                const __grid_constant__ CUtensorMap tm_h, DownParams p) {
+                const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_y,
+                DownParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* misc = smem + OFF_MISC;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                       // 40 barriers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
-  int* md_dst = reinterpret_cast<int*>(misc + 1024);                         // [256] destination rows
-  uint8_t* stg = misc + 1024 + GX_BN * 4;                                    // [32][128] bf16 staging
-  int* s_tiles = reinterpret_cast<int*>(stg + 32 * STG_ROW);
+  uint8_t* stg = misc + 1024;                                                // [2][32][128] bf16 staging
+  int* s_tiles = reinterpret_cast<int*>(stg + 2 * 32 * STG_ROW);
   int* s_off = s_tiles + (NEXP + 2);
   int* s_cnt = s_off + (NEXP + 2);
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
@@ -261,38 +276,21 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
     const int q = warp & 3;                       // TMEM lane quarter = features q*32..q*32+31
     const int te = tid - 320;                     // 0..127
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int nrows_all = 9 * p.T;
     const bool pp = p.pipe != nullptr;
     unsigned long long pc[1] = {0};
     const unsigned long long t_role = pp ? clock64() : 0;
-    uint32_t tc = 0;
+    if (te == 0) tma_prefetch_desc(&tm_y);
+    uint32_t tc = 0, nst = 0;                     // tiles done; TMA stores issued
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
       if (!ti.ok) continue;
-      // the rows' destinations, fetched before waiting for the accumulator (each row's
-      // weight was already applied to its h row by the gate/up epilogue)
-      int dv[2];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int j = c * 128 + te;
-        const bool valid = j < ti.n_rows;
-        dv[c] = valid ? __ldg(p.row_dst + ti.row0 + j) : -1;
-        if (valid && (dv[c] < 0 || dv[c] >= nrows_all)) {
-          atomicOr(p.err, ERRBIT_BOUNDS);
-          dv[c] = -1;
-        }
-      }
       const int buf = tc & 1;
       // the wait is bounded; all four warps then meet and leave together on an abort
-      mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, pc[0], pp);
-      epi_sync();                                 // also: the previous tile's tables are consumed
-      if (*abort_flag) break;
+      const bool got = mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, pc[0], pp);
+      if (epi_sync_or(!got || *abort_flag)) break;   // the same decision in all four warps
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) md_dst[c * 128 + te] = dv[c];
-      epi_sync();
       const int f = q * 32 + lane;                // feature inside the tile
-      const size_t fcol = static_cast<size_t>(ti.mb) * GX_BM;
+      const int fcol = ti.mb * GX_BM;
 #pragma unroll 1
       for (int cc = 0; cc < GX_BN / 32; ++cc) {
         const int col0 = cc * 32;
@@ -300,28 +298,41 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         uint32_t d[32];
         tmem_ld32(tl + buf * 256 + col0, d);
         tmem_ld_wait();
+        if (col0 + 32 >= ti.n_rows) {             // last chunk read: the MMA may reuse the buffer
+          tc_fence_before();
+          mbar_arrive(ACCE(buf));
+        }
+        uint8_t* sb = stg + (nst & 1) * 32 * STG_ROW;
+        // the TMA store issued from this buffer two chunks ago has read it
+        if (te == 0 && nst >= 2) tma_store_wait_read<1>();
+        epi_sync();
         // round and transpose: staged row j holds the chunk's row col0 + j
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          *reinterpret_cast<__nv_bfloat16*>(stg + j * STG_ROW + f * 2) = __float2bfloat16_rn(__uint_as_float(d[j]));
-        epi_sync();
-        // each staged row is 128 features = 16 segments of 16 bytes; 512 segments per chunk
+          *reinterpret_cast<__nv_bfloat16*>(sb + j * STG_ROW + f * 2) = __float2bfloat16_rn(__uint_as_float(d[j]));
+        if (col0 + 32 <= ti.n_rows) {
+          fence_proxy_async_smem();               // the generic writes, before the TMA reads them
+          epi_sync();
+          if (te == 0) tma_store_2d(&tm_y, smem_u32(sb), fcol, ti.row0 + col0);
+          ++nst;
+        } else {
+          // ragged last chunk: only its own rows (the next rows belong to other tiles)
+          epi_sync();
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int item = te + 128 * i;
-          const int j = item >> 4, seg = item & 15;
-          const int dst = md_dst[col0 + j];
-          if (col0 + j < ti.n_rows && dst >= 0) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + j * STG_ROW + seg * 16);
-            *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(dst) * HID + fcol + seg * 8) = v;
+          for (int i = 0; i < 4; ++i) {
+            const int item = te + 128 * i;
+            const int j = item >> 4, seg = item & 15;
+            if (col0 + j < ti.n_rows) {
+              const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + seg * 16);
+              *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.row0 + col0 + j) * HID + fcol + seg * 8) = v;
+            }
           }
+          epi_sync();                             // this buffer is free again
         }
-        epi_sync();                               // the staging rows are free again
       }
-      tc_fence_before();
-      mbar_arrive(ACCE(buf));
       ++tc;
     }
+    if (te == 0) tma_store_wait_all();
     if (pp && te == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
   }
 
@@ -344,8 +355,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 }
 
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
-                        const DownParams& p, int grid, cudaStream_t s) {
-  down_kernel<<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, p);
+                        const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s) {
+  down_kernel<<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, ymap, p);
   return cudaGetLastError();
 }
 

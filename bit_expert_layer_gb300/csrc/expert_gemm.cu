@@ -15,7 +15,8 @@
 //                  the permuted activations, w = the row's routing weight (the shared
 //                  expert, expert 256 over all T tokens, uses sigmoid(g_s . x)).  Two
 //                  TMEM accumulators (gate, up), SwiGLU in the epilogue.
-//   combine_kernel out[t] = sum_k y[8t+k] + y[8T+t] (+ x[t]) in a fixed order.
+//   combine_kernel out[t] = sum_k y[row(t,k)] + y[8T+t] (+ x[t]) in a fixed order,
+//                  row(t,k) = the permuted row of slot t*8+k.
 //
 // Warp roles of gateup_kernel (20 warps, one role per warpgroup but the first):
 //   warp 0      TMA producer of the packed 4-bit tiles (ring of GU_NP)
@@ -396,16 +397,22 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 // One CTA per token, 256 threads x 8 features; fixed summation order: the 8 routed
 // slots in rank order, then the shared expert, then the residual.
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y,
+                                                      const int* __restrict__ slot_row,
                                                       const __nv_bfloat16* x, __nv_bfloat16* out, int T,
                                                       int residual) {
   const int t = blockIdx.x, c = threadIdx.x;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  // the token's eight routed rows (y is in permuted-row order), then its shared-expert row
+  int rows[TOPK + 1];
+#pragma unroll
+  for (int k = 0; k < TOPK; ++k) rows[k] = __ldg(slot_row + static_cast<size_t>(t) * TOPK + k);
+  rows[TOPK] = 8 * T + t;
 #pragma unroll
   for (int k = 0; k <= TOPK; ++k) {
-    const size_t row = (k < TOPK) ? static_cast<size_t>(t) * TOPK + k : static_cast<size_t>(8 * T + t);
-    const uint4 v = ldg_nc_v4(y + row * HID + c * 8);
+    if (rows[k] < 0 || rows[k] >= 9 * T) continue;   // a slot the scatter rejected (error recorded)
+    const uint4 v = ldg_nc_v4(y + static_cast<size_t>(rows[k]) * HID + c * 8);
     acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x);
     acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
     acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z);
@@ -435,9 +442,9 @@ cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CU
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const __nv_bfloat16* y, const __nv_bfloat16* x, __nv_bfloat16* out, int T,
-                           int residual, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(y, x, out, T, residual);
+cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const __nv_bfloat16* x, __nv_bfloat16* out,
+                           int T, int residual, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, x, out, T, residual);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,7 @@ struct ScatterParams {
   const int* base;
   int T;
   int* row_dst;       // [9T] routed part: the permutation of slot ids; shared part: 8T+t
+  int* slot_row;      // [8T] inverse: the permuted row of slot t*8+k
   float* row_w;       // [9T] routing weight (routed rows) or shared-gate sigmoid (shared rows)
   const __nv_bfloat16* x;
   const __nv_bfloat16* shared_gate_w;   // [2048]
@@ -67,9 +68,7 @@ struct DownParams {
   const int* counts;
   const uint16_t* d_scales; const uint16_t* d_biases;    // [256][2048][8]
   const uint16_t* sd_scales; const uint16_t* sd_biases;  // [2048][8]
-  const int* row_dst;
-  const float* row_w;
-  __nv_bfloat16* y;      // [9T][2048]
+  __nv_bfloat16* y;      // [9T][2048] by permuted row (written through a TMA map)
   int T;
   unsigned int* err;
   unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
@@ -151,9 +150,9 @@ cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s);
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
                           const CUtensorMap& squ, const GateUpParams& p, int grid, cudaStream_t s);
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
-                        const DownParams& p, int grid, cudaStream_t s);
-cudaError_t launch_combine(const __nv_bfloat16* y, const __nv_bfloat16* x, __nv_bfloat16* out, int T,
-                           int residual, cudaStream_t s);
+                        const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s);
+cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const __nv_bfloat16* x, __nv_bfloat16* out,
+                           int T, int residual, cudaStream_t s);
 cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s);
 cudaError_t set_kernel_attributes();

@@ -39,6 +39,7 @@ struct moe_layer {
   int* topk_idx;
   float* topk_w;
   int* row_dst;
+  int* slot_row;
   float* row_w;
   __nv_bfloat16 *x_ilv, *h, *y, *x_io, *xn;
   float* dec_logits;
@@ -52,7 +53,7 @@ struct moe_layer {
   unsigned long long* dec_xt;
   unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
-  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h;
+  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h, tm_y;
 };
 
 namespace {
@@ -178,6 +179,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->topk_w = c.take<float>(static_cast<size_t>(Tm) * TOPK * 4);
   d->row_dst = c.take<int>(rows * 4);
   d->row_w = c.take<float>(rows * 4);
+  d->slot_row = c.take<int>(static_cast<size_t>(Tm) * TOPK * 4);
   d->x_ilv = c.take<__nv_bfloat16>(static_cast<size_t>(Tm) * HID * 2);
   d->h = c.take<__nv_bfloat16>(rows * INTER * 2);
   d->y = c.take<__nv_bfloat16>(rows * HID * 2);
@@ -272,7 +274,7 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   MOE_TRY(timed(K_ROUTER, s, L->err, [&] { return launch_router_prefill(tm_x, L->tm_wr, rp, s); }), "router launch");
   ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->tiles_gu, L->tiles_dn};
   MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
-  ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->row_w,
+  ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->slot_row, L->row_w,
                     static_cast<const __nv_bfloat16*>(x),
                     static_cast<const __nv_bfloat16*>(L->w.shared_gate_w), L->x_ilv, gather, L->err};
   MOE_TRY(timed(K_SCATTER, s, L->err, [&] { return launch_scatter(scp, nblk, s); }), "scatter launch");
@@ -400,12 +402,12 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
                 [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, gp, grid_gu, s); }),
           "gate/up launch");
   DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
-                U16(w.sh_down.scales), U16(w.sh_down.biases), L->row_dst, L->row_w, L->y, T, L->err,
+                U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
                 pipe_trace() ? L->pipe + 16 : nullptr};
-  MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_dn, s); }), "down launch");
+  MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
-                  return launch_combine(L->y, static_cast<const __nv_bfloat16*>(x_orig),
+                  return launch_combine(L->y, L->slot_row, static_cast<const __nv_bfloat16*>(x_orig),
                                         static_cast<__nv_bfloat16*>(out), T, residual, s);
                 }),
           "combine launch");
@@ -487,7 +489,9 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
             encode_packed(&L->tm_squ, weights->sh_up.q, HID / 8, SH_INTER) &&
             encode_packed(&L->tm_qd, weights->down.q, INTER / 8, static_cast<uint64_t>(NEXP) * HID) &&
             encode_packed(&L->tm_sqd, weights->sh_down.q, SH_INTER / 8, HID) &&
-            encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX);
+            encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX) &&
+            encode_2d(&L->tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->y, HID, 9ull * Tm, HID * 2, GX_BM, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return fail(MOE_ERR_CUDA);
   *out = L;
   return MOE_OK;

@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
       p.row_dst[pos] = slot0 + s;
       p.row_w[pos] = p.topk_w[slot0 + s];
     }
+    if (s < nslots) p.slot_row[slot0 + s] = pos;   // -1 for a slot that failed validation
   }
   }   // blockIdx.y == 0
   if (!p.gather) return;
