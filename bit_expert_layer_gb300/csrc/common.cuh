@@ -55,7 +55,11 @@ constexpr int GX_TAB_BYTES = 3 * (NEXP + 2) * 4 + 128;   // tile tables staged i
 // + alignment slack, barriers (512 B), tile tables
 constexpr int GU_GW = 6;                            // activation gather warps
 constexpr int GU_GROWS = (GX_BN + GU_GW - 1) / GU_GW + 4;   // token ids per gather warp and tile
-constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4;
+// per-CTA tile schedules (16 bytes a tile): tiles per CTA at the largest token count and
+// 152 SMs are 68 (gate/up) and 270 (down); the host checks the bound per launch
+constexpr int GU_SCHED_CAP = 96;
+constexpr int DN_SCHED_CAP = 288;
+constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16;
 constexpr int GU_THREADS = (14 + GU_GW) * 32;   // packed producer, MMA, 8 dequant, 4 epilogue, gather warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
@@ -64,10 +68,13 @@ constexpr int DN_NP = 8;
 constexpr int DN_NX = 3;
 constexpr int DN_NA = 3;
 constexpr int DN_RINGS = DN_NP * GX_P_BYTES + DN_NX * GX_X_BYTES + DN_NA * GX_A_BYTES;
-// + alignment slack, barriers and words (1 KB), two 32-row staging buffers (16 KB), tile tables
-constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + 2 * 32 * GX_BM * 2 + GX_TAB_BYTES;
+// epilogue staging: per epilogue warp DN_STG_BUFS buffers of 32 rows x 32 features (bf16)
+constexpr int DN_STG_BUFS = 4;
+constexpr int DN_STG_BYTES = 4 * DN_STG_BUFS * 32 * 32 * 2;
+// + alignment slack, barriers and words (1 KB), staging, tile tables
+constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + DN_STG_BYTES + GX_TAB_BYTES + 16 + DN_SCHED_CAP * 16;
 static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
-constexpr int DN_THREADS = 480;   // packed producer, MMA, 8 dequant, 4 epilogue, activation producer
+constexpr int DN_THREADS = 512;   // 16 warps: producers, MMA, 8 dequant, 4 epilogue, one spare
 constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
 
 // scatter: per router block of 128 tokens (1024 slots), SC_SPLIT CTAs; the first also
@@ -252,6 +259,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
         "=r"(r[15])
       : "r"(taddr));
+}
+// 16 lanes x 32 columns in the MMA fragment layout: thread t gets lanes base + t/4 and
+// base + 8 + t/4, columns 8g + 2(t%4) and 8g + 2(t%4) + 1 for g = 0..3, in the order
+// r[4g] = (t/4, 8g+2(t%4)), r[4g+1] = (t/4, +1), r[4g+2] = (8+t/4, 8g+2(t%4)), r[4g+3] = (8+t/4, +1).
+__device__ __forceinline__ void tmem_ld16x256(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// Four 8x8 bf16 matrices stored transposed: register i of thread t holds row t/4,
+// columns 2(t%4), 2(t%4)+1 of matrix i; thread 8i + k gives the shared address of stored
+// row k of matrix i, which receives column k of the source.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(m0), "r"(m1),
+               "r"(m2), "r"(m3)
+               : "memory");
+}
+// Two fp32 values (raw bits) rounded to a bf16 pair, `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));

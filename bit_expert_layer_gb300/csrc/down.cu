@@ -7,17 +7,23 @@
 //
 // A tile is 128 output features (M) x up to 256 permuted rows (N); K = 512 is only 8
 // steps of 64, so one tile's MMAs take ~2 us and the dequant and epilogue have to keep
-// pace with that.  Warp roles (15 warps):
+// pace with that.  Warp w runs on scheduler w % 4.  A single thread issues the MMAs and
+// each tcgen05.mma holds it for ~100 cycles of issue; sharing its scheduler with the
+// ALU-bound dequant warps slowed the MMA stream by ~40%, so no dequant warp runs on
+// scheduler 1.  Warp roles (16 warps):
 //   warp 0      TMA producer of the packed 4-bit tiles (ring of DN_NP, 4 KB stages)
 //   warp 1      TMEM allocator and MMA issuer (double-buffered 128 x 256 accumulator)
-//   warps 2-9   dequant: two threads per weight row, four packed words each (ring of
+//   warp 5      TMA producer of the activation rows h' (ring of DN_NX, 32 KB stages)
+//   warps 2-4, 6-8, 10, 11
+//               dequant: two threads per weight row, four packed words each (ring of
 //               DN_NA dequantised 16 KB tiles)
-//   warps 10-13 epilogue: per 32-row chunk, round to bf16 into a shared-memory tile
-//               of 32 rows x 128 features and write it with one TMA store (y is kept in
+//   warps 12-15 epilogue, one per TMEM lane quarter (32 features), each on its own:
+//               per 32-row chunk, round to bf16 pairs, transpose into a 32 x 32 staging
+//               tile with stmatrix and write it with one TMA store (y is kept in
 //               permuted-row order, so a chunk is one box; the combine reads each
-//               token's nine rows through the slot -> row map); two staging buffers
-//               alternate; a ragged last chunk is written with 16-byte stores
-//   warp 14     TMA producer of the activation rows h' (ring of DN_NX, 32 KB stages)
+//               token's nine rows through the slot -> row map); DN_STG_BUFS staging
+//               tiles per warp rotate; a ragged last chunk is written with 16-byte stores
+//   warp 9      none
 // The rings are separate so the small packed tiles, which come from HBM, run further
 // ahead than the activation tiles, which each expert's 16 row blocks re-read from L2
 // (evict-last) while the weights stream through it (evict-first).
@@ -34,25 +40,9 @@ constexpr int OFF_X = OFF_A + DN_NA * GX_A_BYTES;          // [DN_NX][32 KB]
 constexpr int OFF_P = OFF_X + DN_NX * GX_X_BYTES;          // [DN_NP][4 KB]
 constexpr int OFF_MISC = OFF_P + DN_NP * GX_P_BYTES;
 static_assert(OFF_X % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-constexpr int EPI_BAR = 1;                           // named barrier of the epilogue warps
-constexpr int STG_ROW = GX_BM * 2;                   // bytes of one staged row (128 bf16)
-
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(EPI_BAR), "n"(128) : "memory");
-}
-// the epilogue barrier with a vote: true in every epilogue thread if any passed true
-__device__ __forceinline__ bool epi_sync_or(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "barrier.red.or.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "n"(EPI_BAR), "n"(128)
-      : "memory");
-  return r != 0;
-}
+constexpr int STG_ROW = 32 * 2;                      // bytes of one staged row (32 bf16)
+constexpr int STG_BUF = 32 * STG_ROW;                // one 32 x 32 staging tile
+static_assert(4 * DN_STG_BUFS * STG_BUF == DN_STG_BYTES, "staging size");
 }  // namespace
 
 __global__ void __launch_bounds__(DN_THREADS, 1)
@@ -65,10 +55,12 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                       // 40 barriers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
-  uint8_t* stg = misc + 1024;                                                // [2][32][128] bf16 staging
-  int* s_tiles = reinterpret_cast<int*>(stg + 2 * 32 * STG_ROW);
+  uint8_t* stg = misc + 1024;                                     // [4 warps][DN_STG_BUFS][32][32] bf16
+  int* s_tiles = reinterpret_cast<int*>(stg + DN_STG_BYTES);
   int* s_off = s_tiles + (NEXP + 2);
   int* s_cnt = s_off + (NEXP + 2);
+  constexpr int SCHED_OFF = (1024 + DN_STG_BYTES + GX_TAB_BYTES + 15) / 16 * 16;
+  int4* sched = reinterpret_cast<int4*>(misc + SCHED_OFF);   // [DN_SCHED_CAP] this CTA's tiles
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -114,7 +106,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = s_tiles[NEXP + 1];
+  const int ntiles = build_schedule(sched, DN_SCHED_CAP, s_tiles, s_off, s_cnt, DN_MBLK, p.T, p.err);
+  __syncthreads();
   constexpr int NKB = INTER / 64;   // 8
 
   if (warp == 0) {
@@ -128,8 +121,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       const uint64_t pol = l2_policy_evict_first();   // each weight tile is read once
       uint32_t it = 0;
       bool alive = true;
-      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+      for (int tix = 0; tix < ntiles && alive; ++tix) {
+        const TileInfo ti = sched_tile(sched, tix);
         if (!ti.ok) { atomicOr(p.err, ERRBIT_BOUNDS); continue; }
         const bool sh = ti.e == SHARED_E;
         const CUtensorMap* mq = sh ? &tm_sqd : &tm_qd;
@@ -146,15 +139,15 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       }
       if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
     }
-  } else if (warp == 14) {
+  } else if (warp == 5) {
     if (lane == 0) {
       // ------------------------------------------------ activation-tile producer
       tma_prefetch_desc(&tm_h);
       const uint64_t pol = l2_policy_evict_last();    // each h' block is read by 16 row blocks
       uint32_t it = 0;
       bool alive = true;
-      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+      for (int tix = 0; tix < ntiles && alive; ++tix) {
+        const TileInfo ti = sched_tile(sched, tix);
         if (!ti.ok) continue;
         const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
@@ -177,8 +170,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       unsigned long long pc[3] = {0, 0, 0};
       const unsigned long long t_role = pp ? clock64() : 0;
       uint32_t it = 0, tc = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+      uint32_t rdy = 0;   // bit 0 / 1: AFULL / XFULL of step `it` seen complete by the last poll
+      for (int tix = 0; tix < ntiles; ++tix) {
+        const TileInfo ti = sched_tile(sched, tix);
         if (!ti.ok) continue;
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, N);
@@ -189,17 +183,17 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         bool alive = true;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int sa = it % DN_NA, sx = it % DN_NX;
-          if (!mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, pc[1], pp) ||
-              !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, pc[2], pp)) {
+          if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, pc[1], pp)) ||
+              (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, pc[2], pp))) {
             alive = false;
             break;
           }
           tc_fence_after();
           const uint32_t a = smem_u32(smem + OFF_A + sa * GX_A_BYTES);
           const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, sdesc_sw128(a + kk * 32), sdesc_sw128(x + kk * 32), idesc, (kb | kk) != 0);
+          const uint32_t nx = it + 1;   // the next step's stages are polled while these issue
+          rdy = umma_k64_poll(d, sdesc_sw128(a), sdesc_sw128(x), idesc, kb != 0, AFULL(nx % DN_NA),
+                              (nx / DN_NA) & 1, XFULL(nx % DN_NX), (nx / DN_NX) & 1);
           umma_commit(AEMPTY(sa));
           umma_commit(XEMPTY(sx));
         }
@@ -213,9 +207,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         atomicAdd(p.pipe + 10, static_cast<unsigned long long>(tc));
       }
     }
-  } else if (warp < 10) {
+  } else if (warp < 12 && warp != 9) {
     // ------------------------------------------------ dequant (8 warps, 2 threads per row)
-    const int dt = tid - 64;       // 0..255
+    const int dt = (warp - 2 - (warp - 2) / 4) * 32 + lane;   // warps 2-4, 6-8, 10, 11 -> 0..255
     const int r = dt & 127;        // row inside the tile
     const int hw = dt >> 7;        // which four of the row's eight packed words
     const bool pp = p.pipe != nullptr;
@@ -228,8 +222,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
     ti.ok = false;
     uint4 nsv = make_uint4(0, 0, 0, 0), nbv = nsv;
     auto load_next = [&](int t) {
-      if (t >= total) return;
-      ti = tile_info(s_tiles, s_off, s_cnt, t, DN_MBLK, p.T);
+      if (t >= ntiles) return;
+      ti = sched_tile(sched, t);
       if (!ti.ok) return;
       const bool sh = ti.e == SHARED_E;
       const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + r)
@@ -237,11 +231,11 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       nsv = ldg_nc_v4((sh ? p.sd_scales : p.d_scales) + srow * (INTER / GROUP));
       nbv = ldg_nc_v4((sh ? p.sd_biases : p.d_biases) + srow * (INTER / GROUP));
     };
-    load_next(blockIdx.x);
-    for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+    load_next(0);
+    for (int tix = 0; tix < ntiles && alive; ++tix) {
       const bool cur_ok = ti.ok;
       const uint4 sv = nsv, bv = nbv;
-      load_next(tile + gridDim.x);
+      load_next(tix + 1);
       if (!cur_ok) continue;
       const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
       const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
@@ -271,70 +265,80 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       }
     }
     if (pp && dt == 0) pipe_flush(p.pipe, 6, pc, 1, clock64() - t_role, 7);
-  } else {
-    // ------------------------------------------------ epilogue (4 warps)
+  } else if (warp >= 12) {
+    // ------------------------------------------------ epilogue (4 warps, independent)
     const int q = warp & 3;                       // TMEM lane quarter = features q*32..q*32+31
-    const int te = tid - 320;                     // 0..127
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t* wst = stg + q * (DN_STG_BUFS * STG_BUF);
     const bool pp = p.pipe != nullptr;
     unsigned long long pc[1] = {0};
     const unsigned long long t_role = pp ? clock64() : 0;
-    if (te == 0) tma_prefetch_desc(&tm_y);
-    uint32_t tc = 0, nst = 0;                     // tiles done; TMA stores issued
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, DN_MBLK, p.T);
+    if (lane == 0) tma_prefetch_desc(&tm_y);
+    uint32_t tc = 0, nst = 0;                     // tiles done; staging tiles used (warp-uniform)
+    for (int tix = 0; tix < ntiles; ++tix) {
+      const TileInfo ti = sched_tile(sched, tix);
       if (!ti.ok) continue;
       const int buf = tc & 1;
-      // the wait is bounded; all four warps then meet and leave together on an abort
       const bool got = mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, pc[0], pp);
-      if (epi_sync_or(!got || *abort_flag)) break;   // the same decision in all four warps
+      if (!__all_sync(0xffffffffu, got)) break;   // tcgen05.ld below needs the whole warp
       tc_fence_after();
-      const int f = q * 32 + lane;                // feature inside the tile
-      const int fcol = ti.mb * GX_BM;
-#pragma unroll 1
-      for (int cc = 0; cc < GX_BN / 32; ++cc) {
-        const int col0 = cc * 32;
-        if (col0 >= ti.n_rows) break;
-        uint32_t d[32];
-        tmem_ld32(tl + buf * 256 + col0, d);
-        tmem_ld_wait();
-        if (col0 + 32 >= ti.n_rows) {             // last chunk read: the MMA may reuse the buffer
-          tc_fence_before();
-          mbar_arrive(ACCE(buf));
-        }
-        uint8_t* sb = stg + (nst & 1) * 32 * STG_ROW;
-        // the TMA store issued from this buffer two chunks ago has read it
-        if (te == 0 && nst >= 2) tma_store_wait_read<1>();
-        epi_sync();
-        // round and transpose: staged row j holds the chunk's row col0 + j
+      const int fcol = ti.mb * GX_BM + q * 32;    // this warp's first output feature
+      const uint32_t tb = tl + buf * 256;
+      // One 32-row chunk, read as two 16-lane fragments (features 0-15 and 16-31 of this
+      // warp): round to bf16 pairs and stage it transposed with stmatrix, so staged row j
+      // (the tile's row c0 + j) holds the warp's 32 features in order; then one TMA store.
+      auto stage = [&](const uint32_t (&fa)[16], const uint32_t (&fb)[16], int c0) {
+        uint8_t* sb = wst + (nst % DN_STG_BUFS) * STG_BUF;
+        // the TMA store issued from this staging tile DN_STG_BUFS stores ago has read it
+        if (lane == 0 && nst >= DN_STG_BUFS) tma_store_wait_read<DN_STG_BUFS - 1>();
+        __syncwarp();
+        const uint32_t ra = smem_u32(sb) + (lane & 7) * STG_ROW + (lane >> 3) * 16;   // matrix lane/8, row lane%8
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          *reinterpret_cast<__nv_bfloat16*>(sb + j * STG_ROW + f * 2) = __float2bfloat16_rn(__uint_as_float(d[j]));
-        if (col0 + 32 <= ti.n_rows) {
+        for (int g = 0; g < 4; ++g)   // rows 8g..8g+7; matrices = features 0-7, 8-15, 16-23, 24-31
+          stmatrix_x4_trans(ra + g * 8 * STG_ROW, pack_bf16x2(fa[4 * g], fa[4 * g + 1]),
+                            pack_bf16x2(fa[4 * g + 2], fa[4 * g + 3]), pack_bf16x2(fb[4 * g], fb[4 * g + 1]),
+                            pack_bf16x2(fb[4 * g + 2], fb[4 * g + 3]));
+        const int rows = min(32, ti.n_rows - c0);
+        if (rows == 32) {
           fence_proxy_async_smem();               // the generic writes, before the TMA reads them
-          epi_sync();
-          if (te == 0) tma_store_2d(&tm_y, smem_u32(sb), fcol, ti.row0 + col0);
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tm_y, smem_u32(sb), fcol, ti.row0 + c0);
           ++nst;
         } else {
           // ragged last chunk: only its own rows (the next rows belong to other tiles)
-          epi_sync();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int item = te + 128 * i;
-            const int j = item >> 4, seg = item & 15;
-            if (col0 + j < ti.n_rows) {
-              const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + seg * 16);
-              *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.row0 + col0 + j) * HID + fcol + seg * 8) = v;
-            }
+          __syncwarp();
+          for (int item = lane; item < rows * 4; item += 32) {
+            const int j = item >> 2, seg = item & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + seg * 16);
+            *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.row0 + c0 + j) * HID + fcol + seg * 8) = v;
           }
-          epi_sync();                             // this buffer is free again
+          __syncwarp();                           // this staging tile is free again
         }
+      };
+#pragma unroll 1
+      for (int col0 = 0; col0 < ti.n_rows; col0 += 64) {
+        const bool two = col0 + 32 < ti.n_rows;   // warp-uniform
+        uint32_t a0[16], b0[16], a1[16], b1[16];
+        tmem_ld16x256(tb + col0, a0);
+        tmem_ld16x256(tb + (16u << 16) + col0, b0);
+        if (two) {
+          tmem_ld16x256(tb + col0 + 32, a1);
+          tmem_ld16x256(tb + (16u << 16) + col0 + 32, b1);
+        }
+        tmem_ld_wait();
+        if (col0 + 64 >= ti.n_rows) {             // last read of this buffer: the MMA may reuse it
+          tc_fence_before();
+          mbar_arrive(ACCE(buf));
+        }
+        stage(a0, b0, col0);
+        if (two) stage(a1, b1, col0 + 32);
       }
       ++tc;
     }
-    if (te == 0) tma_store_wait_all();
-    if (pp && te == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
+    if (lane == 0) tma_store_wait_all();
+    if (pp && q == 0 && lane == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
   }
+  // warp 9 has no role
 
   tc_fence_before();
   __syncthreads();

@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   int* s_off = s_tiles + (NEXP + 2);
   int* s_cnt = s_off + (NEXP + 2);
   int* s_tok = reinterpret_cast<int*>(misc + 512 + GX_TAB_BYTES);   // [GU_GW][GU_GROWS] token ids
+  int4* sched = reinterpret_cast<int4*>(s_tok + GU_GW * GU_GROWS);   // [GU_SCHED_CAP] this CTA's tiles
+  static_assert((512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4) % 16 == 0, "schedule alignment");
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -74,6 +76,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 #define AFULL(s) (bar0 + 8u * (2 * GU_NP + 2 * GU_NX + (s)))
 #define AEMPTY(s) (bar0 + 8u * (2 * GU_NP + 2 * GU_NX + GU_NA + (s)))
   constexpr int NB = 2 * GU_NP + 2 * GU_NX + 2 * GU_NA;
+  static_assert(8 * (NB + 3) <= 256, "barriers overlap the TMEM slot");
   const uint32_t ACCF = bar0 + 8u * NB, ACCE = bar0 + 8u * (NB + 1), DRAIN = bar0 + 8u * (NB + 2);
 
   if (tid == 0) {
@@ -103,7 +106,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total = s_tiles[NEXP + 1];
+  const int ntiles = build_schedule(sched, GU_SCHED_CAP, s_tiles, s_off, s_cnt, GU_MBLK, p.T, p.err);
+  __syncthreads();
   constexpr int NKB = HID / 64;
   const bool pp = p.pipe != nullptr;
 
@@ -124,8 +128,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         const uint64_t pol = l2_policy_evict_first();   // each weight tile is read by one CTA once
         uint32_t it = 0;
         bool alive = true;
-        for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-          const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+        for (int tix = 0; tix < ntiles && alive; ++tix) {
+          const TileInfo ti = sched_tile(sched, tix);
           if (!ti.ok) { atomicOr(p.err, ERRBIT_BOUNDS); continue; }
           const bool sh = ti.e == SHARED_E;
           const CUtensorMap* mg = sh ? &tm_sqg : &tm_qg;
@@ -154,8 +158,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         unsigned long long pc[3] = {0, 0, 0};
         const unsigned long long t_role = pp ? clock64() : 0;
         uint32_t it = 0, tc = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-          const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+        uint32_t rdy = 0;   // bit 0 / 1: AFULL / XFULL of step `it` seen complete by the last poll
+        for (int tix = 0; tix < ntiles; ++tix) {
+          const TileInfo ti = sched_tile(sched, tix);
           if (!ti.ok) continue;
           const int N = max(16, (ti.n_rows + 15) & ~15);
           const uint32_t idesc = idesc_bf16(128, N);
@@ -164,8 +169,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           bool alive = true;
           for (int kb = 0; kb < NKB; ++kb, ++it) {
             const int sa = it % GU_NA, sx = it % GU_NX;
-            if (!mbar_wait_t(AFULL(sa), (it / GU_NA) & 1, p.err, abort_flag, pc[1], pp) ||
-                !mbar_wait_t(XFULL(sx), (it / GU_NX) & 1, p.err, abort_flag, pc[2], pp)) {
+            if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / GU_NA) & 1, p.err, abort_flag, pc[1], pp)) ||
+                (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / GU_NX) & 1, p.err, abort_flag, pc[2], pp))) {
               alive = false;
               break;
             }
@@ -173,13 +178,11 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             tc_fence_after();
             const uint32_t a = smem_u32(smem + OFF_A + sa * GU_A_STAGE);
             const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
-  #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = sdesc_sw128(x + kk * 32);
-              const uint32_t acc = (kb | kk) != 0;
-              umma_bf16(tmem, sdesc_sw128(a + kk * 32), bd, idesc, acc);
-              umma_bf16(tmem + 256, sdesc_sw128(a + GX_A_BYTES + kk * 32), bd, idesc, acc);
-            }
+            // gate and up MMAs of this K step; the next step's stages are polled meanwhile
+            const uint32_t nx = it + 1;
+            rdy = umma_k64_x2_poll(tmem, tmem + 256, sdesc_sw128(a), sdesc_sw128(a + GX_A_BYTES), sdesc_sw128(x),
+                                   idesc, kb != 0, AFULL(nx % GU_NA), (nx / GU_NA) & 1, XFULL(nx % GU_NX),
+                                   (nx / GU_NX) & 1);
             umma_commit(AEMPTY(sa));
             umma_commit(XEMPTY(sx));
           }
@@ -203,8 +206,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       const uint64_t pol = l2_policy_evict_last();   // every token row is read by about nine tiles
       uint32_t it = 0;
       bool alive = true;
-      for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+      for (int tix = 0; tix < ntiles && alive; ++tix) {
+        const TileInfo ti = sched_tile(sched, tix);
         if (!ti.ok) continue;
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const int nr = (N - gw + GU_GW - 1) / GU_GW;   // this warp's rows
@@ -255,8 +258,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     const uint16_t *sc = nullptr, *bi = nullptr;
     uint4 nsv = make_uint4(0, 0, 0, 0), nbv = nsv;
     auto load_next = [&](int t) {
-      if (t >= total) return;
-      ti = tile_info(s_tiles, s_off, s_cnt, t, GU_MBLK, p.T);
+      if (t >= ntiles) return;
+      ti = sched_tile(sched, t);
       if (!ti.ok) return;
       const bool sh = ti.e == SHARED_E;
       const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + r)
@@ -266,13 +269,13 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       nsv = ldg_nc_v4(sc);
       nbv = ldg_nc_v4(bi);
     };
-    load_next(blockIdx.x);
-    for (int tile = blockIdx.x; tile < total && alive; tile += gridDim.x) {
+    load_next(0);
+    for (int tix = 0; tix < ntiles && alive; ++tix) {
       const TileInfo cur = ti;
       const uint16_t* csc = sc;
       const uint16_t* cbi = bi;
       if (!cur.ok) {
-        load_next(tile + gridDim.x);
+        load_next(tix + 1);
         continue;
       }
       for (int kc = 0; kc < NKB / 8 && alive; ++kc) {
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           nsv = ldg_nc_v4(csc + (kc + 1) * 8);
           nbv = ldg_nc_v4(cbi + (kc + 1) * 8);
         } else {
-          load_next(tile + gridDim.x);
+          load_next(tix + 1);
         }
         const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
@@ -326,8 +329,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     unsigned long long pc[1] = {0};
     const unsigned long long t_role = pp ? clock64() : 0;
     uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, tile, GU_MBLK, p.T);
+    for (int tix = 0; tix < ntiles; ++tix) {
+      const TileInfo ti = sched_tile(sched, tix);
       if (!ti.ok) continue;
       // each row's weight (routing weight, or the shared-expert gate) is applied here,
       // W_down (w h) = w (W_down h), so the down GEMM's epilogue has no per-row scaling;

@@ -33,6 +33,38 @@ __device__ __forceinline__ TileInfo tile_info(const int* tiles, const int* offse
   return ti;
 }
 
+// This CTA's share of a grouped GEMM's tiles (tile blockIdx.x + i gridDim.x, i = 0, 1,
+// ...), decoded from the staged tables once at kernel start, one thread per tile, so that
+// no role repeats the binary search per tile: its nine dependent shared-memory loads
+// queue behind the rings' traffic and cost the MMA issuer ~3500 cycles per tile.  A
+// record is {expert, row block, first row, rows}; rows = 0 marks a tile whose tables are
+// inconsistent, which every role skips.  More tiles than `cap` is a bounds error (the
+// host sizes the grid so that it cannot happen).  Returns the number of records.
+__device__ __forceinline__ int build_schedule(int4* sched, int cap, const int* s_tiles, const int* s_off,
+                                              const int* s_cnt, int mblk, int T, unsigned int* err) {
+  const int total = s_tiles[NEXP + 1];
+  const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
+  const int n = total > b ? (total - b + g - 1) / g : 0;
+  if (n > cap && threadIdx.x == 0) atomicOr(err, ERRBIT_BOUNDS);
+  const int m = min(n, cap);
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, b + i * g, mblk, T);
+    sched[i] = ti.ok ? make_int4(ti.e, ti.mb, ti.row0, ti.n_rows) : make_int4(0, 0, 0, 0);
+  }
+  return m;
+}
+
+__device__ __forceinline__ TileInfo sched_tile(const int4* sched, int i) {
+  const int4 r = sched[i];
+  TileInfo ti;
+  ti.e = r.x;
+  ti.mb = r.y;
+  ti.row0 = r.z;
+  ti.n_rows = r.w;
+  ti.ok = r.w > 0;
+  return ti;
+}
+
 // Copy the tile prefix [258], row offsets [258] and row counts [257] into shared memory.
 __device__ __forceinline__ void stage_tables(int* s, const int* tiles, const int* offsets, const int* counts) {
   for (int i = threadIdx.x; i < NEXP + 2; i += blockDim.x) {
@@ -48,6 +80,72 @@ __device__ __forceinline__ __nv_bfloat162 bf2(uint32_t bits16) {
 }
 
 __device__ __forceinline__ void st_shared_v4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// MMA issue with the next step's barrier polls folded in.  On sm_103a an mbarrier poll
+// holds the issuing thread for about 200 cycles even when the phase completed long ago,
+// and one K step waits on two barriers: polling them ahead of the MMAs of the current
+// step, and reading the result only after those are issued, hides that latency.  The
+// poll is a non-blocking test_wait (acquire, CTA scope); a stage it finds not yet full is
+// waited for in the ordinary bounded way.  Descriptors advance 32 bytes (16 bf16) of K per
+// MMA: +2 in the 16-byte address field.  Returns bit 0 / bit 1 = first / second barrier
+// already complete.
+//
+// One K step of 64 into two accumulators (gate, up) that share the B operand.
+__device__ __forceinline__ uint32_t umma_k64_x2_poll(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t b,
+                                                     uint32_t idesc, uint32_t accumulate, uint32_t nbar0,
+                                                     uint32_t npar0, uint32_t nbar1, uint32_t npar1) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pa, pt, q0, q1;\n\t.reg .b64 x0, x1, xb;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%8], %9;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%10], %11;\n\t"
+      "setp.ne.b32 pa, %7, 0;\n\t"
+      "setp.ne.b32 pt, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %5, %6, pa;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], %4, %5, %6, pa;\n\t"
+      "add.s64 x0, %3, 2;\n\tadd.s64 x1, %4, 2;\n\tadd.s64 xb, %5, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %6, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], x1, xb, %6, pt;\n\t"
+      "add.s64 x0, %3, 4;\n\tadd.s64 x1, %4, 4;\n\tadd.s64 xb, %5, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %6, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], x1, xb, %6, pt;\n\t"
+      "add.s64 x0, %3, 6;\n\tadd.s64 x1, %4, 6;\n\tadd.s64 xb, %5, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %6, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], x1, xb, %6, pt;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t"
+      "@q1 or.b32 %0, %0, 2;\n\t}"
+      : "=r"(r)
+      : "r"(d0), "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(idesc), "r"(accumulate), "r"(nbar0), "r"(npar0),
+        "r"(nbar1), "r"(npar1)
+      : "memory");
+  return r;
+}
+
+// One K step of 64 into one accumulator.
+__device__ __forceinline__ uint32_t umma_k64_poll(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                  uint32_t accumulate, uint32_t nbar0, uint32_t npar0,
+                                                  uint32_t nbar1, uint32_t npar1) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pa, pt, q0, q1;\n\t.reg .b64 x0, xb;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%6], %7;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%8], %9;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\t"
+      "setp.ne.b32 pt, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pa;\n\t"
+      "add.s64 x0, %2, 2;\n\tadd.s64 xb, %3, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %4, pt;\n\t"
+      "add.s64 x0, %2, 4;\n\tadd.s64 xb, %3, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %4, pt;\n\t"
+      "add.s64 x0, %2, 6;\n\tadd.s64 xb, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %4, pt;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t"
+      "@q1 or.b32 %0, %0, 2;\n\t}"
+      : "=r"(r)
+      : "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(nbar0), "r"(npar0), "r"(nbar1), "r"(npar1)
+      : "memory");
+  return r;
+}
 
 // Pipeline tracing (MOE_PIPE_PROF=1 on the host): a role adds the clock cycles it spends
 // in each barrier wait, and its whole running time, to per-kernel counters.

@@ -148,6 +148,26 @@ cudaError_t timed(int id, cudaStream_t s, const unsigned int* err_word, F&& laun
 
 constexpr int MAX_TOKENS = 65536;
 
+// Upper bound of a grouped GEMM's tile count at T tokens: every touched expert adds at
+// most one partial token block to the full ones.
+long long gemm_tiles_bound(int T, int mblk) {
+  const long long blocks = (8ll * T + GX_BN - 1) / GX_BN + (8ll * T < NEXP ? 8ll * T : NEXP) + (T + GX_BN - 1) / GX_BN;
+  return blocks * mblk;
+}
+// Persistent grid: one CTA per SM, fewer when there are fewer tiles.
+int gemm_grid(int T, int mblk, int num_sms) {
+  const long long t = gemm_tiles_bound(T, mblk);
+  return static_cast<int>(t < num_sms ? t : num_sms);
+}
+// Each CTA decodes its tiles into a fixed-size schedule; T <= Tm must fit it.
+bool schedules_fit(int Tm, int num_sms) {
+  auto per_cta = [&](int mblk) {
+    const long long t = gemm_tiles_bound(Tm, mblk), g = gemm_grid(Tm, mblk, num_sms);
+    return (t + g - 1) / g;
+  };
+  return per_cta(GU_MBLK) <= GU_SCHED_CAP && per_cta(DN_MBLK) <= DN_SCHED_CAP;
+}
+
 struct Carver {
   uint8_t* base;
   size_t off = 0;
@@ -393,11 +413,7 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
                   L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->row_w, L->x_ilv, L->row_dst};
-  // upper bound of the tile count: every touched expert adds at most one partial token block
-  const long long tok_blocks = (8ll * T + GX_BN - 1) / GX_BN + (8ll * T < NEXP ? 8ll * T : NEXP) +
-                               (T + GX_BN - 1) / GX_BN;
-  const int grid_gu = static_cast<int>(tok_blocks * GU_MBLK < L->num_sms ? tok_blocks * GU_MBLK : L->num_sms);
-  const int grid_dn = static_cast<int>(tok_blocks * DN_MBLK < L->num_sms ? tok_blocks * DN_MBLK : L->num_sms);
+  const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
   MOE_TRY(timed(K_GATEUP, s, L->err,
                 [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, gp, grid_gu, s); }),
           "gate/up launch");
@@ -463,6 +479,11 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return fail(cuda_fail("device query", e));
+  if (!schedules_fit(cfg->max_tokens, L->num_sms)) {
+    snprintf(g_detail, sizeof g_detail, "max_tokens %d needs more tiles per CTA than the schedules hold on %d SMs",
+             cfg->max_tokens, L->num_sms);
+    return fail(MOE_ERR_UNSUPPORTED);
+  }
   if (!get_encode()) {
     snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled entry point unavailable");
     return fail(MOE_ERR_CUDA);
@@ -490,7 +511,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
             encode_packed(&L->tm_qd, weights->down.q, INTER / 8, static_cast<uint64_t>(NEXP) * HID) &&
             encode_packed(&L->tm_sqd, weights->sh_down.q, SH_INTER / 8, HID) &&
             encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX) &&
-            encode_2d(&L->tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->y, HID, 9ull * Tm, HID * 2, GX_BM, 32,
+            encode_2d(&L->tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->y, HID, 9ull * Tm, HID * 2, 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return fail(MOE_ERR_CUDA);
   *out = L;
