@@ -45,7 +45,7 @@ constexpr int GX_P_BYTES = GX_BM * 32;              //  4 KB packed 4-bit tile (
 // gate/up: three rings of different depth -- packed 4-bit tiles (gate + up, 8 KB, fetched
 // from HBM, deepest), activation tiles (32 KB, mostly from L2), dequantised tiles (gate +
 // up, 32 KB, only between dequant and MMA)
-constexpr int GU_NP = 6;
+constexpr int GU_NP = 5;
 constexpr int GU_NX = 3;
 constexpr int GU_NA = 2;
 constexpr int GU_P_STAGE = 2 * GX_P_BYTES;
@@ -59,7 +59,10 @@ constexpr int GU_GROWS = (GX_BN + GU_GW - 1) / GU_GW + 4;   // token ids per gat
 // 152 SMs are 68 (gate/up) and 270 (down); the host checks the bound per launch
 constexpr int GU_SCHED_CAP = 96;
 constexpr int DN_SCHED_CAP = 288;
-constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16;
+// gate/up epilogue staging: per epilogue warp GU_STG_BUFS tiles of 32 rows x 32 features
+constexpr int GU_STG_BUFS = 2;
+constexpr int GU_STG_BYTES = 4 * GU_STG_BUFS * 32 * 32 * 2;
+constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + GU_STG_BYTES;
 constexpr int GU_THREADS = (14 + GU_GW) * 32;   // packed producer, MMA, 8 dequant, 4 epilogue, gather warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
@@ -352,6 +355,12 @@ __host__ __device__ __forceinline__ int ilv_pos(int f) {
   const int i = f & 7;
   return (f & ~7) | (i < 4 ? 2 * i : 2 * (i - 4) + 1);
 }
+
+// Weight row held by row r of a dequantised gate/up tile: rows are permuted inside each
+// group of 8 so that the accumulator's lanes come out in the order of ilv_pos (lane r
+// holds the feature whose interleaved column is r): lanes 0..7 of a group hold features
+// 0, 4, 1, 5, 2, 6, 3, 7.
+__host__ __device__ __forceinline__ int ilv_row(int r) { return (r & ~7) | ((r & 1) << 2) | ((r & 7) >> 1); }
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

@@ -1,9 +1,8 @@
-// down.cu -- the grouped down GEMM of the prefill path: y[row] = W_down h'[row] for every
-// permuted row (8 routed slots and 1 shared row per token), where h' already carries the
-// row's weight (applied by the gate/up epilogue), with the 4-bit weights dequantised
-// inside the kernel (Lily restores the 4-bit weights inside its
-// grouped GEMM: aimanavo.com, "Why is Perplexity's local AI Lily faster than MLX",
-// section "Prefill and decode are not treated as the same job").
+// down.cu -- the grouped down GEMM of the prefill path: y[row] = W_down h[row] for every
+// permuted row (8 routed slots and 1 shared row per token; the rows' weights are applied
+// by the combine), with the 4-bit weights dequantised inside the kernel (Lily restores
+// the 4-bit weights inside its grouped GEMM: aimanavo.com, "Why is Perplexity's local AI
+// Lily faster than MLX", section "Prefill and decode are not treated as the same job").
 //
 // A tile is 128 output features (M) x up to 256 permuted rows (N); K = 512 is only 8
 // steps of 64, so one tile's MMAs take ~2 us and the dequant and epilogue have to keep
@@ -13,7 +12,7 @@
 // scheduler 1.  Warp roles (16 warps):
 //   warp 0      TMA producer of the packed 4-bit tiles (ring of DN_NP, 4 KB stages)
 //   warp 1      TMEM allocator and MMA issuer (double-buffered 128 x 256 accumulator)
-//   warp 5      TMA producer of the activation rows h' (ring of DN_NX, 32 KB stages)
+//   warp 5      TMA producer of the activation rows h (ring of DN_NX, 32 KB stages)
 //   warps 2-4, 6-8, 10, 11
 //               dequant: two threads per weight row, four packed words each (ring of
 //               DN_NA dequantised 16 KB tiles)
@@ -143,7 +142,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------ activation-tile producer
       tma_prefetch_desc(&tm_h);
-      const uint64_t pol = l2_policy_evict_last();    // each h' block is read by 16 row blocks
+      const uint64_t pol = l2_policy_evict_last();    // each h block is read by 16 row blocks
       uint32_t it = 0;
       bool alive = true;
       for (int tix = 0; tix < ntiles && alive; ++tix) {

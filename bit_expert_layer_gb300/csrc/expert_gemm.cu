@@ -11,12 +11,13 @@
 // to 256 per tile, rounded up to 16), K steps of 64 = one quantisation group, so each
 // dequantised row needs exactly one scale and one bias per K step.
 //
-//   gateup_kernel  h' = w * silu(W_gate x) * (W_up x) for every (expert, token) pair of
-//                  the permuted activations, w = the row's routing weight (the shared
-//                  expert, expert 256 over all T tokens, uses sigmoid(g_s . x)).  Two
-//                  TMEM accumulators (gate, up), SwiGLU in the epilogue.
-//   combine_kernel out[t] = sum_k y[row(t,k)] + y[8T+t] (+ x[t]) in a fixed order,
-//                  row(t,k) = the permuted row of slot t*8+k.
+//   gateup_kernel  h = silu(W_gate x) * (W_up x) for every (expert, token) pair of the
+//                  permuted activations (the shared expert is expert 256 over all T
+//                  tokens).  Two TMEM accumulators (gate, up), SwiGLU in the epilogue.
+//   combine_kernel out[t] = sum_k w_k y[row(t,k)] + g_s y[8T+t] (+ x[t]) in a fixed
+//                  order, row(t,k) = the permuted row of slot t*8+k, w_k its routing
+//                  weight, g_s = sigmoid(g_s . x) the shared-expert gate; the weights are
+//                  applied here, where they cost nothing in a memory-bound pass.
 //
 // Warp roles of gateup_kernel (20 warps, one role per warpgroup but the first):
 //   warp 0      TMA producer of the packed 4-bit tiles (ring of GU_NP)
@@ -28,7 +29,10 @@
 //               activation rows are kept in L2 (evict-last), the weights streamed
 //               through it (evict-first)
 //   warps 8-15  dequant: packed tile -> 128-byte-swizzled bf16 tiles (ring of GU_NA)
-//   warps 16-19 epilogue: SwiGLU and row weight, bf16 h' rows
+//   warps 16-19 epilogue, one per TMEM lane quarter: SwiGLU; per 32-row
+//               chunk, bf16 pairs transposed into a 32 x 32 staging tile with stmatrix
+//               and written with one TMA store (the dequant permutes the weight rows
+//               so that lane order is h column order)
 // The rings are separate so the HBM-bound packed tiles can be fetched further ahead than
 // the large activation tiles fit.
 //
@@ -47,12 +51,16 @@ constexpr int OFF_X = OFF_A + GU_NA * GU_A_STAGE;            // [GU_NX][32 KB]
 constexpr int OFF_P = OFF_X + GU_NX * GX_X_BYTES;            // [GU_NP][gate 4 KB | up 4 KB]
 constexpr int OFF_MISC = OFF_P + GU_NP * GU_P_STAGE;
 static_assert(OFF_X % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr int STG_ROW = 32 * 2;                      // bytes of one staged row (32 bf16)
+constexpr int STG_BUF = 32 * STG_ROW;                // one 32 x 32 staging tile
+static_assert(4 * GU_STG_BUFS * STG_BUF == GU_STG_BYTES, "staging size");
+static_assert((512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4) % 16 == 0, "schedule and staging alignment");
 }  // namespace
 
 __global__ void __launch_bounds__(GU_THREADS, 1)
     gateup_kernel(const __grid_constant__ CUtensorMap tm_qg, const __grid_constant__ CUtensorMap tm_qu,
                   const __grid_constant__ CUtensorMap tm_sqg, const __grid_constant__ CUtensorMap tm_squ,
-                  GateUpParams p) {
+                  const __grid_constant__ CUtensorMap tm_hs, GateUpParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* misc = smem + OFF_MISC;
@@ -64,7 +72,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   int* s_cnt = s_off + (NEXP + 2);
   int* s_tok = reinterpret_cast<int*>(misc + 512 + GX_TAB_BYTES);   // [GU_GW][GU_GROWS] token ids
   int4* sched = reinterpret_cast<int4*>(s_tok + GU_GW * GU_GROWS);   // [GU_SCHED_CAP] this CTA's tiles
-  static_assert((512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4) % 16 == 0, "schedule alignment");
+  uint8_t* stg = reinterpret_cast<uint8_t*>(sched + GU_SCHED_CAP);     // [4 warps][GU_STG_BUFS][32][32] bf16
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     const int dt = tid - (2 + GU_GW) * 32;   // 0..255
     const int mat = dt >> 7;           // 0: gate rows, 1: up rows
     const int r = dt & 127;            // row inside the tile
+    const int wr = ilv_row(r);         // the weight row it holds
     unsigned long long pc[1] = {0};
     const unsigned long long t_role = pp ? clock64() : 0;
     uint32_t it = 0;
@@ -262,8 +271,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       ti = sched_tile(sched, t);
       if (!ti.ok) return;
       const bool sh = ti.e == SHARED_E;
-      const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + r)
-                             : static_cast<size_t>(ti.e) * INTER + ti.mb * GX_BM + r;
+      const size_t srow = sh ? static_cast<size_t>(ti.mb * GX_BM + wr)
+                             : static_cast<size_t>(ti.e) * INTER + ti.mb * GX_BM + wr;
       sc = (mat == 0 ? (sh ? p.sg_scales : p.g_scales) : (sh ? p.su_scales : p.u_scales)) + srow * (HID / GROUP);
       bi = (mat == 0 ? (sh ? p.sg_biases : p.g_biases) : (sh ? p.su_biases : p.u_biases)) + srow * (HID / GROUP);
       nsv = ldg_nc_v4(sc);
@@ -299,7 +308,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           ++it;
           const __nv_bfloat162 ms = bf2((j & 1) ? (sw[j >> 1] >> 16) : sw[j >> 1]);
           const __nv_bfloat162 mbv = bf2((j & 1) ? (bw[j >> 1] >> 16) : bw[j >> 1]);
-          const uint4* P = reinterpret_cast<const uint4*>(smem + OFF_P + sp * GU_P_STAGE + mat * GX_P_BYTES + r * 32);
+          const uint4* P = reinterpret_cast<const uint4*>(smem + OFF_P + sp * GU_P_STAGE + mat * GX_P_BYTES + wr * 32);
           const uint4 w0 = P[0], w1 = P[1];
           // the packed words are in registers; the next TMA write into this stage is an
           // async-proxy access, so the generic reads are fenced before the release
@@ -326,56 +335,83 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     // While these warps drain TMEM, the dequant warps already fill the next tile's stages.
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t* wst = stg + q * (GU_STG_BUFS * STG_BUF);
     unsigned long long pc[1] = {0};
     const unsigned long long t_role = pp ? clock64() : 0;
-    uint32_t tc = 0;
+    if (lane == 0) tma_prefetch_desc(&tm_hs);
+    uint32_t tc = 0, nst = 0;   // tiles done; staging tiles used (warp-uniform)
     for (int tix = 0; tix < ntiles; ++tix) {
       const TileInfo ti = sched_tile(sched, tix);
       if (!ti.ok) continue;
-      // each row's weight (routing weight, or the shared-expert gate) is applied here,
-      // W_down (w h) = w (W_down h), so the down GEMM's epilogue has no per-row scaling;
-      // the weights are fetched before waiting for the accumulator
-      float wv[GX_BN / 32];
-#pragma unroll
-      for (int c = 0; c < GX_BN / 32; ++c) {
-        const int j = c * 32 + lane;
-        wv[c] = (j < ti.n_rows) ? __ldg(p.row_w + ti.row0 + j) : 0.0f;
-      }
       bool ok = mbar_wait_t(ACCF, tc & 1, p.err, abort_flag, pc[0], pp);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int f = ti.mb * GX_BM + q * 32 + lane;   // intermediate feature of this lane
-      const int hcol = ilv_pos(f);
-#pragma unroll
+      const int hcol = ti.mb * GX_BM + q * 32;   // h column of this warp's first lane
+      // One 32-row chunk: gate and up read as 16-lane fragments (lanes 0-15, then 16-31
+      // of this warp), SwiGLU, rounded to bf16 pairs (rows j, j+1) and
+      // staged transposed with stmatrix: staged row j = the tile's row col0 + j, its 32
+      // bf16 in lane order = h column order (the dequant permuted the weight rows).
+      // Thread t holds rows 8g + 2(t%4) + {0,1}, g = 0..3, of lanes t/4 and 8 + t/4.
+#pragma unroll 1
       for (int cc = 0; cc < GX_BN / 32; ++cc) {
         const int col0 = cc * 32;
         if (col0 >= ti.n_rows) break;
-        uint32_t g[32], u[32];
-        tmem_ld32(tl + col0, g);
-        tmem_ld32(tl + 256 + col0, u);
-        tmem_ld_wait();
-        if (col0 + 32 >= ti.n_rows) {   // last chunk read: the MMA may overwrite the accumulator
-          tc_fence_before();
-          mbar_arrive(ACCE);
-        }
-        __nv_bfloat16* hp = p.h + static_cast<size_t>(ti.row0 + col0) * INTER + hcol;
+        uint32_t m[2][4][2];   // [lane half][g][lane t/4 or 8 + t/4]
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, wv[cc], j);
-          if (col0 + j < ti.n_rows) {
-            const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-            // silu(g) = g * sigmoid(g), sigmoid(g) = (1 + tanh(g/2)) / 2 with the hardware
-            // tanh (max relative error 2^-10.99, below the bf16 rounding of h)
-            float th;
-            asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * gv));
-            const float hv = gv * fmaf(0.5f, th, 0.5f) * uv * wj;
-            hp[static_cast<size_t>(j) * INTER] = __float2bfloat16_rn(hv);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t g[16], u[16];
+          tmem_ld16x256(tl + (static_cast<uint32_t>(16 * hh) << 16) + col0, g);
+          tmem_ld16x256(tl + (static_cast<uint32_t>(16 * hh) << 16) + 256 + col0, u);
+          tmem_ld_wait();
+          if (hh == 1 && col0 + 32 >= ti.n_rows) {   // last read: the MMA may overwrite the accumulator
+            tc_fence_before();
+            mbar_arrive(ACCE);
           }
+          float hv[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            // silu(g) = g sigmoid(g) = g/2 + (g/2) tanh(g/2), with the hardware tanh (max
+            // relative error 2^-10.99, below the bf16 rounding of h)
+            const float hg = 0.5f * __uint_as_float(g[k]);
+            float th;
+            asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hg));
+            hv[k] = fmaf(hg, th, hg) * __uint_as_float(u[k]);
+          }
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            m[hh][gg][0] = pack_bf16x2(__float_as_uint(hv[4 * gg]), __float_as_uint(hv[4 * gg + 1]));
+            m[hh][gg][1] = pack_bf16x2(__float_as_uint(hv[4 * gg + 2]), __float_as_uint(hv[4 * gg + 3]));
+          }
+        }
+        uint8_t* sb = wst + (nst % GU_STG_BUFS) * STG_BUF;
+        // the TMA store issued from this staging tile GU_STG_BUFS stores ago has read it
+        if (lane == 0 && nst >= GU_STG_BUFS) tma_store_wait_read<GU_STG_BUFS - 1>();
+        __syncwarp();
+        const uint32_t ra = smem_u32(sb) + (lane & 7) * STG_ROW + (lane >> 3) * 16;   // matrix lane/8, row lane%8
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg)   // rows 8g..8g+7; matrices = lanes 0-7, 8-15, 16-23, 24-31
+          stmatrix_x4_trans(ra + gg * 8 * STG_ROW, m[0][gg][0], m[0][gg][1], m[1][gg][0], m[1][gg][1]);
+        const int rows = min(32, ti.n_rows - col0);
+        if (rows == 32) {
+          fence_proxy_async_smem();   // the generic writes, before the TMA reads them
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tm_hs, smem_u32(sb), hcol, ti.row0 + col0);
+          ++nst;
+        } else {
+          // ragged last chunk: only its own rows (the next rows belong to other tiles)
+          __syncwarp();
+          for (int item = lane; item < rows * 4; item += 32) {
+            const int j = item >> 2, seg = item & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + seg * 16);
+            *reinterpret_cast<uint4*>(p.h + static_cast<size_t>(ti.row0 + col0 + j) * INTER + hcol + seg * 8) = v;
+          }
+          __syncwarp();   // this staging tile is free again
         }
       }
       ++tc;
     }
+    if (lane == 0) tma_store_wait_all();
     if (pp && warp == 2 + GU_GW + 8 && lane == 0) pipe_flush(p.pipe, 8, pc, 1, clock64() - t_role, 9);
   }
 
@@ -401,6 +437,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 // slots in rank order, then the shared expert, then the residual.
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ y,
                                                       const int* __restrict__ slot_row,
+                                                      const float* __restrict__ row_w,
                                                       const __nv_bfloat16* x, __nv_bfloat16* out, int T,
                                                       int residual) {
   const int t = blockIdx.x, c = threadIdx.x;
@@ -415,11 +452,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 #pragma unroll
   for (int k = 0; k <= TOPK; ++k) {
     if (rows[k] < 0 || rows[k] >= 9 * T) continue;   // a slot the scatter rejected (error recorded)
+    const float w = __ldg(row_w + rows[k]);   // routing weight, or the shared-expert gate
     const uint4 v = ldg_nc_v4(y + static_cast<size_t>(rows[k]) * HID + c * 8);
-    acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x);
-    acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
-    acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z);
-    acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+    acc[0] = fmaf(w, bf16lo(v.x), acc[0]); acc[1] = fmaf(w, bf16hi(v.x), acc[1]);
+    acc[2] = fmaf(w, bf16lo(v.y), acc[2]); acc[3] = fmaf(w, bf16hi(v.y), acc[3]);
+    acc[4] = fmaf(w, bf16lo(v.z), acc[4]); acc[5] = fmaf(w, bf16hi(v.z), acc[5]);
+    acc[6] = fmaf(w, bf16lo(v.w), acc[6]); acc[7] = fmaf(w, bf16hi(v.w), acc[7]);
   }
   const size_t o = static_cast<size_t>(t) * HID + c * 8;
   if (residual) {
@@ -440,14 +478,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 }
 
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
-                          const CUtensorMap& squ, const GateUpParams& p, int grid, cudaStream_t s) {
-  gateup_kernel<<<grid, GU_THREADS, GU_SMEM, s>>>(qg, qu, sqg, squ, p);
+                          const CUtensorMap& squ, const CUtensorMap& hs, const GateUpParams& p, int grid,
+                          cudaStream_t s) {
+  gateup_kernel<<<grid, GU_THREADS, GU_SMEM, s>>>(qg, qu, sqg, squ, hs, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const __nv_bfloat16* x, __nv_bfloat16* out,
-                           int T, int residual, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, x, out, T, residual);
+cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
+                           __nv_bfloat16* out, int T, int residual, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, row_w, x, out, T, residual);
   return cudaGetLastError();
 }
 

@@ -53,11 +53,10 @@ struct GateUpParams {
   const uint16_t* u_scales; const uint16_t* u_biases;
   const uint16_t* sg_scales; const uint16_t* sg_biases;  // [512][32]
   const uint16_t* su_scales; const uint16_t* su_biases;
-  __nv_bfloat16* h;      // [9T][512], K-interleaved columns, each row scaled by its row_w
+  __nv_bfloat16* h;      // [9T][512] silu(gate) * up, K-interleaved columns
   int T;
   unsigned int* err;
   unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
-  const float* row_w;         // [9T] weight of each permuted row
   const __nv_bfloat16* x_ilv; // [T][2048] K-interleaved activations, gathered by token
   const int* row_dst;         // [9T] slot id (t*8+k) of each routed permuted row
 };
@@ -148,10 +147,12 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s);
 cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s);
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
-                          const CUtensorMap& squ, const GateUpParams& p, int grid, cudaStream_t s);
+                          const CUtensorMap& squ, const CUtensorMap& hs, const GateUpParams& p, int grid,
+                          cudaStream_t s);
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s);
-cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const __nv_bfloat16* x, __nv_bfloat16* out,
+cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
+                           __nv_bfloat16* out,
                            int T, int residual, cudaStream_t s);
 cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s);

@@ -53,7 +53,7 @@ struct moe_layer {
   unsigned long long* dec_xt;
   unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
-  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h, tm_y;
+  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h, tm_y, tm_hs;
 };
 
 namespace {
@@ -412,10 +412,10 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->row_w, L->x_ilv, L->row_dst};
+                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst};
   const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
   MOE_TRY(timed(K_GATEUP, s, L->err,
-                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, gp, grid_gu, s); }),
+                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
           "gate/up launch");
   DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
@@ -423,7 +423,7 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
-                  return launch_combine(L->y, L->slot_row, static_cast<const __nv_bfloat16*>(x_orig),
+                  return launch_combine(L->y, L->slot_row, L->row_w, static_cast<const __nv_bfloat16*>(x_orig),
                                         static_cast<__nv_bfloat16*>(out), T, residual, s);
                 }),
           "combine launch");
@@ -511,6 +511,8 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
             encode_packed(&L->tm_qd, weights->down.q, INTER / 8, static_cast<uint64_t>(NEXP) * HID) &&
             encode_packed(&L->tm_sqd, weights->sh_down.q, SH_INTER / 8, HID) &&
             encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX) &&
+            encode_2d(&L->tm_hs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->h, INTER, 9ull * Tm, INTER * 2, 32, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
             encode_2d(&L->tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->y, HID, 9ull * Tm, HID * 2, 32, 32,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return fail(MOE_ERR_CUDA);
