@@ -95,7 +95,7 @@ def make_hosts(wl):
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("expert_gemm.cu", "common.cuh"):
+    for f in ("expert_gemm.cu", "common.cuh", "gemm_common.cuh"):
         h.update(open(os.path.join(ROOT, "bit_expert_layer_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
