@@ -52,6 +52,9 @@ WORKLOADS = {
     "layer-T4096-skew": dict(layers=1, T_prefill=4096, T_decode=0, skew=True),
     "layer-T4096": dict(layers=1, T_prefill=4096, T_decode=0, skew=False),
     "layer-T16384": dict(layers=1, T_prefill=16384, T_decode=0, skew=False),
+    "layer-T8192": dict(layers=1, T_prefill=8192, T_decode=0, skew=False),
+    "layer-T2048": dict(layers=1, T_prefill=2048, T_decode=0, skew=False),
+    "layer-T1024": dict(layers=1, T_prefill=1024, T_decode=0, skew=False),
     "layer-decode-T1": dict(layers=1, T_prefill=0, T_decode=1, skew=False),
     "layer-decode-T8": dict(layers=1, T_prefill=0, T_decode=8, skew=False),
     "layer-T512": dict(layers=1, T_prefill=512, T_decode=0, skew=False),

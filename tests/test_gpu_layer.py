@@ -4,7 +4,9 @@ Workloads are the seeded synthetic layer at its real shapes: T=32 (the reference
 configuration), T=1 and 8 (decode), T=512 uniform, T=4096 with the skewed log-Zipf
 router bias, a sweep of ragged T, all tokens forced onto one expert set, in-place
 residual, determinism, a short stack, and argument errors.  The rules are in
-tests/parity.py.
+tests/parity.py.  Every prefill case runs on both implementations of the grouped
+expert GEMMs: the weight-streaming kernels ("small") and the tcgen05 tile kernels
+("tiles", the default).
 """
 from __future__ import annotations
 
@@ -34,10 +36,15 @@ def host0():
     return synth.make_layer(0)
 
 
-@pytest.fixture(scope="module")
-def dev0(lib, host0):
+PATHS = {"small": 4096, "tiles": 0}   # largest T on the weight-streaming kernels
+
+
+@pytest.fixture(scope="module", params=sorted(PATHS))
+def dev0(lib, host0, request):
     w = lib.DeviceWeights(host0)
-    return lib.MoELayer(w, max_tokens=4096)
+    layer = lib.MoELayer(w, max_tokens=4096)
+    layer.set_small_tokens(PATHS[request.param])
+    return layer
 
 
 def to_dev(x_np):
@@ -92,9 +99,11 @@ def test_prefill_T512(oracle, host0, dev0):
     print(f"T=512 {rep} max_err={err:.3e} scale={scale:.3e}")
 
 
-def test_skewed_T4096(oracle, lib):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_skewed_T4096(oracle, lib, path):
     L = synth.make_layer(0, skew=True)
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=4096)
+    layer.set_small_tokens(PATHS[path])
     x = synth.make_x(0, 4096)
     out, r = run(layer, x)
     rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
@@ -116,13 +125,15 @@ def test_skewed_T4096(oracle, lib):
           f"max_err={err:.3e} scale={scale:.3e}")
 
 
-def test_all_tokens_on_one_expert_set(oracle, lib):
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_all_tokens_on_one_expert_set(oracle, lib, path):
     L = synth.make_layer(7)
     chosen = [3, 17, 40, 77, 100, 150, 200, 255]
     bias = np.zeros(256, np.float32)
     bias[chosen] = 20.0
     L.router_bias = bias
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=1024)
+    layer.set_small_tokens(PATHS[path])
     x = synth.make_x(7, 600)
     out, r = run(layer, x)
     assert set(np.unique(r["idx"]).tolist()) == set(chosen)
@@ -156,6 +167,10 @@ def test_deterministic(host0, dev0):
 
 
 def test_short_stack(oracle, lib):
+    """The stack entry against the layers run one by one (bit-identical), and each layer
+    teacher-forced against the oracle: the oracle gets the GPU's own input of that layer,
+    so a routing choice that an earlier layer's rounding moved across a narrow gap does
+    not carry into later layers."""
     hosts = [synth.stack_layer(l) for l in range(3)]
     ws = lib.new_workspace(64)
     layers = [lib.MoELayer(lib.DeviceWeights(h), max_tokens=64, workspace=ws) for h in hosts]
@@ -166,19 +181,20 @@ def test_short_stack(oracle, lib):
         stack.forward_(x)
         torch.cuda.synchronize()
         got = to_host(x)
-        # the oracle chains its own bf16 outputs; tokens with a routing near-tie in any
-        # layer are left out (their downstream value depends on the valid choice made)
         cur = x_np.copy()
-        keep = np.ones(T, bool)
-        for h in hosts:
-            r = oracle.forward(h, cur, residual=True)
-            keep &= r["gap"] > 1e-4
-            cur = r["out"]
-        # about 2% of tokens sit within 1e-4 of a tie at each layer of this router
-        assert keep.sum() >= T // 2
-        ref = bf16_to_f64(cur[keep])
-        err = np.max(np.abs(bf16_to_f64(got[keep]) - ref))
-        assert err <= 1e-2 * np.max(np.abs(ref)), err
+        for h, layer in zip(hosts, layers):
+            inp = cur
+            cur = to_host(layer.forward(to_dev(inp), residual=True))
+            torch.cuda.synchronize()
+            assert layer.get_error() == 0
+            r = oracle.forward(h, inp, residual=True)
+            keep = r["gap"] > 1e-4
+            # about 2% of tokens sit within 1e-4 of a tie at each layer of this router
+            assert keep.sum() >= T // 2
+            ref = bf16_to_f64(r["out"][keep])
+            err = np.max(np.abs(bf16_to_f64(cur[keep]) - ref))
+            assert err <= 1e-2 * np.max(np.abs(ref)), err
+        assert np.array_equal(cur, got)
         # the host-memory entry gives the same bytes as the device entry
         xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
         oh = torch.empty_like(xh).pin_memory()
@@ -205,6 +221,9 @@ def test_argument_errors(lib, dev0):
     assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
     with pytest.raises(_abi.MoEError) as ei:
         _abi.moe_forward_residual(dev0.handle, x.data_ptr(), 16, x.data_ptr() + 4096)
+    assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
+    with pytest.raises(_abi.MoEError) as ei:
+        _abi.moe_layer_set_small_tokens(dev0.handle, -1)
     assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert dev0.get_error() == 0
