@@ -80,8 +80,6 @@ def lib() -> C.CDLL:
         L.moe_stack_forward_launches.restype = I
         L.moe_layer_get_error.argtypes = [P]
         L.moe_layer_get_error.restype = S
-        L.moe_layer_set_small_tokens.argtypes = [P, C.c_int]
-        L.moe_layer_set_small_tokens.restype = S
         L.moe_layer_destroy.argtypes = [P]
         L.moe_layer_destroy.restype = None
         L.moe_status_string.argtypes = [S]
@@ -157,10 +155,6 @@ def moe_forward_launches(layer: int, T: int) -> int:
 def moe_stack_forward_launches(layers, T: int) -> int:
     arr = (C.c_void_p * len(layers))(*layers)
     return int(lib().moe_stack_forward_launches(arr, len(layers), T))
-
-
-def moe_layer_set_small_tokens(layer: int, max_tokens: int) -> None:
-    _check(lib().moe_layer_set_small_tokens(layer, max_tokens), "moe_layer_set_small_tokens")
 
 
 def moe_layer_get_error(layer: int) -> int:

@@ -18,8 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_layer.so")
-SOURCES = ["router.cu", "expert_gemm.cu", "down.cu", "small_gemm.cu", "decode.cu", "decode_layers.cu", "moe_layer.cu",
-           "noalloc.cu"]
+SOURCES = ["router.cu", "expert_gemm.cu", "down.cu", "decode.cu", "decode_layers.cu", "moe_layer.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

@@ -61,20 +61,6 @@ struct GateUpParams {
   const int* row_dst;         // [9T] slot id (t*8+k) of each routed permuted row
 };
 
-// Grouped expert GEMMs for few tokens per expert (small_gemm.cu).
-struct SmallParams {
-  const int* offsets;          // [258] first permuted row per expert
-  const int* counts;           // [257] rows per expert (shared = T)
-  const int* row_dst;          // [9T] slot id (t*8+k) of each routed permuted row
-  const __nv_bfloat16* x_ilv;  // [T][2048] K-interleaved activations
-  __nv_bfloat16* h;            // [9T][512] silu(gate) * up, K-interleaved columns
-  __nv_bfloat16* y;            // [9T][2048] W_down h per permuted row
-  int T;
-  unsigned int* err;
-  const uint32_t *gq, *uq, *sgq, *suq, *dq, *sdq;   // packed codes
-  const uint16_t *gs, *gb, *us, *ub, *sgs, *sgb, *sus, *sub, *ds, *db, *sds, *sdb;   // scales, biases
-};
-
 struct DownParams {
   const int* tiles;      // [258]
   const int* offsets;
@@ -163,9 +149,6 @@ cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s);
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
                           const CUtensorMap& squ, const CUtensorMap& hs, const GateUpParams& p, int grid,
                           cudaStream_t s);
-// which = 0: gate/up (x_ilv -> h), 1: down (h -> y); grid: one CTA per SM
-cudaError_t launch_small_gemms(const SmallParams& p, int grid, cudaStream_t s, int which);
-cudaError_t set_small_attributes();
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,

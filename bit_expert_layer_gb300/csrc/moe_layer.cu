@@ -32,7 +32,6 @@ struct moe_layer {
   uint8_t* ws;
   size_t ws_bytes;
   int num_sms;
-  int small_max;   // prefill calls with T <= small_max use the weight-streaming grouped kernels
   // workspace segments
   unsigned int* err;
   unsigned int* dec_counter;
@@ -70,12 +69,12 @@ void set_detail(const char* what, cudaError_t e) {
 // durations are resolved (and the record cleared) by moe_profiler_read.
 enum KernelId {
   K_ROUTER, K_SCAN, K_SCATTER, K_GATEUP, K_DOWN, K_COMBINE, K_DEC_ROUTER, K_DEC_LAYERS, K_NORM,
-  K_SMALL_GU, K_SMALL_DN, K_COUNT
+  K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"router_prefill", "route_scan",    "route_scatter",
                                            "gateup",         "down",          "combine",
                                            "decode_router",  "decode_layers",
-                                           "rmsnorm",        "small_gateup",  "small_down"};
+                                           "rmsnorm"};
 struct ProfRec {
   int id;
   cudaEvent_t a, b;
@@ -410,33 +409,18 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   if (st != MOE_OK) return st;
   auto U16 = [](const void* p) { return static_cast<const uint16_t*>(p); };
   const moe_weights_t& w = L->w;
-  if (T <= L->small_max) {
-    // few rows per expert: the weight-streaming grouped kernels (same h and y layouts)
-    auto U32 = [](const void* p) { return static_cast<const uint32_t*>(p); };
-    const SmallParams sp{L->offsets, L->counts, L->row_dst, L->x_ilv, L->h, L->y, T, L->err,
-                         U32(w.gate.q), U32(w.up.q), U32(w.sh_gate.q), U32(w.sh_up.q), U32(w.down.q),
-                         U32(w.sh_down.q),
-                         U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
-                         U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                         U16(w.down.scales), U16(w.down.biases), U16(w.sh_down.scales), U16(w.sh_down.biases)};
-    MOE_TRY(timed(K_SMALL_GU, s, L->err, [&] { return launch_small_gemms(sp, L->num_sms, s, 0); }),
-            "small gate/up launch");
-    MOE_TRY(timed(K_SMALL_DN, s, L->err, [&] { return launch_small_gemms(sp, L->num_sms, s, 1); }),
-            "small down launch");
-  } else {
-    GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
-                    U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
-                    U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                    L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst};
-    const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
-    MOE_TRY(timed(K_GATEUP, s, L->err,
-                  [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
-            "gate/up launch");
-    DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
-                  U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
-                  pipe_trace() ? L->pipe + 16 : nullptr};
-    MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
-  }
+  GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
+                  U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
+                  U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
+                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst};
+  const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
+  MOE_TRY(timed(K_GATEUP, s, L->err,
+                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
+          "gate/up launch");
+  DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
+                U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
+                pipe_trace() ? L->pipe + 16 : nullptr};
+  MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
                   return launch_combine(L->y, L->slot_row, L->row_w, static_cast<const __nv_bfloat16*>(x_orig),
@@ -488,7 +472,6 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
   L->w = *weights;
   L->ws = static_cast<uint8_t*>(workspace);
   L->ws_bytes = workspace_bytes;
-  L->small_max = MOE_SMALL_TOKENS_DEFAULT;
   carve(cfg->max_tokens, L->ws, L);
 
   auto fail = [&](moe_status_t s) { delete L; return s; };
@@ -505,8 +488,7 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
     snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled entry point unavailable");
     return fail(MOE_ERR_CUDA);
   }
-  if ((e = set_router_attributes()) != cudaSuccess || (e = set_gemm_attributes()) != cudaSuccess ||
-      (e = set_small_attributes()) != cudaSuccess)
+  if ((e = set_router_attributes()) != cudaSuccess || (e = set_gemm_attributes()) != cudaSuccess)
     return fail(cuda_fail("kernel attributes", e));
   // workspace state shared by every layer bound to it: the error word, the decode
   // ticket and the fused decode kernel's tagged tables and epoch, which start at zero
@@ -620,12 +602,6 @@ int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, i
   int n = 0;
   for (int l = 0; l < n_layers; ++l) n += moe_forward_launches(layers[l], T);
   return n;
-}
-
-moe_status_t moe_layer_set_small_tokens(moe_layer_t* L, int max_tokens) {
-  if (!L || max_tokens < 0) return MOE_ERR_INVALID_ARG;
-  L->small_max = max_tokens;
-  return MOE_OK;
 }
 
 moe_status_t moe_layer_get_error(moe_layer_t* L) {

@@ -133,10 +133,6 @@ class MoELayer:
                        r["offsets"].data_ptr(), r["perm"].data_ptr(), _stream_handle(stream))
         return r
 
-    def set_small_tokens(self, max_tokens: int) -> None:
-        """Prefill calls with T <= max_tokens use the weight-streaming grouped kernels."""
-        _abi.moe_layer_set_small_tokens(self.handle, max_tokens)
-
     def get_error(self) -> int:
         return _abi.moe_layer_get_error(self.handle)
 

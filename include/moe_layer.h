@@ -162,16 +162,6 @@ int moe_forward_launches(const moe_layer_t* layer, int T);
  * array or layer, n_layers < 1 or T out of range. */
 int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, int T);
 
-/* Prefill calls (T > 8) with T <= max_tokens run the grouped expert GEMMs as
- * weight-streaming dequant-GEMV kernels (mma.sync over groups of 8 rows of an expert);
- * larger calls run the tcgen05 tile kernels.  Both compute the same layer and give the
- * same results up to fp32 summation order; the choice is a speed trade-off.
- * max_tokens = 0 (the default) always selects the tile kernels.  Host-side only, takes
- * effect for calls enqueued afterwards.  MOE_ERR_INVALID_ARG for a NULL layer or a
- * negative count. */
-#define MOE_SMALL_TOKENS_DEFAULT 0
-moe_status_t moe_layer_set_small_tokens(moe_layer_t* layer, int max_tokens);
-
 /* Synchronise the device, read and clear the layer's device error word.
  * MOE_OK if nothing was recorded. */
 moe_status_t moe_layer_get_error(moe_layer_t* layer);

@@ -4,9 +4,7 @@ Workloads are the seeded synthetic layer at its real shapes: T=32 (the reference
 configuration), T=1 and 8 (decode), T=512 uniform, T=4096 with the skewed log-Zipf
 router bias, a sweep of ragged T, all tokens forced onto one expert set, in-place
 residual, determinism, a short stack, and argument errors.  The rules are in
-tests/parity.py.  Every prefill case runs on both implementations of the grouped
-expert GEMMs: the weight-streaming kernels ("small") and the tcgen05 tile kernels
-("tiles", the default).
+tests/parity.py.
 """
 from __future__ import annotations
 
@@ -36,15 +34,10 @@ def host0():
     return synth.make_layer(0)
 
 
-PATHS = {"small": 4096, "tiles": 0}   # largest T on the weight-streaming kernels
-
-
-@pytest.fixture(scope="module", params=sorted(PATHS))
-def dev0(lib, host0, request):
+@pytest.fixture(scope="module")
+def dev0(lib, host0):
     w = lib.DeviceWeights(host0)
-    layer = lib.MoELayer(w, max_tokens=4096)
-    layer.set_small_tokens(PATHS[request.param])
-    return layer
+    return lib.MoELayer(w, max_tokens=4096)
 
 
 def to_dev(x_np):
@@ -99,11 +92,9 @@ def test_prefill_T512(oracle, host0, dev0):
     print(f"T=512 {rep} max_err={err:.3e} scale={scale:.3e}")
 
 
-@pytest.mark.parametrize("path", sorted(PATHS))
-def test_skewed_T4096(oracle, lib, path):
+def test_skewed_T4096(oracle, lib):
     L = synth.make_layer(0, skew=True)
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=4096)
-    layer.set_small_tokens(PATHS[path])
     x = synth.make_x(0, 4096)
     out, r = run(layer, x)
     rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
@@ -125,15 +116,13 @@ def test_skewed_T4096(oracle, lib, path):
           f"max_err={err:.3e} scale={scale:.3e}")
 
 
-@pytest.mark.parametrize("path", sorted(PATHS))
-def test_all_tokens_on_one_expert_set(oracle, lib, path):
+def test_all_tokens_on_one_expert_set(oracle, lib):
     L = synth.make_layer(7)
     chosen = [3, 17, 40, 77, 100, 150, 200, 255]
     bias = np.zeros(256, np.float32)
     bias[chosen] = 20.0
     L.router_bias = bias
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=1024)
-    layer.set_small_tokens(PATHS[path])
     x = synth.make_x(7, 600)
     out, r = run(layer, x)
     assert set(np.unique(r["idx"]).tolist()) == set(chosen)
@@ -221,9 +210,6 @@ def test_argument_errors(lib, dev0):
     assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
     with pytest.raises(_abi.MoEError) as ei:
         _abi.moe_forward_residual(dev0.handle, x.data_ptr(), 16, x.data_ptr() + 4096)
-    assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
-    with pytest.raises(_abi.MoEError) as ei:
-        _abi.moe_layer_set_small_tokens(dev0.handle, -1)
     assert ei.value.status == _abi.MOE_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert dev0.get_error() == 0
