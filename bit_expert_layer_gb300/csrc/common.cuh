@@ -365,6 +365,43 @@ __host__ __device__ __forceinline__ int ilv_row(int r) { return (r & ~7) | ((r &
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// RMSNorm of one token row over a CTA of 256 threads, thread c holding elements
+// 8c..8c+7 (bf16 pairs in v): returns 1 / sqrt(mean(x^2) + 1e-6) in every thread.  The
+// fp32 sum of squares has one fixed order (each thread's 8 elements in order, a
+// butterfly over the lanes, the 8 warps in order), shared by every kernel that
+// normalises a layer input, so they all give the same bits.  s_warp: 8 floats of shared
+// memory; contains two __syncthreads.
+__device__ __forceinline__ float row_inv_rms(const uint4& v, float* s_warp) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ss = fmaf(bf16lo(u[i]), bf16lo(u[i]), ss);
+    ss = fmaf(bf16hi(u[i]), bf16hi(u[i]), ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += s_warp[w];
+  __syncthreads();
+  return 1.0f / sqrtf(t / static_cast<float>(HID) + 1e-6f);
+}
+// bf16(x * r * w) for the 8 elements of v and of the matching norm weights g.
+__device__ __forceinline__ uint4 rms_scale8(const uint4& v, const uint4& g, float r) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(bf16lo(u[i]) * r * bf16lo(gw[i]), bf16hi(u[i]) * r * bf16hi(gw[i]));
+    o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"

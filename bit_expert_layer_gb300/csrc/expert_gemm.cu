@@ -439,7 +439,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const int* __restrict__ slot_row,
                                                       const float* __restrict__ row_w,
                                                       const __nv_bfloat16* x, __nv_bfloat16* out, int T,
-                                                      int residual) {
+                                                      int residual, const __nv_bfloat16* __restrict__ next_norm_w,
+                                                      __nv_bfloat16* __restrict__ next_xn) {
   const int t = blockIdx.x, c = threadIdx.x;
   float acc[8];
 #pragma unroll
@@ -475,6 +476,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     rp[i] = *reinterpret_cast<const uint32_t*>(&b2);
   }
   *reinterpret_cast<uint4*>(out + o) = r;
+  if (next_norm_w) {
+    // the next stacked layer's input RMSNorm of this output row, while it is in registers
+    __shared__ float s_warp[8];
+    const float rr = row_inv_rms(r, s_warp);
+    *reinterpret_cast<uint4*>(next_xn + o) = rms_scale8(r, ldg_nc_v4(next_norm_w + c * 8), rr);
+  }
 }
 
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
@@ -485,8 +492,9 @@ cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CU
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
-                           __nv_bfloat16* out, int T, int residual, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, row_w, x, out, T, residual);
+                           __nv_bfloat16* out, int T, int residual, const __nv_bfloat16* next_norm_w,
+                           __nv_bfloat16* next_xn, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, row_w, x, out, T, residual, next_norm_w, next_xn);
   return cudaGetLastError();
 }
 

@@ -151,9 +151,11 @@ cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CU
                           cudaStream_t s);
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s);
+// next_norm_w != nullptr: also writes next_xn = RMSNorm(out) with those weights (the next
+// stacked layer's input)
 cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
-                           __nv_bfloat16* out,
-                           int T, int residual, cudaStream_t s);
+                           __nv_bfloat16* out, int T, int residual, const __nv_bfloat16* next_norm_w,
+                           __nv_bfloat16* next_xn, cudaStream_t s);
 cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s);
 cudaError_t set_kernel_attributes();

@@ -387,9 +387,15 @@ moe_status_t decode_forward(moe_layer* const* layers, int n, const void* x, int 
 }
 
 // The layer's input to routing and experts: x itself, or its RMSNorm when the layer has one.
-moe_status_t layer_input(moe_layer* L, const void* x, int T, cudaStream_t s, const void** xin) {
+// The layer's input: x, or its RMSNorm in L->xn (computed here unless the previous
+// stacked layer's combine already wrote it: xn_ready).
+moe_status_t layer_input(moe_layer* L, const void* x, int T, cudaStream_t s, const void** xin, bool xn_ready) {
   *xin = x;
   if (!L->w.norm_w) return MOE_OK;
+  if (xn_ready) {
+    *xin = L->xn;
+    return MOE_OK;
+  }
   MOE_TRY(timed(K_NORM, s, L->err,
                 [&] {
                   return launch_rmsnorm(static_cast<const __nv_bfloat16*>(x),
@@ -400,10 +406,14 @@ moe_status_t layer_input(moe_layer* L, const void* x, int T, cudaStream_t s, con
   return MOE_OK;
 }
 
-moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, int residual, cudaStream_t s) {
+// One prefill layer.  next: the following stacked layer, whose input RMSNorm (if it has
+// one) the combine computes into next->xn; xn_ready: this layer's RMSNorm is already in
+// L->xn.
+moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, int residual, cudaStream_t s,
+                          moe_layer* next = nullptr, bool xn_ready = false) {
   if (T <= DEC_MAX_T) return decode_forward(&L, 1, x_orig, T, out, residual, s);
   const void* x = nullptr;
-  const moe_status_t sn = layer_input(L, x_orig, T, s, &x);
+  const moe_status_t sn = layer_input(L, x_orig, T, s, &x, xn_ready);
   if (sn != MOE_OK) return sn;
   const moe_status_t st = route_prefill(L, x, T, 1, s);
   if (st != MOE_OK) return st;
@@ -423,8 +433,11 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
+                  const bool fuse = next && next->w.norm_w;
                   return launch_combine(L->y, L->slot_row, L->row_w, static_cast<const __nv_bfloat16*>(x_orig),
-                                        static_cast<__nv_bfloat16*>(out), T, residual, s);
+                                        static_cast<__nv_bfloat16*>(out), T, residual,
+                                        fuse ? static_cast<const __nv_bfloat16*>(next->w.norm_w) : nullptr,
+                                        fuse ? next->xn : nullptr, s);
                 }),
           "combine launch");
   return MOE_OK;
@@ -527,7 +540,7 @@ moe_status_t moe_route(moe_layer_t* L, const void* x, int T, int32_t* topk_idx, 
   if (!aligned(x, 16)) return MOE_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* xin = nullptr;
-  const moe_status_t sn = layer_input(L, x, T, s, &xin);
+  const moe_status_t sn = layer_input(L, x, T, s, &xin, false);
   if (sn != MOE_OK) return sn;
   x = xin;
   if (T <= DEC_MAX_T) {
@@ -568,8 +581,11 @@ moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x
     if (st != MOE_OK) return st;
   }
   if (T <= DEC_MAX_T) return decode_forward(layers, n_layers, x_io, T, x_io, 1, reinterpret_cast<cudaStream_t>(stream));
+  // each layer's combine also normalises the next layer's input (no separate RMSNorm pass)
   for (int l = 0; l < n_layers; ++l) {
-    const moe_status_t st = forward_impl(layers[l], x_io, T, x_io, 1, reinterpret_cast<cudaStream_t>(stream));
+    moe_layer* next = l + 1 < n_layers ? layers[l + 1] : nullptr;
+    const moe_status_t st = forward_impl(layers[l], x_io, T, x_io, 1, reinterpret_cast<cudaStream_t>(stream), next,
+                                         l > 0);
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
@@ -599,8 +615,9 @@ int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, i
   for (int l = 0; l < n_layers; ++l)
     if (!layers[l] || T < 1 || T > layers[l]->cfg.max_tokens) return 0;
   if (T <= DEC_MAX_T) return (n_layers + DEC_MAX_LAYERS - 1) / DEC_MAX_LAYERS;
+  // layers after the first get their input RMSNorm from the previous layer's combine
   int n = 0;
-  for (int l = 0; l < n_layers; ++l) n += moe_forward_launches(layers[l], T);
+  for (int l = 0; l < n_layers; ++l) n += moe_forward_launches(layers[l], T) - (l > 0 && layers[l]->w.norm_w ? 1 : 0);
   return n;
 }
 

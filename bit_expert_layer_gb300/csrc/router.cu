@@ -347,51 +347,22 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   }
 }
 
-// Input RMSNorm of a stacked layer: xn = bf16(x / sqrt(mean(x^2) + 1e-6) * w), one warp
-// per token row, fp32 sum of squares in a fixed order (lane partials, xor tree).
+// Input RMSNorm of a stacked layer: xn = bf16(x / sqrt(mean(x^2) + 1e-6) * w), one CTA
+// of 256 threads per token row (the fixed summation order of row_inv_rms, which the
+// combine uses when it normalises the next layer's input itself).
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
                                                       const __nv_bfloat16* __restrict__ w,
                                                       __nv_bfloat16* __restrict__ xn, int T) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + warp;
-  if (row >= T) return;
-  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(row) * HID);
-  const uint4* wv = reinterpret_cast<const uint4*>(w);
-  uint4 v[8];
-  float ss = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    v[j] = ldg_nc_v4(src + lane + 32 * j);
-    const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ss = fmaf(bf16lo(u[i]), bf16lo(u[i]), ss);
-      ss = fmaf(bf16hi(u[i]), bf16hi(u[i]), ss);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float r = 1.0f / sqrtf(ss / static_cast<float>(HID) + 1e-6f);
-  uint4* dst = reinterpret_cast<uint4*>(xn + static_cast<size_t>(row) * HID);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint4 g = ldg_nc_v4(wv + lane + 32 * j);
-    const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 b2 = __floats2bfloat162_rn(bf16lo(u[i]) * r * bf16lo(gw[i]),
-                                                      bf16hi(u[i]) * r * bf16hi(gw[i]));
-      o[i] = *reinterpret_cast<const uint32_t*>(&b2);
-    }
-    dst[lane + 32 * j] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+  __shared__ float s_warp[8];
+  const int row = blockIdx.x, c = threadIdx.x;
+  const uint4 v = ldg_nc_v4(x + static_cast<size_t>(row) * HID + c * 8);
+  const float r = row_inv_rms(v, s_warp);
+  *reinterpret_cast<uint4*>(xn + static_cast<size_t>(row) * HID + c * 8) = rms_scale8(v, ldg_nc_v4(w + c * 8), r);
 }
 
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* xn, int T,
                            cudaStream_t s) {
-  rmsnorm_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, w, xn, T);
+  rmsnorm_kernel<<<T, 256, 0, s>>>(x, w, xn, T);
   return cudaGetLastError();
 }
 
