@@ -389,6 +389,29 @@ __device__ __forceinline__ float row_inv_rms(const uint4& v, float* s_warp) {
   __syncthreads();
   return 1.0f / sqrtf(t / static_cast<float>(HID) + 1e-6f);
 }
+// Dot product of one token row with a weight row over a CTA of 256 threads, thread c
+// holding elements 8c..8c+7 of both: the same fixed order as row_inv_rms (each thread's 8
+// products in order, a butterfly over the lanes, the 8 warps in order); the result in
+// every thread.  s_warp: 8 floats of shared memory; contains two __syncthreads.
+__device__ __forceinline__ float row_dot(const uint4& v, const uint4& g, float* s_warp) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+  float d = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    d = fmaf(bf16lo(u[i]), bf16lo(gw[i]), d);
+    d = fmaf(bf16hi(u[i]), bf16hi(gw[i]), d);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = d;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += s_warp[w];
+  __syncthreads();
+  return t;
+}
 // bf16(x * r * w) for the 8 elements of v and of the matching norm weights g.
 __device__ __forceinline__ uint4 rms_scale8(const uint4& v, const uint4& g, float r) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};

@@ -439,8 +439,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const int* __restrict__ slot_row,
                                                       const float* __restrict__ row_w,
                                                       const __nv_bfloat16* x, __nv_bfloat16* out, int T,
-                                                      int residual, const __nv_bfloat16* __restrict__ next_norm_w,
-                                                      __nv_bfloat16* __restrict__ next_xn) {
+                                                      int residual, NextLayerIn nx) {
   const int t = blockIdx.x, c = threadIdx.x;
   float acc[8];
 #pragma unroll
@@ -476,11 +475,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     rp[i] = *reinterpret_cast<const uint32_t*>(&b2);
   }
   *reinterpret_cast<uint4*>(out + o) = r;
-  if (next_norm_w) {
-    // the next stacked layer's input RMSNorm of this output row, while it is in registers
+  if (nx.norm_w) {
+    // The next stacked layer's inputs from this output row while it is in registers: its
+    // RMSNorm, the K-interleaved copy its gate/up GEMM gathers, and its shared-expert gate
+    // (the work its scatter does otherwise, in the same summation order).
     __shared__ float s_warp[8];
     const float rr = row_inv_rms(r, s_warp);
-    *reinterpret_cast<uint4*>(next_xn + o) = rms_scale8(r, ldg_nc_v4(next_norm_w + c * 8), rr);
+    const uint4 xn = rms_scale8(r, ldg_nc_v4(nx.norm_w + c * 8), rr);
+    *reinterpret_cast<uint4*>(nx.xn + o) = xn;
+    *reinterpret_cast<uint4*>(nx.x_ilv + o) = interleave8(xn);
+    const float dot = row_dot(xn, ldg_nc_v4(nx.gate_w + c * 8), s_warp);
+    if (c == 0) {
+      const int srow = 8 * T + t;
+      nx.row_dst[srow] = srow;
+      nx.row_w[srow] = 1.0f / (1.0f + expf(-dot));
+    }
   }
 }
 
@@ -492,9 +501,8 @@ cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CU
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
-                           __nv_bfloat16* out, int T, int residual, const __nv_bfloat16* next_norm_w,
-                           __nv_bfloat16* next_xn, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, row_w, x, out, T, residual, next_norm_w, next_xn);
+                           __nv_bfloat16* out, int T, int residual, const NextLayerIn& nx, cudaStream_t s) {
+  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, row_w, x, out, T, residual, nx);
   return cudaGetLastError();
 }
 

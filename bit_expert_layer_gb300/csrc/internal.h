@@ -41,7 +41,8 @@ struct ScatterParams {
   const __nv_bfloat16* x;
   const __nv_bfloat16* shared_gate_w;   // [2048]
   __nv_bfloat16* x_ilv;    // [T][2048] copy of x with K-interleaved rows (read by the gate/up gather)
-  int gather;              // 0: routing tables only (moe_route)
+  int gather;              // 0: routing tables only (moe_route; or the previous stacked layer's
+                           // combine already wrote x_ilv and the shared rows)
   unsigned int* err;
 };
 
@@ -151,11 +152,19 @@ cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CU
                           cudaStream_t s);
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s);
-// next_norm_w != nullptr: also writes next_xn = RMSNorm(out) with those weights (the next
-// stacked layer's input)
+// The next stacked layer's inputs that the combine writes from its output rows (norm_w
+// == nullptr: none): the RMSNorm xn, its K-interleaved copy and the shared-expert rows'
+// index and gate, in that layer's workspace.
+struct NextLayerIn {
+  const __nv_bfloat16* norm_w;
+  const __nv_bfloat16* gate_w;
+  __nv_bfloat16* xn;
+  __nv_bfloat16* x_ilv;
+  int* row_dst;
+  float* row_w;
+};
 cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
-                           __nv_bfloat16* out, int T, int residual, const __nv_bfloat16* next_norm_w,
-                           __nv_bfloat16* next_xn, cudaStream_t s);
+                           __nv_bfloat16* out, int T, int residual, const NextLayerIn& nx, cudaStream_t s);
 cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s);
 cudaError_t set_kernel_attributes();

@@ -415,7 +415,9 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   const void* x = nullptr;
   const moe_status_t sn = layer_input(L, x_orig, T, s, &x, xn_ready);
   if (sn != MOE_OK) return sn;
-  const moe_status_t st = route_prefill(L, x, T, 1, s);
+  // the scatter's copy of x and shared gate are already there when the previous layer's
+  // combine wrote them with the normalised input
+  const moe_status_t st = route_prefill(L, x, T, xn_ready && L->w.norm_w ? 0 : 1, s);
   if (st != MOE_OK) return st;
   auto U16 = [](const void* p) { return static_cast<const uint16_t*>(p); };
   const moe_weights_t& w = L->w;
@@ -433,11 +435,13 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
-                  const bool fuse = next && next->w.norm_w;
+                  NextLayerIn nx{};
+                  if (next && next->w.norm_w)
+                    nx = NextLayerIn{static_cast<const __nv_bfloat16*>(next->w.norm_w),
+                                     static_cast<const __nv_bfloat16*>(next->w.shared_gate_w), next->xn,
+                                     next->x_ilv, next->row_dst, next->row_w};
                   return launch_combine(L->y, L->slot_row, L->row_w, static_cast<const __nv_bfloat16*>(x_orig),
-                                        static_cast<__nv_bfloat16*>(out), T, residual,
-                                        fuse ? static_cast<const __nv_bfloat16*>(next->w.norm_w) : nullptr,
-                                        fuse ? next->xn : nullptr, s);
+                                        static_cast<__nv_bfloat16*>(out), T, residual, nx, s);
                 }),
           "combine launch");
   return MOE_OK;

@@ -16,7 +16,8 @@
 //                          the per-row weight (first CTA of each router block), one
 //                          K-interleaved copy of x per token (the gate/up GEMM gathers
 //                          its rows from it by token) and, on the same read of x, the
-//                          shared-expert gate sigmoid(g_s . x).
+//                          shared-expert gate sigmoid(g_s . x) (in a stack, the previous
+//                          layer's combine writes these two instead).
 #include "common.cuh"
 #include "internal.h"
 
@@ -319,23 +320,27 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
     if (t >= p.T) break;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * HID);
     uint4 v[8];
+    // the summation order of row_dot (chunk lane + 32c is "thread" lane of "warp" c), so
+    // the combine, which computes this dot for the next stacked layer, gets the same bits
     float dot = 0.0f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const uint4 raw = ldg_nc_v4(src + lane + 32 * c);
       const uint4 g = ldg_nc_v4(gsv + lane + 32 * c);
-      dot = fmaf(bf16lo(raw.x), bf16lo(g.x), dot);
-      dot = fmaf(bf16hi(raw.x), bf16hi(g.x), dot);
-      dot = fmaf(bf16lo(raw.y), bf16lo(g.y), dot);
-      dot = fmaf(bf16hi(raw.y), bf16hi(g.y), dot);
-      dot = fmaf(bf16lo(raw.z), bf16lo(g.z), dot);
-      dot = fmaf(bf16hi(raw.z), bf16hi(g.z), dot);
-      dot = fmaf(bf16lo(raw.w), bf16lo(g.w), dot);
-      dot = fmaf(bf16hi(raw.w), bf16hi(g.w), dot);
+      float d = 0.0f;
+      d = fmaf(bf16lo(raw.x), bf16lo(g.x), d);
+      d = fmaf(bf16hi(raw.x), bf16hi(g.x), d);
+      d = fmaf(bf16lo(raw.y), bf16lo(g.y), d);
+      d = fmaf(bf16hi(raw.y), bf16hi(g.y), d);
+      d = fmaf(bf16lo(raw.z), bf16lo(g.z), d);
+      d = fmaf(bf16hi(raw.z), bf16hi(g.z), d);
+      d = fmaf(bf16lo(raw.w), bf16lo(g.w), d);
+      d = fmaf(bf16hi(raw.w), bf16hi(g.w), d);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      dot += d;
       v[c] = interleave8(raw);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     if (lane == 0) {
       const int srow = n8 + t;
       p.row_dst[srow] = srow;
@@ -379,7 +384,7 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
-  route_scatter_kernel<<<dim3(nblk, SC_SPLIT), SC_THREADS, 0, s>>>(p);
+  route_scatter_kernel<<<dim3(nblk, p.gather ? SC_SPLIT : 1), SC_THREADS, 0, s>>>(p);
   return cudaGetLastError();
 }
 
