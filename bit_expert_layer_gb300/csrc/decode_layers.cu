@@ -140,9 +140,14 @@ __device__ __forceinline__ void cta_copy(void* dst, const void* src, int bytes) 
 }
 
 // ---- tagged words
+// Published with an atomic exchange (performed at L2, its old value discarded) rather than
+// a plain store: measured with per-CTA phase stamps, plain relaxed stores of the router
+// logits became visible to the polling CTAs 4-7 us after they were issued (write-through,
+// release and fenced stores likewise), the exchanges about 2 us after.
 __device__ __forceinline__ void st_tagged(unsigned long long* p, uint32_t payload, uint32_t tag) {
   const unsigned long long v = (static_cast<unsigned long long>(tag) << 32) | payload;
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+  asm volatile("{\n\t.reg .b64 old;\n\tatom.relaxed.gpu.global.exch.b64 old, [%0], %1;\n\t}" ::"l"(p), "l"(v)
+               : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
   unsigned long long v;
