@@ -54,7 +54,10 @@ static_assert(OFF_X % 1024 == 0 && OFF_P % 1024 == 0, "swizzled tiles need 1024-
 constexpr int STG_ROW = 32 * 2;                      // bytes of one staged row (32 bf16)
 constexpr int STG_BUF = 32 * STG_ROW;                // one 32 x 32 staging tile
 static_assert(4 * GU_STG_BUFS * STG_BUF == GU_STG_BYTES, "staging size");
-static_assert((512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4) % 16 == 0, "schedule and staging alignment");
+static_assert((512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4) % 16 == 0, "schedule alignment");
+// the epilogue's staging tiles are TMA-store sources: 128-byte aligned (misc is 1024-aligned)
+constexpr int STG_OFF = (512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + 127) / 128 * 128;
+static_assert(STG_OFF % 128 == 0 && OFF_MISC % 1024 == 0, "staging alignment");
 }  // namespace
 
 __global__ void __launch_bounds__(GU_THREADS, 1)
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   int* s_cnt = s_off + (NEXP + 2);
   int* s_tok = reinterpret_cast<int*>(misc + 512 + GX_TAB_BYTES);   // [GU_GW][GU_GROWS] token ids
   int4* sched = reinterpret_cast<int4*>(s_tok + GU_GW * GU_GROWS);   // [GU_SCHED_CAP] this CTA's tiles
-  uint8_t* stg = reinterpret_cast<uint8_t*>(sched + GU_SCHED_CAP);     // [4 warps][GU_STG_BUFS][32][32] bf16
+  uint8_t* stg = misc + STG_OFF;                                       // [4 warps][GU_STG_BUFS][32][32] bf16
   stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
