@@ -31,8 +31,10 @@ constexpr int RT_STAGES = 4;
 constexpr int RT_A_BYTES = RT_BM * 64 * 2;          // 16 KB  x tile
 constexpr int RT_B_BYTES = NEXP * 64 * 2;           // 32 KB  router tile
 constexpr int RT_STAGE_BYTES = RT_A_BYTES + RT_B_BYTES;
-constexpr int RT_SMEM = RT_STAGES * RT_STAGE_BYTES + 1024 + 3072;
-constexpr int RT_THREADS = 128;
+constexpr int RT_SEGS = 4;                          // expert segments scanned by separate warps
+constexpr int RT_CAND_BYTES = (RT_SEGS - 1) * 8 * RT_BM * 8;   // top-8 lists of segments 1-3
+constexpr int RT_SMEM = RT_STAGES * RT_STAGE_BYTES + 1024 + 3072 + RT_CAND_BYTES;
+constexpr int RT_THREADS = 128 * RT_SEGS;
 
 // Grouped expert GEMMs: 128 weight rows (M) x up to 256 tokens (N) per tile, K step 64
 // (= one quantisation group).

@@ -82,11 +82,16 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   const uint32_t bar0 = smem_u32(bars);
 #define PFULL(s) (bar0 + 8u * (s))
 #define PEMPTY(s) (bar0 + 8u * (GU_NP + (s)))
-#define XFULL(s) (bar0 + 8u * (2 * GU_NP + (s)))
-#define XEMPTY(s) (bar0 + 8u * (2 * GU_NP + GU_NX + (s)))
-#define AFULL(s) (bar0 + 8u * (2 * GU_NP + 2 * GU_NX + (s)))
-#define AEMPTY(s) (bar0 + 8u * (2 * GU_NP + 2 * GU_NX + GU_NA + (s)))
-  constexpr int NB = 2 * GU_NP + 2 * GU_NX + 2 * GU_NA;
+#define XEMPTY(s) (bar0 + 8u * (2 * GU_NP + (s)))
+#define AEMPTY(s) (bar0 + 8u * (2 * GU_NP + GU_NX + (s)))
+  // One READY barrier per K step: the dequant threads arrive on it after writing the
+  // weight stage, the gather threads once their copies into the activation stage landed,
+  // so the MMA issuer polls one barrier per step.  With a ring of max(GU_NX, GU_NA), the
+  // arrivals for step it + GU_NR wait for stages that the MMAs of step it or later free,
+  // and those MMAs follow the completion of step it's phase: phases never overlap.
+  constexpr int GU_NR = GU_NX > GU_NA ? GU_NX : GU_NA;
+#define READY(s) (bar0 + 8u * (2 * GU_NP + GU_NX + GU_NA + (s)))
+  constexpr int NB = 2 * GU_NP + GU_NX + GU_NA + GU_NR;
   static_assert(8 * (NB + 3) <= 256, "barriers overlap the TMEM slot");
   const uint32_t ACCF = bar0 + 8u * NB, ACCE = bar0 + 8u * (NB + 1), DRAIN = bar0 + 8u * (NB + 2);
 
@@ -95,14 +100,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       mbar_init(PFULL(s), 1);
       mbar_init(PEMPTY(s), 256);
     }
-    for (int s = 0; s < GU_NX; ++s) {
-      mbar_init(XFULL(s), GU_GW * 32);   // one arrival per gather thread, after its copies landed
-      mbar_init(XEMPTY(s), 1);
-    }
-    for (int s = 0; s < GU_NA; ++s) {
-      mbar_init(AFULL(s), 256);
-      mbar_init(AEMPTY(s), 1);
-    }
+    for (int s = 0; s < GU_NX; ++s) mbar_init(XEMPTY(s), 1);
+    for (int s = 0; s < GU_NA; ++s) mbar_init(AEMPTY(s), 1);
+    // one arrival per dequant thread and per gather thread (after its copies landed)
+    for (int s = 0; s < GU_NR; ++s) mbar_init(READY(s), 256 + GU_GW * 32);
     mbar_init(ACCF, 1);
     mbar_init(ACCE, 128);
     mbar_init(DRAIN, 1);
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         unsigned long long pc[3] = {0, 0, 0};
         const unsigned long long t_role = pp ? clock64() : 0;
         uint32_t it = 0, tc = 0;
-        uint32_t rdy = 0;   // bit 0 / 1: AFULL / XFULL of step `it` seen complete by the last poll
+        uint32_t rdy = 0;   // bit 0: READY of step `it` seen complete by the last poll
         for (int tix = 0; tix < ntiles; ++tix) {
           const TileInfo ti = sched_tile(sched, tix);
           if (!ti.ok) continue;
@@ -180,8 +181,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           bool alive = true;
           for (int kb = 0; kb < NKB; ++kb, ++it) {
             const int sa = it % GU_NA, sx = it % GU_NX;
-            if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / GU_NA) & 1, p.err, abort_flag, pc[1], pp)) ||
-                (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / GU_NX) & 1, p.err, abort_flag, pc[2], pp))) {
+            if (!(rdy & 1u) && !mbar_wait_t(READY(it % GU_NR), (it / GU_NR) & 1, p.err, abort_flag, pc[1], pp)) {
               alive = false;
               break;
             }
@@ -192,8 +192,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             // gate and up MMAs of this K step; the next step's stages are polled meanwhile
             const uint32_t nx = it + 1;
             rdy = umma_k64_x2_poll(tmem, tmem + 256, sdesc_sw128(a), sdesc_sw128(a + GX_A_BYTES), sdesc_sw128(x),
-                                   idesc, kb != 0, AFULL(nx % GU_NA), (nx / GU_NA) & 1, XFULL(nx % GU_NX),
-                                   (nx / GU_NX) & 1);
+                                   idesc, kb != 0, READY(nx % GU_NR), (nx / GU_NR) & 1);
             umma_commit(AEMPTY(sa));
             umma_commit(XEMPTY(sx));
           }
@@ -247,7 +246,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           }
           // one arrival per thread once its copies into the stage have landed; the MMA
           // issuer fences them into the async proxy after its wait
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(XFULL(s)) : "memory");
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(READY(it % GU_NR)) : "memory");
         }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int sp = it % GU_NP, sa = it % GU_NA;
+          const int sp = it % GU_NP, sa = it % GU_NA, sr = it % GU_NR;
           if (!mbar_wait_t(PFULL(sp), (it / GU_NP) & 1, p.err, abort_flag, pc[0], pp) ||
               !mbar_wait(AEMPTY(sa), ((it / GU_NA) & 1) ^ 1, p.err, abort_flag)) {
             alive = false;
@@ -327,7 +326,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           st_shared_v4(A + sw128_off(r, 6), dequant8(w1.z, ms, mbv));
           st_shared_v4(A + sw128_off(r, 7), dequant8(w1.w, ms, mbv));
           fence_proxy_async_smem();
-          mbar_arrive(AFULL(sa));
+          mbar_arrive(READY(sr));
         }
       }
     }
@@ -429,10 +428,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   }
 #undef PFULL
 #undef PEMPTY
-#undef XFULL
 #undef XEMPTY
-#undef AFULL
 #undef AEMPTY
+#undef READY
 }
 
 // ============================================================================ combine

@@ -82,23 +82,22 @@ __device__ __forceinline__ __nv_bfloat162 bf2(uint32_t bits16) {
 __device__ __forceinline__ void st_shared_v4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // MMA issue with the next step's barrier polls folded in.  On sm_103a an mbarrier poll
-// holds the issuing thread for about 200 cycles even when the phase completed long ago,
-// and one K step waits on two barriers: polling them ahead of the MMAs of the current
-// step, and reading the result only after those are issued, hides that latency.  The
-// poll is a non-blocking test_wait (acquire, CTA scope); a stage it finds not yet full is
+// holds the issuing thread for about 200 cycles even when the phase completed long ago:
+// polling ahead of the MMAs of the current step, and reading the result only after those
+// are issued, hides part of that, and fewer barriers per K step hide the rest.  The poll
+// is a non-blocking test_wait (acquire, CTA scope); a stage it finds not yet full is
 // waited for in the ordinary bounded way.  Descriptors advance 32 bytes (16 bf16) of K per
-// MMA: +2 in the 16-byte address field.  Returns bit 0 / bit 1 = first / second barrier
-// already complete.
+// MMA: +2 in the 16-byte address field.  Returns bit 0 = the barrier already complete.
 //
-// One K step of 64 into two accumulators (gate, up) that share the B operand.
+// One K step of 64 into two accumulators (gate, up) that share the B operand; one
+// barrier covers both operands of the next step.
 __device__ __forceinline__ uint32_t umma_k64_x2_poll(uint32_t d0, uint32_t d1, uint64_t a0, uint64_t a1, uint64_t b,
-                                                     uint32_t idesc, uint32_t accumulate, uint32_t nbar0,
-                                                     uint32_t npar0, uint32_t nbar1, uint32_t npar1) {
+                                                     uint32_t idesc, uint32_t accumulate, uint32_t nbar,
+                                                     uint32_t npar) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred pa, pt, q0, q1;\n\t.reg .b64 x0, x1, xb;\n\t"
+      "{\n\t.reg .pred pa, pt, q0;\n\t.reg .b64 x0, x1, xb;\n\t"
       "mbarrier.test_wait.parity.shared::cta.b64 q0, [%8], %9;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%10], %11;\n\t"
       "setp.ne.b32 pa, %7, 0;\n\t"
       "setp.ne.b32 pt, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%1], %3, %5, %6, pa;\n\t"
@@ -112,16 +111,15 @@ __device__ __forceinline__ uint32_t umma_k64_x2_poll(uint32_t d0, uint32_t d1, u
       "add.s64 x0, %3, 6;\n\tadd.s64 x1, %4, 6;\n\tadd.s64 xb, %5, 6;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %6, pt;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%2], x1, xb, %6, pt;\n\t"
-      "selp.u32 %0, 1, 0, q0;\n\t"
-      "@q1 or.b32 %0, %0, 2;\n\t}"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
       : "=r"(r)
-      : "r"(d0), "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(idesc), "r"(accumulate), "r"(nbar0), "r"(npar0),
-        "r"(nbar1), "r"(npar1)
+      : "r"(d0), "r"(d1), "l"(a0), "l"(a1), "l"(b), "r"(idesc), "r"(accumulate), "r"(nbar), "r"(npar)
       : "memory");
   return r;
 }
 
-// One K step of 64 into one accumulator.
+// One K step of 64 into one accumulator; two barriers (weights, activations) cover the
+// next step's operands: bit 0 / bit 1 of the result.
 __device__ __forceinline__ uint32_t umma_k64_poll(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                                   uint32_t accumulate, uint32_t nbar0, uint32_t npar0,
                                                   uint32_t nbar1, uint32_t npar1) {
@@ -149,7 +147,8 @@ __device__ __forceinline__ uint32_t umma_k64_poll(uint32_t d, uint64_t a, uint64
 
 // Pipeline tracing (MOE_PIPE_PROF=1 on the host): a role adds the clock cycles it spends
 // in each barrier wait, and its whole running time, to per-kernel counters.
-//   slot 0..2  MMA issuer: waiting for the accumulator to drain / dequant / TMA; 3 total
+//   slot 0..2  MMA issuer: waiting for the accumulator to drain / dequant / TMA (gate/up:
+//              slot 1 = both operands, slot 2 unused); 3 total
 //   slot 4, 5  TMA producer: waiting for a free stage; total
 //   slot 6, 7  one dequant thread: waiting for the TMA; total
 //   slot 8, 9  one epilogue thread: waiting for the accumulator; total

@@ -5,7 +5,8 @@
 // "Perplexity opened the Lily engine", section "Where the speed-up comes from").
 //
 //   router_prefill_kernel  logits = x W_r^T on tcgen05 (bf16 in, fp32 accumulate in
-//                          TMEM); per token: top-8 by logit with lowest-index ties,
+//                          TMEM); per token: top-8 by logit with lowest-index ties (four
+//                          warps per token quarter, each over 64 experts, then a merge),
 //                          weights exp(l_k - l_1) / sum (equal to softmax over all 256
 //                          followed by renormalisation over the 8), and a per-CTA
 //                          expert histogram.
@@ -33,6 +34,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   int* hist_s = reinterpret_cast<int*>(tmem_slot + 4);
   float* bias_s = reinterpret_cast<float*>(hist_s + NEXP);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bias_s + NEXP);
+  // top-8 lists of expert segments 1-3: values [seg-1][k][row], then expert ids
+  float* cand_v = reinterpret_cast<float*>(smem + RT_STAGES * RT_STAGE_BYTES + 3072);
+  int* cand_e = reinterpret_cast<int*>(cand_v + (RT_SEGS - 1) * TOPK * RT_BM);
+  static_assert(RT_STAGES * RT_STAGE_BYTES + 3072 + RT_CAND_BYTES + 1024 <= RT_SMEM, "router shared memory");
+  static_assert(NEXP == RT_SEGS * 64 && RT_THREADS == RT_SEGS * RT_BM, "one warp per (token quarter, segment)");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * RT_BM;
@@ -104,39 +110,58 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
   __syncwarp();
 
-  // ---- epilogue: thread = token row (TMEM lane), all four warps
+  // ---- epilogue: warp w reads TMEM lane quarter w % 4 (32 token rows) and the 64
+  // expert columns of segment w / 4 and keeps its top 8; the segment-0 warps then take
+  // the other segments' lists in segment order.  Insertion is strictly-greater and the
+  // candidates of equal logit arrive in ascending expert order, so ties go to the lowest
+  // index exactly as in one pass over all 256 experts.
   bool ok = mbar_wait(done, 0, p.err, abort_flag);
-  ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
+  ok = __syncthreads_and(ok && !*abort_flag) != 0;   // the merge reads every warp's list
   tc_fence_after();
-  const int t = m0 + tid;
-  if (ok) {
-    float tv[TOPK];
-    int ti[TOPK];
+  const int seg = warp >> 2, row = (warp & 3) * 32 + lane;
+  const int t = m0 + row;
+  float tv[TOPK];
+  int ti[TOPK];
 #pragma unroll
-    for (int k = 0; k < TOPK; ++k) { tv[k] = -INFINITY; ti[k] = NEXP; }
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-    for (int c = 0; c < NEXP / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(lane_base + c * 32, r);
-      tmem_ld_wait();
+  for (int k = 0; k < TOPK; ++k) { tv[k] = -INFINITY; ti[k] = NEXP; }
+  auto insert = [&](float v, int e) {
+    if (v > tv[TOPK - 1]) {          // strictly greater: equal logits keep the lower index
+      tv[TOPK - 1] = v;
+      ti[TOPK - 1] = e;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = c * 32 + j;
-        const float v = __uint_as_float(r[j]) + bias_s[e];
-        if (v > tv[TOPK - 1]) {          // strictly greater: equal logits keep the lower index
-          tv[TOPK - 1] = v;
-          ti[TOPK - 1] = e;
-#pragma unroll
-          for (int k = TOPK - 1; k > 0; --k) {
-            if (tv[k] > tv[k - 1]) {
-              const float fv = tv[k]; tv[k] = tv[k - 1]; tv[k - 1] = fv;
-              const int iv = ti[k]; ti[k] = ti[k - 1]; ti[k - 1] = iv;
-            }
-          }
+      for (int k = TOPK - 1; k > 0; --k) {
+        if (tv[k] > tv[k - 1]) {
+          const float fv = tv[k]; tv[k] = tv[k - 1]; tv[k - 1] = fv;
+          const int iv = ti[k]; ti[k] = ti[k - 1]; ti[k - 1] = iv;
         }
       }
     }
+  };
+  if (ok) {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      const int col = seg * 64 + c * 32;
+      uint32_t r[32];
+      tmem_ld32(lane_base + col, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) insert(__uint_as_float(r[j]) + bias_s[col + j], col + j);
+    }
+    if (seg > 0) {
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) {
+        cand_v[((seg - 1) * TOPK + k) * RT_BM + row] = tv[k];
+        cand_e[((seg - 1) * TOPK + k) * RT_BM + row] = ti[k];
+      }
+    }
+  }
+  __syncthreads();
+  if (ok && seg == 0) {
+#pragma unroll 1
+    for (int sg = 0; sg < RT_SEGS - 1; ++sg)
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) insert(cand_v[(sg * TOPK + k) * RT_BM + row], cand_e[(sg * TOPK + k) * RT_BM + row]);
     if (t < p.T) {
       // fewer than 8 ordered logits (NaN input): record it and route to expert 0
       if (ti[TOPK - 1] >= NEXP) {

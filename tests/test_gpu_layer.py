@@ -2,8 +2,8 @@
 
 Workloads are the seeded synthetic layer at its real shapes: T=32 (the reference
 configuration), T=1 and 8 (decode), T=512 uniform, T=4096 with the skewed log-Zipf
-router bias, a sweep of ragged T, all tokens forced onto one expert set, in-place
-residual, determinism, a short stack, and argument errors.  The rules are in
+router bias, a sweep of ragged T, all tokens forced onto one expert set, exact routing
+ties, in-place residual, determinism, a short stack, and argument errors.  The rules are in
 tests/parity.py.
 """
 from __future__ import annotations
@@ -131,6 +131,22 @@ def test_all_tokens_on_one_expert_set(oracle, lib):
     rng = np.random.default_rng(600)
     sample = np.unique(np.concatenate([rng.choice(600, 60, replace=False), np.arange(590, 600)]))
     check_output(oracle, L, x, out, tokens=sample, alt=alt)
+
+
+@pytest.mark.parametrize("T", [1, 8, 40])
+def test_exact_ties_lowest_index(oracle, lib, T):
+    """Every router logit equal (zero router matrix, no bias): each token takes experts
+    0..7, each with weight exactly 1/8, on the decode path (T <= 8) and the prefill path;
+    the output follows the oracle, which breaks the tie the same way."""
+    L = synth.make_layer(11)
+    L.router_w = np.zeros_like(L.router_w)
+    layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=64)
+    x = synth.make_x(11, T)
+    out, r = run(layer, x)
+    assert (r["idx"] == np.arange(8)[None, :]).all()
+    assert (r["w"] == np.float32(0.125)).all()
+    assert (r["counts"][:8] == T).all() and (r["counts"][8:256] == 0).all()
+    check_output(oracle, L, x, out)
 
 
 @pytest.mark.parametrize("T", [5, 40])
