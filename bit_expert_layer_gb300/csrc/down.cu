@@ -55,12 +55,11 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
   uint8_t* stg = misc + 1024;                                     // [4 warps][DN_STG_BUFS][32][32] bf16
-  int* s_tiles = reinterpret_cast<int*>(stg + DN_STG_BYTES);
-  int* s_off = s_tiles + (NEXP + 2);
+  int* s_off = reinterpret_cast<int*>(stg + DN_STG_BYTES);   // row tables (GX_TAB_BYTES reserved)
   int* s_cnt = s_off + (NEXP + 2);
   constexpr int SCHED_OFF = (1024 + DN_STG_BYTES + GX_TAB_BYTES + 15) / 16 * 16;
   int4* sched = reinterpret_cast<int4*>(misc + SCHED_OFF);   // [DN_SCHED_CAP] this CTA's tiles
-  stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
+  stage_tables(s_off, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -105,7 +104,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ntiles = build_schedule(sched, DN_SCHED_CAP, s_tiles, s_off, s_cnt, DN_MBLK, p.T, p.err);
+  const int ntiles = build_schedule(sched, DN_SCHED_CAP, p.blocks, s_off, s_cnt, DN_MBLK, p.T, p.err);
   __syncthreads();
   constexpr int NKB = INTER / 64;   // 8
 

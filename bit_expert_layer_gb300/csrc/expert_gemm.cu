@@ -70,13 +70,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                   // 32 barriers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
-  int* s_tiles = reinterpret_cast<int*>(misc + 512);
-  int* s_off = s_tiles + (NEXP + 2);
+  int* s_off = reinterpret_cast<int*>(misc + 512);   // row tables (GX_TAB_BYTES reserved)
   int* s_cnt = s_off + (NEXP + 2);
   int* s_tok = reinterpret_cast<int*>(misc + 512 + GX_TAB_BYTES);   // [GU_GW][GU_GROWS] token ids
   int4* sched = reinterpret_cast<int4*>(s_tok + GU_GW * GU_GROWS);   // [GU_SCHED_CAP] this CTA's tiles
   uint8_t* stg = misc + STG_OFF;                                       // [4 warps][GU_STG_BUFS][32][32] bf16
-  stage_tables(s_tiles, p.tiles, p.offsets, p.counts);
+  stage_tables(s_off, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -118,7 +117,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ntiles = build_schedule(sched, GU_SCHED_CAP, s_tiles, s_off, s_cnt, GU_MBLK, p.T, p.err);
+  const int ntiles = build_schedule(sched, GU_SCHED_CAP, p.blocks, s_off, s_cnt, GU_MBLK, p.T, p.err);
   __syncthreads();
   constexpr int NKB = HID / 64;
   const bool pp = p.pipe != nullptr;

@@ -1,5 +1,5 @@
 // gemm_common.cuh -- helpers shared by the grouped expert GEMM kernels (gate/up and
-// down): the device-side tile lookup, staging of the tile tables in shared memory,
+// down): the device-side tile schedule, staging of the row tables in shared memory,
 // bf16 pair construction, bounded teardown waits and the pipeline-trace counters.
 #pragma once
 
@@ -12,43 +12,49 @@ struct TileInfo {
   bool ok;   // tables consistent: every role skips a bad tile the same way
 };
 
-__device__ __forceinline__ TileInfo tile_info(const int* tiles, const int* offsets, const int* counts, int tile,
+// Tile `tile` = token block tile / mblk of the ordered list built by route_scan_kernel
+// (entry: expert | (block index << 9)) x weight row block tile % mblk.  The offsets and
+// counts live in shared memory (stage_tables).
+__device__ __forceinline__ TileInfo tile_info(const int* blocks, const int* offsets, const int* counts, int tile,
                                               int mblk, int T) {
-  // the tables live in shared memory (stage_tables): a binary search over global memory
-  // would be nine dependent L2 round trips per tile and role
-  int lo = 0, hi = NEXP;   // largest e in [0, 256] with tiles[e] <= tile
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tiles[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
+  const int j = tile / mblk;
+  const int v = __ldg(blocks + 1 + j);
   TileInfo ti;
-  ti.e = lo;
-  const int local = tile - tiles[lo];
-  const int nb = local / mblk;
-  ti.mb = local - nb * mblk;
-  ti.row0 = offsets[lo] + nb * GX_BN;
-  ti.n_rows = min(GX_BN, counts[lo] - nb * GX_BN);
-  ti.ok = ti.n_rows >= 1 && ti.row0 >= 0 && ti.row0 + ti.n_rows <= 9 * T && local >= 0;
+  ti.e = v & 511;
+  ti.mb = tile - j * mblk;
+  const int nb = v >> 9;
+  const int e = ti.e <= NEXP ? ti.e : 0;
+  ti.row0 = offsets[e] + nb * GX_BN;
+  ti.n_rows = min(GX_BN, counts[e] - nb * GX_BN);
+  ti.ok = ti.e <= NEXP && nb >= 0 && ti.n_rows >= 1 && ti.row0 >= 0 && ti.row0 + ti.n_rows <= 9 * T;
   return ti;
 }
 
-// This CTA's share of a grouped GEMM's tiles (tile blockIdx.x + i gridDim.x, i = 0, 1,
-// ...), decoded from the staged tables once at kernel start, one thread per tile, so that
-// no role repeats the binary search per tile: its nine dependent shared-memory loads
-// queue behind the rings' traffic and cost the MMA issuer ~3500 cycles per tile.  A
-// record is {expert, row block, first row, rows}; rows = 0 marks a tile whose tables are
-// inconsistent, which every role skips.  More tiles than `cap` is a bounds error (the
-// host sizes the grid so that it cannot happen).  Returns the number of records.
-__device__ __forceinline__ int build_schedule(int4* sched, int cap, const int* s_tiles, const int* s_off,
+// This CTA's share of a grouped GEMM's tiles, decoded once at kernel start, one thread
+// per tile, into a shared-memory schedule that every role reads.  The tiles are dealt in
+// snake order: round i gives CTA b tile i G + b for even i and i G + G - 1 - b for odd i,
+// so that with the token blocks ordered by size (full blocks first, then the partial
+// ones largest first) each CTA's sum of tile sizes evens out and the last, incomplete
+// round holds the smallest tiles.  A record is {expert, row block, first row, rows};
+// rows = 0 marks a tile whose tables are inconsistent, which every role skips.  More
+// tiles than `cap` is a bounds error (the host sizes the grid so that it cannot
+// happen).  Returns the number of records.
+__device__ __forceinline__ int build_schedule(int4* sched, int cap, const int* blocks, const int* s_off,
                                               const int* s_cnt, int mblk, int T, unsigned int* err) {
-  const int total = s_tiles[NEXP + 1];
+  int nblocks = __ldg(blocks);
+  // at most ceil(8T / 256) + min(8T, 256) routed blocks and ceil(T / 256) shared ones
+  if (nblocks < 0 || nblocks > (8 * T + GX_BN - 1) / GX_BN + min(8 * T, NEXP) + (T + GX_BN - 1) / GX_BN) {
+    if (threadIdx.x == 0) atomicOr(err, ERRBIT_BOUNDS);
+    nblocks = 0;
+  }
+  const int total = nblocks * mblk;
   const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
-  const int n = total > b ? (total - b + g - 1) / g : 0;
+  const int rounds = total / g, rem = total - rounds * g;
+  const int n = rounds + (((rounds & 1) ? g - 1 - b : b) < rem ? 1 : 0);
   if (n > cap && threadIdx.x == 0) atomicOr(err, ERRBIT_BOUNDS);
   const int m = min(n, cap);
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
-    const TileInfo ti = tile_info(s_tiles, s_off, s_cnt, b + i * g, mblk, T);
+    const TileInfo ti = tile_info(blocks, s_off, s_cnt, i * g + ((i & 1) ? g - 1 - b : b), mblk, T);
     sched[i] = ti.ok ? make_int4(ti.e, ti.mb, ti.row0, ti.n_rows) : make_int4(0, 0, 0, 0);
   }
   return m;
@@ -65,12 +71,11 @@ __device__ __forceinline__ TileInfo sched_tile(const int4* sched, int i) {
   return ti;
 }
 
-// Copy the tile prefix [258], row offsets [258] and row counts [257] into shared memory.
-__device__ __forceinline__ void stage_tables(int* s, const int* tiles, const int* offsets, const int* counts) {
+// Copy the row offsets [258] and row counts [257] into shared memory: s[0..257], s[258..].
+__device__ __forceinline__ void stage_tables(int* s, const int* offsets, const int* counts) {
   for (int i = threadIdx.x; i < NEXP + 2; i += blockDim.x) {
-    s[i] = __ldg(tiles + i);
-    s[(NEXP + 2) + i] = __ldg(offsets + i);
-    s[2 * (NEXP + 2) + i] = (i <= NEXP) ? __ldg(counts + i) : 0;
+    s[i] = __ldg(offsets + i);
+    s[(NEXP + 2) + i] = (i <= NEXP) ? __ldg(counts + i) : 0;
   }
 }
 

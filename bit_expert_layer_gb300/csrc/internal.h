@@ -26,8 +26,7 @@ struct ScanParams {
   int* base;          // [nblk][256] first permuted row of (block, expert)
   int* counts;        // [257]: 256 experts + shared (= T)
   int* offsets;       // [258]: exclusive scan; [256] = 8T, [257] = 9T
-  int* tiles_gu;      // [258]: prefix of gate/up tiles per expert (shared = 256), [257] = total
-  int* tiles_dn;      // [258]: same for the down GEMM
+  int* blocks;        // [0] = number of token blocks, then the blocks (see route_scan_kernel)
 };
 
 struct ScatterParams {
@@ -47,7 +46,7 @@ struct ScatterParams {
 };
 
 struct GateUpParams {
-  const int* tiles;      // [258]
+  const int* blocks;     // token blocks: [0] = count, then expert | (block << 9)
   const int* offsets;    // [258]
   const int* counts;     // [257]
   const uint16_t* g_scales; const uint16_t* g_biases;    // [256][512][32]
@@ -63,7 +62,7 @@ struct GateUpParams {
 };
 
 struct DownParams {
-  const int* tiles;      // [258]
+  const int* blocks;     // token blocks: [0] = count, then expert | (block << 9)
   const int* offsets;
   const int* counts;
   const uint16_t* d_scales; const uint16_t* d_biases;    // [256][2048][8]

@@ -35,7 +35,7 @@ struct moe_layer {
   // workspace segments
   unsigned int* err;
   unsigned int* dec_counter;
-  int *hist, *base, *counts, *offsets, *tiles_gu, *tiles_dn;
+  int *hist, *base, *counts, *offsets, *blocks;
   int* topk_idx;
   float* topk_w;
   int* row_dst;
@@ -193,8 +193,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->base = c.take<int>(nblk * NEXP * 4);
   d->counts = c.take<int>((NEXP + 1) * 4);
   d->offsets = c.take<int>((NEXP + 2) * 4);
-  d->tiles_gu = c.take<int>((NEXP + 2) * 4);
-  d->tiles_dn = c.take<int>((NEXP + 2) * 4);
+  d->blocks = c.take<int>((gemm_tiles_bound(Tm, 1) + 1) * 4);
   d->topk_idx = c.take<int>(static_cast<size_t>(Tm) * TOPK * 4);
   d->topk_w = c.take<float>(static_cast<size_t>(Tm) * TOPK * 4);
   d->row_dst = c.take<int>(rows * 4);
@@ -292,7 +291,7 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   if (!encode_bf16_rows(&tm_x, x, HID, T, RT_BM)) return MOE_ERR_CUDA;
   RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist, L->err};
   MOE_TRY(timed(K_ROUTER, s, L->err, [&] { return launch_router_prefill(tm_x, L->tm_wr, rp, s); }), "router launch");
-  ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->tiles_gu, L->tiles_dn};
+  ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->blocks};
   MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
   ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->slot_row, L->row_w,
                     static_cast<const __nv_bfloat16*>(x),
@@ -421,7 +420,7 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   if (st != MOE_OK) return st;
   auto U16 = [](const void* p) { return static_cast<const uint16_t*>(p); };
   const moe_weights_t& w = L->w;
-  GateUpParams gp{L->tiles_gu, L->offsets, L->counts,
+  GateUpParams gp{L->blocks, L->offsets, L->counts,
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
                   L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst};
@@ -429,7 +428,7 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   MOE_TRY(timed(K_GATEUP, s, L->err,
                 [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
           "gate/up launch");
-  DownParams dp{L->tiles_dn, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
+  DownParams dp{L->blocks, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
                 pipe_trace() ? L->pipe + 16 : nullptr};
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");

@@ -12,7 +12,7 @@
 //                          expert histogram.
 //   route_scan_kernel      per-expert counts, exclusive-scan offsets, the first
 //                          permuted row of every (router block, expert), and the
-//                          tile tables of both grouped GEMMs.
+//                          ordered token blocks that both grouped GEMMs deal as tiles.
 //   route_scatter_kernel   stable permutation of the slots t*8+k into expert order and
 //                          the per-row weight (first CTA of each router block), one
 //                          K-interleaved copy of x per token (the gate/up GEMM gathers
@@ -198,78 +198,104 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
 }
 
-__global__ void __launch_bounds__(256) route_scan_kernel(ScanParams p) {
+// 1024 threads: thread (q, e) = expert e's router blocks of quarter q (the per-expert
+// sums and prefixes over the blocks run four ways in parallel); the per-expert steps
+// below run on the q = 0 threads, every thread reaching the barriers.
+constexpr int SCAN_Q = 4;
+__global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p) {
   __shared__ int sc[NEXP];
-  __shared__ int s_tot[2];
-  const int e = threadIdx.x;
-  constexpr int CH = 16;   // histogram entries loaded together (independent loads in flight)
-  int c = 0;
-  for (int b0 = 0; b0 < p.nblk; b0 += CH) {
+  __shared__ int s_seg[SCAN_Q][NEXP];
+  const int e = threadIdx.x % NEXP, q = threadIdx.x / NEXP;
+  const bool lead = q == 0;
+  const int per_q = (p.nblk + SCAN_Q - 1) / SCAN_Q;
+  const int b_lo = q * per_q, b_hi = min(p.nblk, b_lo + per_q);
+  constexpr int CH = 8;   // histogram entries loaded together (independent loads in flight)
+  int cq = 0;
+  for (int b0 = b_lo; b0 < b_hi; b0 += CH) {
     int h[CH];
 #pragma unroll
-    for (int i = 0; i < CH; ++i) h[i] = (b0 + i < p.nblk) ? __ldg(p.hist + (b0 + i) * NEXP + e) : 0;
+    for (int i = 0; i < CH; ++i) h[i] = (b0 + i < b_hi) ? __ldg(p.hist + (b0 + i) * NEXP + e) : 0;
 #pragma unroll
-    for (int i = 0; i < CH; ++i) c += h[i];
+    for (int i = 0; i < CH; ++i) cq += h[i];
+  }
+  s_seg[q][e] = cq;
+  __syncthreads();
+  int c = 0, pre = 0;   // expert e's count; the count of its blocks before quarter q
+#pragma unroll
+  for (int j = 0; j < SCAN_Q; ++j) {
+    pre += (j < q) ? s_seg[j][e] : 0;
+    c += s_seg[j][e];
   }
   // block-wide inclusive scan (Hillis-Steele) of the counts
-  sc[e] = c;
+  if (lead) sc[e] = c;
   __syncthreads();
   for (int off = 1; off < NEXP; off <<= 1) {
-    const int v = (e >= off) ? sc[e - off] : 0;
+    const int v = (lead && e >= off) ? sc[e - off] : 0;
     __syncthreads();
-    sc[e] += v;
+    if (lead) sc[e] += v;
     __syncthreads();
   }
   const int excl = sc[e] - c;
   // first permuted row of (block, expert): the expert's offset plus earlier blocks' counts
-  int run = excl;
-  for (int b0 = 0; b0 < p.nblk; b0 += CH) {
+  int run = excl + pre;
+  for (int b0 = b_lo; b0 < b_hi; b0 += CH) {
     int h[CH];
 #pragma unroll
-    for (int i = 0; i < CH; ++i) h[i] = (b0 + i < p.nblk) ? __ldg(p.hist + (b0 + i) * NEXP + e) : 0;
+    for (int i = 0; i < CH; ++i) h[i] = (b0 + i < b_hi) ? __ldg(p.hist + (b0 + i) * NEXP + e) : 0;
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
-      if (b0 + i < p.nblk) p.base[(b0 + i) * NEXP + e] = run;
+      if (b0 + i < b_hi) p.base[(b0 + i) * NEXP + e] = run;
       run += h[i];
     }
   }
-  p.counts[e] = c;
-  p.offsets[e] = excl;
-  __syncthreads();
-  // tiles per expert: ceil(count / 256) token blocks x row blocks
-  const int nblk_tok = (c + GX_BN - 1) / GX_BN;
-  const int tg = nblk_tok * GU_MBLK, td = nblk_tok * DN_MBLK;
-  sc[e] = tg;
+  if (lead) {
+    p.counts[e] = c;
+    p.offsets[e] = excl;
+  }
+  __syncthreads();   // every thread has read sc
+  // Token blocks of the grouped GEMMs (a block = up to 256 consecutive permuted rows of
+  // one expert; every tile is a block x one row block of the weights): all full blocks
+  // first (expert order, the shared expert last), then each expert's partial last block,
+  // largest first (ties: lower expert first).  The GEMMs deal their tiles in this order,
+  // so the smallest tiles are the last ones dealt and the CTAs' loads even out.  Entry:
+  // expert | (block index << 9).
+  __shared__ int s_part[NEXP + 1];
+  const int full = c / GX_BN, part = c % GX_BN;
+  if (lead) s_part[e] = part;
+  if (threadIdx.x == 0) s_part[NEXP] = p.T % GX_BN;
+  if (lead) sc[e] = full;
   __syncthreads();
   for (int off = 1; off < NEXP; off <<= 1) {
-    const int v = (e >= off) ? sc[e - off] : 0;
+    const int v = (lead && e >= off) ? sc[e - off] : 0;
     __syncthreads();
-    sc[e] += v;
-    __syncthreads();
-  }
-  p.tiles_gu[e] = sc[e] - tg;
-  if (e == NEXP - 1) s_tot[0] = sc[e];
-  __syncthreads();
-  sc[e] = td;
-  __syncthreads();
-  for (int off = 1; off < NEXP; off <<= 1) {
-    const int v = (e >= off) ? sc[e - off] : 0;
-    __syncthreads();
-    sc[e] += v;
+    if (lead) sc[e] += v;
     __syncthreads();
   }
-  p.tiles_dn[e] = sc[e] - td;
-  if (e == NEXP - 1) s_tot[1] = sc[e];
-  __syncthreads();
-  if (e == 0) {
-    const int sh_blk = (p.T + GX_BN - 1) / GX_BN;
+  const int full_routed = sc[NEXP - 1], full_sh = p.T / GX_BN;
+  const int n_full = full_routed + full_sh;
+  int* blk = p.blocks + 1;
+  if (lead)
+    for (int k = 0; k < full; ++k) blk[sc[e] - full + k] = e | (k << 9);
+  for (int k = threadIdx.x; k < full_sh; k += blockDim.x) blk[full_routed + k] = NEXP | (k << 9);
+  // rank of a partial block among all partial blocks (four independent counts in flight)
+  auto prank = [&](int x) {
+    const int px = s_part[x];
+    int r[4] = {0, 0, 0, 0};
+#pragma unroll 4
+    for (int y = 0; y < NEXP; ++y) {
+      const int py = s_part[y];
+      r[y & 3] += (py > px) || (py == px && y < x);
+    }
+    return r[0] + r[1] + r[2] + r[3] + (s_part[NEXP] > px);   // the shared expert sorts last among equals
+  };
+  if (lead && part > 0) blk[n_full + prank(e)] = e | (full << 9);
+  if (threadIdx.x == NEXP && s_part[NEXP] > 0) blk[n_full + prank(NEXP)] = NEXP | (full_sh << 9);
+  const int np = __syncthreads_count(lead && part > 0) + (s_part[NEXP] > 0);
+  if (threadIdx.x == 0) {
     p.counts[NEXP] = p.T;
     p.offsets[NEXP] = 8 * p.T;
     p.offsets[NEXP + 1] = 9 * p.T;
-    p.tiles_gu[NEXP] = s_tot[0];
-    p.tiles_gu[NEXP + 1] = s_tot[0] + sh_blk * GU_MBLK;
-    p.tiles_dn[NEXP] = s_tot[1];
-    p.tiles_dn[NEXP + 1] = s_tot[1] + sh_blk * DN_MBLK;
+    p.blocks[0] = n_full + np;
   }
 }
 
@@ -404,7 +430,7 @@ cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm
 }
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
-  route_scan_kernel<<<1, NEXP, 0, s>>>(p);
+  route_scan_kernel<<<1, SCAN_Q * NEXP, 0, s>>>(p);
   return cudaGetLastError();
 }
 
