@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ntiles = build_schedule(sched, DN_SCHED_CAP, p.blocks, s_off, s_cnt, DN_MBLK, p.T, p.err);
+  const int ntiles = build_schedule(sched, DN_SCHED_CAP, p.blocks, s_off, s_cnt, DN_MBLK, p.T, p.err, false);
   __syncthreads();
   constexpr int NKB = INTER / 64;   // 8
 
