@@ -15,8 +15,9 @@ with CUDA events on the launching stream, inputs resident in HBM, max over ranks
 The weights read per step (18.2 GB) are far larger than L2, so no L2 flush is needed.
 ``e2e`` is the same metric through the C entry ``moe_stack_forward_host`` with the
 input copied from pinned host memory and the output copied back inside the timed
-region.  ``roofline`` is for the dominant kernel (the grouped gate/up GEMM), timed live
-by the library's event profiler during the timed steps.  ``cpu_baseline`` times the
+region.  ``roofline`` is for the dominant kernel (the grouped gate/up GEMM; on the
+decode-only workloads the fused decode kernel against HBM), timed live by the library's
+event profiler during the timed steps.  ``cpu_baseline`` times the
 CPU oracle on a bounded sample.  With N>1 (torchrun) every rank runs an independent
 replica on its own GPU (weak scaling, no collective on the data path).
 
@@ -46,6 +47,8 @@ UNIT = "layer-tokens/s"
 FLOP_PER_TOKEN = 57_675_776          # per layer: 8 routed + 1 shared SwiGLU expert, router, shared gate
 GATEUP_FLOP_PER_ROW = 2 * 2 * 512 * 2048
 LAYER_BYTES = 455_806_976
+EXPERT_BYTES = 1_769_472              # one expert: 3 packed 4-bit matrices + scales + biases
+ROUTER_BYTES = 1_048_576 + 4_096      # router matrix + shared-expert gate vector
 
 WORKLOADS = {
     "stack40-T16384+T1": dict(layers=40, T_prefill=16384, T_decode=1, skew=False),
@@ -385,7 +388,26 @@ def run_ours(args, wl):
     dec = None
     if Td:
         dms = part_ms["decode"] / args.steps
-        dec = dict(us_per_layer=1e3 * dms / n_layers, us_per_stack=1e3 * dms)
+        # algorithmic HBM bytes of one decode pass: per layer the touched experts (counted
+        # from the routing of that layer's actual input; the shared expert included), the
+        # router matrix and the shared gate
+        x = xd_src.clone()
+        dbytes = 0
+        for L in layers:
+            n_e = int(torch.unique(L.route(x)["idx"]).numel())
+            dbytes += (n_e + 1) * EXPERT_BYTES + ROUTER_BYTES
+            if resid:
+                x = L.forward(x, residual=True)
+        torch.cuda.synchronize(dev)
+        gbs = dbytes / (dms / 1e3) / 1e9
+        dec = dict(us_per_layer=1e3 * dms / n_layers, us_per_stack=1e3 * dms,
+                   hbm_bytes_per_pass=dbytes, hbm_gbs=gbs, hbm_frac=gbs / peaks["hbm"])
+        if roof is None:
+            roof = dict(kernel="decode_layers", bound="hbm", achieved=gbs, peak=peaks["hbm"], unit="GB/s",
+                        frac=gbs / peaks["hbm"], traffic=None,
+                        algorithmic=f"touched experts x {EXPERT_BYTES} B + {ROUTER_BYTES} B per layer, "
+                                    f"{dbytes} B per pass of {n_layers} layer(s), T={Td}",
+                        peak_source=f"{peaks['src']} HBM copy")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
