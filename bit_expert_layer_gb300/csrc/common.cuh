@@ -67,6 +67,9 @@ constexpr int GU_STG_BYTES = 4 * GU_STG_BUFS * 32 * 32 * 2;
 constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + 128 + GU_STG_BYTES;
 constexpr int GU_THREADS = (14 + GU_GW) * 32;   // packed producer, MMA, 8 dequant, 4 epilogue, gather warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
+// gate/up tiles of at most this many tokens run with the operands swapped: tokens on the
+// MMA's M side (128, padded), the tile's 128 gate and 128 up weight rows on its N side
+constexpr int GU_SWAP_ROWS = 128;
 // down: one A tile + X + one packed tile per stage; double-buffered accumulator
 // down: rings of packed tiles (4 KB), activation tiles (32 KB) and dequantised tiles (16 KB)
 constexpr int DN_NP = 8;

@@ -174,7 +174,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           const TileInfo ti = sched_tile(sched, tix);
           if (!ti.ok) continue;
           const int N = max(16, (ti.n_rows + 15) & ~15);
-          const uint32_t idesc = idesc_bf16(128, N);
+          // a tile of at most GU_SWAP_ROWS tokens: one M = 128 (tokens) x N = 256 (gate and
+          // up rows) MMA per K slice instead of a gate and an up MMA of N tokens each
+          const bool swp = ti.n_rows <= GU_SWAP_ROWS;
+          const uint32_t idesc = swp ? idesc_bf16(128, 2 * GX_BM) : idesc_bf16(128, N);
           if (!mbar_wait_t(ACCE, (tc & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
           tc_fence_after();
           bool alive = true;
@@ -190,8 +193,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             const uint32_t x = smem_u32(smem + OFF_X + sx * GX_X_BYTES);
             // gate and up MMAs of this K step; the next step's stages are polled meanwhile
             const uint32_t nx = it + 1;
-            rdy = umma_k64_x2_poll(tmem, tmem + 256, sdesc_sw128(a), sdesc_sw128(a + GX_A_BYTES), sdesc_sw128(x),
-                                   idesc, kb != 0, READY(nx % GU_NR), (nx / GU_NR) & 1);
+            if (swp)
+              rdy = umma_k64_poll1(tmem, sdesc_sw128(x), sdesc_sw128(a), idesc, kb != 0, READY(nx % GU_NR),
+                                   (nx / GU_NR) & 1);
+            else
+              rdy = umma_k64_x2_poll(tmem, tmem + 256, sdesc_sw128(a), sdesc_sw128(a + GX_A_BYTES), sdesc_sw128(x),
+                                     idesc, kb != 0, READY(nx % GU_NR), (nx / GU_NR) & 1);
             umma_commit(AEMPTY(sa));
             umma_commit(XEMPTY(sx));
           }
@@ -348,6 +355,43 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      if (ti.n_rows <= GU_SWAP_ROWS) {
+        // swapped tile: TMEM lane = the tile's row 32q + lane (a token), columns 0-127 the
+        // gate and 128-255 the up outputs of the tile's 128 h columns, in h column order
+        // (the dequant permuted the weight rows); each thread writes its row's 256 bytes
+        const int row = 32 * q + lane;
+        __nv_bfloat16* hrow = p.h + static_cast<size_t>(ti.row0 + row) * INTER + ti.mb * GX_BM;
+#pragma unroll 1
+        for (int c0 = 0; c0 < GX_BM; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(tl + c0, g);
+          tmem_ld16(tl + GX_BM + c0, u);
+          tmem_ld_wait();
+          if (c0 + 16 == GX_BM) {   // last read: the MMA may overwrite the accumulator
+            tc_fence_before();
+            mbar_arrive(ACCE);
+          }
+          uint32_t w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float hv[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float hg = 0.5f * __uint_as_float(g[2 * k + i]);
+              float th;
+              asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hg));
+              hv[i] = fmaf(hg, th, hg) * __uint_as_float(u[2 * k + i]);
+            }
+            w[k] = pack_bf16x2(__float_as_uint(hv[0]), __float_as_uint(hv[1]));
+          }
+          if (row < ti.n_rows) {
+            *reinterpret_cast<uint4*>(hrow + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(hrow + c0 + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        }
+        ++tc;
+        continue;
+      }
       const int hcol = ti.mb * GX_BM + q * 32;   // h column of this warp's first lane
       // One 32-row chunk: gate and up read as 16-lane fragments (lanes 0-15, then 16-31
       // of this warp), SwiGLU, rounded to bf16 pairs (rows j, j+1) and

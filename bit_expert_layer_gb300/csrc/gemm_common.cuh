@@ -125,6 +125,29 @@ __device__ __forceinline__ uint32_t umma_k64_x2_poll(uint32_t d0, uint32_t d1, u
   return r;
 }
 
+// One K step of 64 into one accumulator; one barrier covers both operands of the next step.
+__device__ __forceinline__ uint32_t umma_k64_poll1(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                   uint32_t accumulate, uint32_t nbar, uint32_t npar) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pa, pt, q0;\n\t.reg .b64 x0, xb;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%6], %7;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\t"
+      "setp.ne.b32 pt, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pa;\n\t"
+      "add.s64 x0, %2, 2;\n\tadd.s64 xb, %3, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %4, pt;\n\t"
+      "add.s64 x0, %2, 4;\n\tadd.s64 xb, %3, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %4, pt;\n\t"
+      "add.s64 x0, %2, 6;\n\tadd.s64 xb, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], x0, xb, %4, pt;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
+      : "=r"(r)
+      : "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(nbar), "r"(npar)
+      : "memory");
+  return r;
+}
+
 // One K step of 64 into one accumulator; two barriers (weights, activations) cover the
 // next step's operands: bit 0 / bit 1 of the result.
 __device__ __forceinline__ uint32_t umma_k64_poll(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
