@@ -248,7 +248,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         ++it;
         const __nv_bfloat162 ms = bf2((kb & 1) ? (sw[kb >> 1] >> 16) : sw[kb >> 1]);
         const __nv_bfloat162 mbv = bf2((kb & 1) ? (bw[kb >> 1] >> 16) : bw[kb >> 1]);
-        const uint4 w = *reinterpret_cast<const uint4*>(smem + OFF_P + sp * GX_P_BYTES + r * 32 + hw * 16);
+        // this thread's 16-byte half of the row, stored 32-byte swizzled (half c at c ^ bit 2 of the row)
+        const uint4 w = *reinterpret_cast<const uint4*>(smem + OFF_P + sp * GX_P_BYTES + r * 32 +
+                                                        ((hw ^ ((r >> 2) & 1)) << 4));
         // the packed words are in registers; the next TMA write into this stage is an
         // async-proxy access, so the generic reads are fenced before the release
         fence_proxy_async_smem();

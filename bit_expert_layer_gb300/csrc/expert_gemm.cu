@@ -316,8 +316,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           ++it;
           const __nv_bfloat162 ms = bf2((j & 1) ? (sw[j >> 1] >> 16) : sw[j >> 1]);
           const __nv_bfloat162 mbv = bf2((j & 1) ? (bw[j >> 1] >> 16) : bw[j >> 1]);
-          const uint4* P = reinterpret_cast<const uint4*>(smem + OFF_P + sp * GU_P_STAGE + mat * GX_P_BYTES + wr * 32);
-          const uint4 w0 = P[0], w1 = P[1];
+          // the row's two 16-byte halves, stored 32-byte swizzled (half c at c ^ bit 2 of the row)
+          const uint8_t* P = smem + OFF_P + sp * GU_P_STAGE + mat * GX_P_BYTES + wr * 32;
+          const int hs = ((wr >> 2) & 1) << 4;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(P + hs), w1 = *reinterpret_cast<const uint4*>(P + (16 ^ hs));
           // the packed words are in registers; the next TMA write into this stage is an
           // async-proxy access, so the generic reads are fenced before the release
           fence_proxy_async_smem();

@@ -258,9 +258,12 @@ bool encode_bf16_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t 
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Packed 4-bit tiles: 128 rows x 8 words (32 bytes) per box, stored with the 32-byte
+// swizzle (the 16-byte half c of row r lands at c ^ ((r >> 2) & 1)), so that the dequant
+// threads, one or two per row, read their halves without bank conflicts.
 bool encode_packed(CUtensorMap* m, const void* base, uint64_t words, uint64_t rows) {
   return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, words, rows, words * 4, 8, GX_BM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
+                   CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 bool qmat_ok(const moe_qmat_t& q, moe_status_t* st) {
