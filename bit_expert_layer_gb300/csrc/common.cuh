@@ -64,7 +64,7 @@ constexpr int DN_SCHED_CAP = 288;
 // gate/up epilogue staging: per epilogue warp GU_STG_BUFS tiles of 32 rows x 32 features
 constexpr int GU_STG_BUFS = 2;
 constexpr int GU_STG_BYTES = 4 * GU_STG_BUFS * 32 * 32 * 2;
-constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + 128 + GU_STG_BYTES;
+constexpr int GU_SMEM = GU_RINGS + 1024 + 512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + 1024 + GU_STG_BYTES;
 constexpr int GU_THREADS = (14 + GU_GW) * 32;   // packed producer, MMA, 8 dequant, 4 epilogue, gather warps
 constexpr int GU_MBLK = INTER / GX_BM;              // 4 row blocks per matrix
 // gate/up tiles of at most this many tokens run with the operands swapped: tokens on the

@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         // the TMA store issued from this staging tile DN_STG_BUFS stores ago has read it
         if (lane == 0 && nst >= DN_STG_BUFS) tma_store_wait_read<DN_STG_BUFS - 1>();
         __syncwarp();
-        const uint32_t ra = smem_u32(sb) + (lane & 7) * STG_ROW + (lane >> 3) * 16;   // matrix lane/8, row lane%8
+        // matrix lane/8, row lane%8; the staging tile is 64-byte swizzled like the TMA box
+        const uint32_t ra = smem_u32(sb) + (lane & 7) * STG_ROW + ((((lane >> 3) ^ ((lane >> 1) & 3))) << 4);
 #pragma unroll
         for (int g = 0; g < 4; ++g)   // rows 8g..8g+7; matrices = features 0-7, 8-15, 16-23, 24-31
           stmatrix_x4_trans(ra + g * 8 * STG_ROW, pack_bf16x2(fa[4 * g], fa[4 * g + 1]),
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
           __syncwarp();
           for (int item = lane; item < rows * 4; item += 32) {
             const int j = item >> 2, seg = item & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + seg * 16);
+            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + ((seg ^ ((j >> 1) & 3)) << 4));
             *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.row0 + c0 + j) * HID + fcol + seg * 8) = v;
           }
           __syncwarp();                           // this staging tile is free again

@@ -55,9 +55,10 @@ constexpr int STG_ROW = 32 * 2;                      // bytes of one staged row 
 constexpr int STG_BUF = 32 * STG_ROW;                // one 32 x 32 staging tile
 static_assert(4 * GU_STG_BUFS * STG_BUF == GU_STG_BYTES, "staging size");
 static_assert((512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4) % 16 == 0, "schedule alignment");
-// the epilogue's staging tiles are TMA-store sources: 128-byte aligned (misc is 1024-aligned)
-constexpr int STG_OFF = (512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + 127) / 128 * 128;
-static_assert(STG_OFF % 128 == 0 && OFF_MISC % 1024 == 0, "staging alignment");
+// the epilogue's staging tiles are 64-byte-swizzled TMA-store sources: 1024-byte aligned
+// (misc is 1024-aligned)
+constexpr int STG_OFF = (512 + GX_TAB_BYTES + GU_GW * GU_GROWS * 4 + GU_SCHED_CAP * 16 + 1023) / 1024 * 1024;
+static_assert(STG_OFF % 1024 == 0 && OFF_MISC % 1024 == 0 && STG_BUF % 1024 == 0, "staging alignment");
 }  // namespace
 
 __global__ void __launch_bounds__(GU_THREADS, 1)
@@ -435,7 +436,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         // the TMA store issued from this staging tile GU_STG_BUFS stores ago has read it
         if (lane == 0 && nst >= GU_STG_BUFS) tma_store_wait_read<GU_STG_BUFS - 1>();
         __syncwarp();
-        const uint32_t ra = smem_u32(sb) + (lane & 7) * STG_ROW + (lane >> 3) * 16;   // matrix lane/8, row lane%8
+        // matrix lane/8, row lane%8; the staging tile is 64-byte swizzled like the TMA box
+        const uint32_t ra = smem_u32(sb) + (lane & 7) * STG_ROW + ((((lane >> 3) ^ ((lane >> 1) & 3))) << 4);
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg)   // rows 8g..8g+7; matrices = lanes 0-7, 8-15, 16-23, 24-31
           stmatrix_x4_trans(ra + gg * 8 * STG_ROW, m[0][gg][0], m[0][gg][1], m[1][gg][0], m[1][gg][1]);
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           __syncwarp();
           for (int item = lane; item < rows * 4; item += 32) {
             const int j = item >> 2, seg = item & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + seg * 16);
+            const uint4 v = *reinterpret_cast<const uint4*>(sb + j * STG_ROW + ((seg ^ ((j >> 1) & 3)) << 4));
             *reinterpret_cast<uint4*>(p.h + static_cast<size_t>(ti.row0 + col0 + j) * INTER + hcol + seg * 8) = v;
           }
           __syncwarp();   // this staging tile is free again

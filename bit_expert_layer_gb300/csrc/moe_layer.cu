@@ -530,10 +530,13 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
             encode_packed(&L->tm_qd, weights->down.q, INTER / 8, static_cast<uint64_t>(NEXP) * HID) &&
             encode_packed(&L->tm_sqd, weights->sh_down.q, SH_INTER / 8, HID) &&
             encode_bf16_rows(&L->tm_h, L->h, INTER, 9ull * Tm, GX_XBOX) &&
+            // epilogue stores of 32 x 32 bf16 boxes from staging tiles written by stmatrix,
+            // 64-byte swizzled (16-byte chunk c of staged row k at c ^ ((k >> 1) & 3)) so
+            // that stmatrix's eight rows of a matrix fall in different banks
             encode_2d(&L->tm_hs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->h, INTER, 9ull * Tm, INTER * 2, 32, 32,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                      CU_TENSOR_MAP_SWIZZLE_64B) &&
             encode_2d(&L->tm_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, L->y, HID, 9ull * Tm, HID * 2, 32, 32,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+                      CU_TENSOR_MAP_SWIZZLE_64B);
   if (!ok) return fail(MOE_ERR_CUDA);
   *out = L;
   return MOE_OK;
