@@ -100,9 +100,15 @@ def make_hosts(wl):
 
 
 def kernel_hash() -> str:
+    """Hash of the gate/up kernel's source with comments and blank lines removed, so that a
+    stored DRAM-traffic capture stays attached to the code it was taken on."""
+    import re
     h = hashlib.sha256()
     for f in ("expert_gemm.cu", "common.cuh", "gemm_common.cuh"):
-        h.update(open(os.path.join(ROOT, "bit_expert_layer_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "bit_expert_layer_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 
