@@ -18,7 +18,7 @@ constexpr int TOPK = 8;          // experts kept per token
 constexpr int INTER = 512;       // routed expert intermediate size
 constexpr int SH_INTER = 512;    // shared expert intermediate size
 constexpr int GROUP = 64;        // quantisation group along the input dim
-constexpr int SHARED_E = NEXP;   // the shared expert's index in the tile tables
+constexpr int SHARED_E = NEXP;   // the shared expert's index in the row tables and token blocks
 
 // ----------------------------------------------------------------- device error word
 enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_BOUNDS = 2u };
@@ -53,8 +53,8 @@ constexpr int GU_NA = 2;
 constexpr int GU_P_STAGE = 2 * GX_P_BYTES;
 constexpr int GU_A_STAGE = 2 * GX_A_BYTES;
 constexpr int GU_RINGS = GU_NA * GU_A_STAGE + GU_NX * GX_X_BYTES + GU_NP * GU_P_STAGE;
-constexpr int GX_TAB_BYTES = 3 * (NEXP + 2) * 4 + 128;   // tile tables staged in shared memory
-// + alignment slack, barriers (512 B), tile tables
+constexpr int GX_TAB_BYTES = 3 * (NEXP + 2) * 4 + 128;   // row tables staged in shared memory (one spare)
+// + alignment slack, barriers (512 B), row tables
 constexpr int GU_GW = 6;                            // activation gather warps
 constexpr int GU_GROWS = (GX_BN + GU_GW - 1) / GU_GW + 4;   // token ids per gather warp and tile
 // per-CTA tile schedules (16 bytes a tile): tiles per CTA at the largest token count and
@@ -79,7 +79,7 @@ constexpr int DN_RINGS = DN_NP * GX_P_BYTES + DN_NX * GX_X_BYTES + DN_NA * GX_A_
 // epilogue staging: per epilogue warp DN_STG_BUFS buffers of 32 rows x 32 features (bf16)
 constexpr int DN_STG_BUFS = 4;
 constexpr int DN_STG_BYTES = 4 * DN_STG_BUFS * 32 * 32 * 2;
-// + alignment slack, barriers and words (1 KB), staging, tile tables
+// + alignment slack, barriers and words (1 KB), staging, row tables
 constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + DN_STG_BYTES + GX_TAB_BYTES + 16 + DN_SCHED_CAP * 16;
 static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
 constexpr int DN_THREADS = 512;   // 16 warps: producers, MMA, 8 dequant, 4 epilogue, one spare

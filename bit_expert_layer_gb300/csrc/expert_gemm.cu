@@ -34,10 +34,11 @@
 //               and written with one TMA store (the dequant permutes the weight rows
 //               so that lane order is h column order)
 // The rings are separate so the HBM-bound packed tiles can be fetched further ahead than
-// the large activation tiles fit.
+// the large activation tiles fit.  A tile of at most GU_SWAP_ROWS tokens runs with the
+// operands swapped (tokens on M, its gate and up rows together on N = 256).
 //
-// Persistent kernel: grid = number of SMs, tiles taken in a static stride from the
-// device-side tile tables built by route_scan_kernel (no host readback).
+// Persistent kernel: grid = number of SMs, tiles dealt from the size-ordered token-block
+// list that route_scan_kernel builds on the device (no host readback).
 #include "common.cuh"
 #include "gemm_common.cuh"
 #include "internal.h"
