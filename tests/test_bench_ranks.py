@@ -63,3 +63,44 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(12.5, 1, "cpu") == 12.5
     assert bench.job_throughput(1, 100, 4, 2.0) == pytest.approx(200000.0)
+
+
+def test_reference_arm_json_line():
+    """The reference arm (the CPU oracle on a bounded sample of the workload) prints one
+    JSON line with the contract's keys, on CPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "layer-T32",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["warmup"] >= 3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "layer-T32"
+
+
+def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
+    """The stored gate/up DRAM-traffic capture is keyed by a hash of the kernel source that
+    comments and blank lines do not change, while code does."""
+    import shutil
+    import bench
+    root = tmp_path / "repo"
+    csrc = root / "bit_expert_layer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("expert_gemm.cu", "common.cuh", "gemm_common.cuh"):
+        shutil.copy(os.path.join(bench.ROOT, "bit_expert_layer_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    h0 = bench.kernel_hash()
+    p = csrc / "common.cuh"
+    p.write_text(p.read_text() + "\n// a new comment\n/* and a block\n   comment */\n\n")
+    assert bench.kernel_hash() == h0
+    p.write_text(p.read_text() + "constexpr int UNUSED_FOR_TEST = 1;\n")
+    assert bench.kernel_hash() != h0
