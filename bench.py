@@ -112,6 +112,12 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
+# The ncu DRAM-traffic record that holds a workload's gate/up launch: the stack's gate/up
+# launch at T=16384 is the same kernel on the same token count as a single layer's, and
+# the capture is taken on the single layer (a few GB on the device, not the 19 GB stack).
+TRAFFIC_RECORD = {"stack40-T16384+T1": "layer-T16384", "layer-T16384": "layer-T16384"}
+
+
 def load_traffic(workload: str):
     """DRAM bytes per gate/up launch from a committed ncu summary, if it was taken on the
     current kernel source; else None."""
@@ -120,7 +126,7 @@ def load_traffic(workload: str):
         d = json.load(open(p))
     except Exception:
         return None
-    e = d.get(workload)
+    e = d.get(TRAFFIC_RECORD.get(workload, workload))
     if not e or e.get("kernel_hash") != kernel_hash():
         return None
     return e.get("bytes_per_launch")
@@ -178,12 +184,34 @@ class ClockSampler:
         return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
 
 
-def oracle_sample(hosts, wl, n_prefill: int, n_decode: int):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the core count."""
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                name = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not name:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu part")):
+                    name = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return f"{name or 'unknown'} ({os.cpu_count()} logical CPUs)"
+
+
+def oracle_sample(hosts, wl, n_prefill: int, n_decode: int, threads: int | None = None):
     """Time the CPU oracle on a bounded sample of the workload; returns (layer-tokens, s, threads)."""
     import synth
     from oracle import Oracle, default_threads
     o = Oracle()
-    threads = default_threads()
+    threads = threads or default_threads()
     n_layers = len(hosts)
     resid = n_layers > 1
     layer_tokens = 0
@@ -202,8 +230,9 @@ def run_reference(args, wl):
     rank, world, _ = rank_info()
     if rank != 0:
         return 0
+    from oracle import default_threads
     hosts = make_hosts(wl)
-    n_pf = 4 if wl["T_prefill"] else 0
+    n_pf = min(wl["T_prefill"], max(16, default_threads())) if wl["T_prefill"] else 0
     n_dc = 1 if wl["T_decode"] else 0
     for _ in range(args.warmup):
         oracle_sample(hosts[:1], wl, 1, 0 if n_pf else 1)
@@ -214,7 +243,7 @@ def run_reference(args, wl):
         tot_s += s
     value = tot_tokens / tot_s
     sample = (f"per step: {n_pf} of the {wl['T_prefill']} prefill tokens and {n_dc} decode token(s) "
-              f"through all {wl['layers']} layers on {threads} host threads")
+              f"through all {wl['layers']} layers on {threads} host threads; CPU: {cpu_model()}")
     line = dict(impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=1e3 * tot_s / args.steps, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic",
@@ -223,6 +252,143 @@ def run_reference(args, wl):
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
     return 0
+
+
+def use_burst_peak(clk) -> bool:
+    """The burst bf16 peak applies when the sampled SM clock sat at its maximum with no
+    power-cap sample (the conditions the burst figure was measured under); otherwise the
+    sustained one does."""
+    if not clk:
+        return False
+    return clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"] and "sw_power_cap" not in clk["reasons"]
+
+
+def peak_reason(clk) -> str:
+    if not clk:
+        return "no clock samples"
+    return (f"median SM clock {clk['sm_mhz']:.0f} of {clk['sm_max_mhz']:.0f} MHz, "
+            f"{'power cap seen' if 'sw_power_cap' in clk['reasons'] else 'no power-cap sample'}")
+
+
+def decode_bytes(layers, x0, resid: bool) -> int:
+    """Algorithmic HBM bytes of one decode pass: per layer the touched experts (counted from
+    the routing of that layer's actual input; the shared expert included), the router
+    matrix and the shared gate."""
+    import torch
+    x = x0.clone()
+    total = 0
+    for L in layers:
+        n_e = int(torch.unique(L.route(x)["idx"]).numel())
+        total += (n_e + 1) * EXPERT_BYTES + ROUTER_BYTES
+        if resid:
+            x = L.forward(x, residual=True)
+    torch.cuda.synchronize()
+    return total
+
+
+def time_configs(ml, dev, stream, stack, stack_layers, peaks, burst, steps: int = 10, warmup: int = 3):
+    """Whole-layer time, tokens/s and roofline fraction of each single-layer configuration
+    (CUDA events around the forward on the launching stream, a 256 MB L2 flush between
+    steps, outside the events; median of `steps`), the 40-layer decode at T=8, and the
+    grouped-query decode attention."""
+    import torch
+    import synth
+    from bit_expert_layer_gb300 import _abi
+    bf16 = peaks["bf16"] if burst else peaks["bf16_sustained"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    host_u = synth.make_layer(0)
+    host_s = synth.make_layer(0, skew=True)
+    lay_u = ml.MoELayer(ml.DeviceWeights(host_u, dev), 4096)
+    lay_s = ml.MoELayer(ml.DeviceWeights(host_s, dev), 4096)
+
+    def timed(fn, pre=None):
+        for _ in range(warmup):
+            if pre:
+                pre()
+            fn()
+            flush.zero_()
+        ts = []
+        for _ in range(steps):
+            if pre:
+                pre()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            flush.zero_()
+            ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+    for name, layer, T in (("layer-T32", lay_u, 32), ("layer-T512", lay_u, 512), ("layer-T4096", lay_u, 4096),
+                           ("layer-T4096-skew", lay_s, 4096)):
+        x = torch.from_numpy(synth.make_x(0, T).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty_like(x)
+        ms = timed(lambda: layer.forward(x, out=y))
+        assert layer.get_error() == 0
+        n_e = int(torch.unique(layer.route(x)["idx"]).numel())
+        hbm_bytes = (n_e + 1) * EXPERT_BYTES + ROUTER_BYTES + 2 * T * 2048 * 2
+        tflops = FLOP_PER_TOKEN * T / (ms / 1e3) / 1e12
+        gbs = hbm_bytes / (ms / 1e3) / 1e9
+        out[name] = dict(us_per_layer=1e3 * ms, tokens_per_s=T / (ms / 1e3), tflops=tflops,
+                         tensor_frac=tflops / bf16, hbm_bytes=hbm_bytes, hbm_gbs=gbs, hbm_frac=gbs / peaks["hbm"],
+                         touched_experts=n_e,
+                         bound="tensor" if FLOP_PER_TOKEN * T / (bf16 * 1e12) > hbm_bytes / (peaks["hbm"] * 1e9)
+                         else "hbm")
+    if stack is not None:
+        T = 8
+        xs = torch.from_numpy(synth.make_x(1, T).view(np.int16)).to(dev).view(torch.bfloat16)
+        xw = torch.empty_like(xs)
+
+        ms = timed(lambda: stack.forward_(xw), pre=lambda: xw.copy_(xs))
+        assert stack_layers[0].get_error() == 0
+        nb = decode_bytes(stack_layers, xs, True)
+        gbs = nb / (ms / 1e3) / 1e9
+        out["decode-T8"] = dict(us_per_layer=1e3 * ms / len(stack_layers), us_per_stack=1e3 * ms,
+                                hbm_bytes_per_pass=nb, hbm_gbs=gbs, hbm_frac=gbs / peaks["hbm"], layers=len(stack_layers))
+    # grouped-query decode attention (the full-attention layers' decode step): 8 sequences
+    # of 4K and 32K cached positions, HBM-bound on the KV rows
+    for name, S in (("gqa-decode-ctx4K-B8", 4096), ("gqa-decode-ctx32K-B8", 32768)):
+        B = 8
+        q, k, v, lens = synth.make_gqa(7, B, S)
+        dv = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+        qd, kd, vd = dv(q), dv(k), dv(v)
+        od = torch.empty_like(qd)
+        nws = _abi.gqa_decode_workspace_bytes(B)
+        gws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+        lens_l = [int(x) for x in lens]
+        ms = timed(lambda: _abi.gqa_decode_attention(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), lens_l, B, S,
+                                                     od.data_ptr(), gws.data_ptr(), nws, stream.cuda_stream))
+        assert _abi.gqa_decode_get_error(gws.data_ptr()) == 0
+        nb = B * 2 * S * 128 * 2 * 2 + 2 * B * 16 * 128 * 2
+        gbs = nb / (ms / 1e3) / 1e9
+        out[name] = dict(us=1e3 * ms, kv_bytes=nb, hbm_gbs=gbs, hbm_frac=gbs / peaks["hbm"], bound="hbm",
+                         shape="16 query heads, 2 KV heads, head 128, bf16 KV cache")
+        del kd, vd
+    out["peak_bf16_tflops"] = bf16
+    out["peak_hbm_gbs"] = peaks["hbm"]
+    out["method"] = "median of 10 CUDA-event timings per configuration, 256 MB L2 flush between steps"
+    del lay_u, lay_s
+    return out
+
+
+def cpu_baseline(hosts, wl, n_layers):
+    """The oracle on the host cores: as many prefill tokens as host threads (and one
+    decode token) through every layer on all threads, and one prefill token through every
+    layer on one thread."""
+    from oracle import default_threads
+    threads = default_threads()
+    n_pf = min(wl["T_prefill"], max(16, threads)) if wl["T_prefill"] else 0
+    n_dc = 1 if wl["T_decode"] else 0
+    n, s, threads = oracle_sample(hosts, wl, n_pf, n_dc, threads)
+    n1, s1, _ = oracle_sample(hosts, wl, 1 if n_pf else 0, 0 if n_pf else 1, 1)
+    return dict(value=n / s, unit=UNIT, cores=threads, kind="oracle",
+                sample=f"{n_pf} prefill + {n_dc} decode tokens through all {n_layers} layers on {threads} threads "
+                       f"({n} layer-tokens, {s:.1f} s)",
+                one_thread=dict(value=n1 / s1, unit=UNIT,
+                                sample=f"1 token through all {n_layers} layers on 1 thread ({s1:.1f} s)"),
+                cpu=cpu_model())
 
 
 def run_ours(args, wl):
@@ -380,49 +546,44 @@ def run_ours(args, wl):
 
     # ---------------- roofline of the dominant kernel
     peaks = load_peaks()
+    burst = use_burst_peak(clk)
+    bf16_peak = peaks["bf16"] if burst else peaks["bf16_sustained"]
+    bf16_src = f"{peaks['src']} bf16 {'burst' if burst else 'sustained'} ({peak_reason(clk)})"
     roof = None
     gu_ms, gu_n = kern.get("gateup", (0.0, 0))
     if Tp and gu_n:
         flop = GATEUP_FLOP_PER_ROW * 9 * Tp
         achieved = flop / (gu_ms / gu_n / 1e3) / 1e12
-        peak = peaks["bf16_sustained"] if n_layers > 1 else peaks["bf16"]
         tb = load_traffic(args.workload)
-        roof = dict(kernel="gateup", bound="tensor", achieved=achieved, peak=peak, unit="TFLOP/s",
-                    frac=achieved / peak, traffic=tb,
+        roof = dict(kernel="gateup", bound="tensor", achieved=achieved, peak=bf16_peak, unit="TFLOP/s",
+                    frac=achieved / bf16_peak, traffic=tb,
                     algorithmic=f"{GATEUP_FLOP_PER_ROW} FLOP x 9T rows per launch (T={Tp})",
-                    peak_source=f"{peaks['src']} bf16 {'sustained' if n_layers > 1 else 'burst'}")
+                    peak_source=bf16_src)
     dec = None
+    dec_roof = None
     if Td:
         dms = part_ms["decode"] / args.steps
-        # algorithmic HBM bytes of one decode pass: per layer the touched experts (counted
-        # from the routing of that layer's actual input; the shared expert included), the
-        # router matrix and the shared gate
-        x = xd_src.clone()
-        dbytes = 0
-        for L in layers:
-            n_e = int(torch.unique(L.route(x)["idx"]).numel())
-            dbytes += (n_e + 1) * EXPERT_BYTES + ROUTER_BYTES
-            if resid:
-                x = L.forward(x, residual=True)
-        torch.cuda.synchronize(dev)
+        dbytes = decode_bytes(layers, xd_src, resid)
         gbs = dbytes / (dms / 1e3) / 1e9
         dec = dict(us_per_layer=1e3 * dms / n_layers, us_per_stack=1e3 * dms,
                    hbm_bytes_per_pass=dbytes, hbm_gbs=gbs, hbm_frac=gbs / peaks["hbm"])
-        if roof is None:
-            roof = dict(kernel="decode_layers", bound="hbm", achieved=gbs, peak=peaks["hbm"], unit="GB/s",
-                        frac=gbs / peaks["hbm"], traffic=None,
+        dec_roof = dict(kernel="decode_layers", bound="hbm", achieved=gbs, peak=peaks["hbm"], unit="GB/s",
+                        frac=gbs / peaks["hbm"], T=Td, us_per_layer=1e3 * dms / n_layers,
                         algorithmic=f"touched experts x {EXPERT_BYTES} B + {ROUTER_BYTES} B per layer, "
                                     f"{dbytes} B per pass of {n_layers} layer(s), T={Td}",
                         peak_source=f"{peaks['src']} HBM copy")
+        if roof is None:
+            roof = dict(dec_roof, traffic=None)
+
+    # ---------------- the other configurations, timed in the same run (single layers with
+    # an L2 flush between steps; decode at T=8 through the same 40-layer stack)
+    cfg_block = None
+    if rank == 0 and not args.no_configs and args.workload == DEFAULT_WORKLOAD:
+        cfg_block = time_configs(ml, dev, stream, stack if resid else None, layers, peaks, burst)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_pf = 6 if Tp else 0
-        n_dc = 1 if Td else 0
-        n, s, threads = oracle_sample(hosts, wl, n_pf, n_dc)
-        cpu = dict(value=n / s, unit=UNIT, cores=threads, kind="oracle",
-                   sample=f"{n_pf} prefill + {n_dc} decode tokens through all {n_layers} layers "
-                          f"({n} layer-tokens, {s:.1f} s)")
+        cpu = cpu_baseline(hosts, wl, n_layers)
 
     per_kernel = {k: dict(ms_avg=(v[0] / v[1]) if v[1] else None, launches=v[1], ms_total=v[0])
                   for k, v in kern.items() if v[1]}
@@ -438,8 +599,8 @@ def run_ours(args, wl):
         prefill_layer_tokens_per_s=(Tp * n_layers * args.steps / (part_ms["prefill"] / 1e3)) if Tp else None,
         prefill_tflops=(FLOP_PER_TOKEN * Tp * n_layers * args.steps / (part_ms["prefill"] / 1e3) / 1e12)
         if Tp else None,
-        decode=dec, roofline=roof, cpu_baseline=cpu, e2e=e2e, gpu_launches=launches, clocks=clk,
-        kernels=per_kernel,
+        decode=dec, roofline=roof, decode_roofline=dec_roof, configs=cfg_block, cpu_baseline=cpu, e2e=e2e,
+        gpu_launches=launches, clocks=clk, kernels=per_kernel,
     )
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -447,6 +608,18 @@ def run_ours(args, wl):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Run this script as n ranks of one node under torch.distributed.run (one rank per
+    GPU, rendezvous on 127.0.0.1); returns the launcher's exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 def main(argv=None):
@@ -457,9 +630,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration block")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
     wl = WORKLOADS[args.workload]
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return spawn_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv))
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -13,6 +13,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_layer.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe_layer.h")
+HEADERS = [HEADER, os.path.join(os.path.dirname(_PKG), "include", "gqa_decode.h")]
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
@@ -88,6 +89,18 @@ def lib() -> C.CDLL:
         L.moe_last_error_detail.restype = C.c_char_p
         L.moe_decode_forward_static.argtypes = [C.POINTER(MoeWeights), P, I, P, I, P]
         L.moe_decode_forward_static.restype = S
+        L.moe_decode_static_get_error.argtypes = []
+        L.moe_decode_static_get_error.restype = S
+        L.gqa_decode_workspace_bytes.argtypes = [I]
+        L.gqa_decode_workspace_bytes.restype = C.c_size_t
+        L.gqa_decode_attention.argtypes = [P, P, P, P, I, I, P, P, C.c_size_t, P]
+        L.gqa_decode_attention.restype = S
+        L.gqa_decode_get_error.argtypes = [P]
+        L.gqa_decode_get_error.restype = S
+        L.moe_decode_trace.argtypes = [P, P, C.c_size_t]
+        L.moe_decode_trace.restype = S
+        L.moe_set_wait_limit_ns.argtypes = [C.c_ulonglong]
+        L.moe_set_wait_limit_ns.restype = None
         L.moe_pipeline_counters.argtypes = [P, P]
         L.moe_pipeline_counters.restype = S
         L.moe_profiler_enable.argtypes = [I]
@@ -175,6 +188,27 @@ def moe_decode_forward_static(weights: MoeWeights, x: int, T: int, out: int, res
            "moe_decode_forward_static")
 
 
+def moe_decode_static_get_error() -> int:
+    return int(lib().moe_decode_static_get_error())
+
+
+DEC_TRACE_CTAS, DEC_TRACE_STAMPS = 256, 16
+
+
+def moe_decode_trace(layer: int, n_layers: int):
+    """Phase timestamps of the last decode launch (MOE_DECODE_TRACE=1), as a uint64 array
+    [n_layers][256 CTAs][16 stamps]."""
+    import numpy as np
+    n = n_layers * DEC_TRACE_CTAS * DEC_TRACE_STAMPS
+    buf = np.zeros(n, np.uint64)
+    _check(lib().moe_decode_trace(layer, buf.ctypes.data_as(C.c_void_p), n), "moe_decode_trace")
+    return buf.reshape(n_layers, DEC_TRACE_CTAS, DEC_TRACE_STAMPS)
+
+
+def moe_set_wait_limit_ns(ns: int) -> None:
+    lib().moe_set_wait_limit_ns(int(ns))
+
+
 PIPE_SLOTS = ["mma_wait_acc_drain", "mma_wait_dequant", "mma_wait_tma", "mma_total", "producer_wait_stage",
               "producer_total", "dequant_wait_tma", "dequant_total", "epilogue_wait_acc", "epilogue_total",
               "tiles"]
@@ -201,9 +235,28 @@ def moe_profiler_read() -> dict:
     return {names[i].decode(): (tot[i], cnt[i]) for i in range(min(k, n))}
 
 
+def gqa_decode_workspace_bytes(B: int) -> int:
+    return int(lib().gqa_decode_workspace_bytes(int(B)))
+
+
+def gqa_decode_attention(q: int, k: int, v: int, lens, B: int, S_max: int, out: int, workspace: int,
+                         workspace_bytes: int, stream: int = 0) -> None:
+    """lens: a sequence of B ints (host memory, as the C entry takes it)."""
+    vals = [int(x) for x in lens]
+    arr = (C.c_int32 * max(1, len(vals)))(*vals)
+    _check(lib().gqa_decode_attention(q, k, v, C.cast(arr, C.c_void_p), B, S_max, out, workspace, workspace_bytes,
+                                      stream or None), "gqa_decode_attention")
+
+
+def gqa_decode_get_error(workspace: int) -> int:
+    return int(lib().gqa_decode_get_error(workspace))
+
+
 def declared_functions() -> list[str]:
-    """Names of the functions declared in include/moe_layer.h."""
+    """Names of the functions declared in include/*.h."""
     import re
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:moe|gqa)_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)

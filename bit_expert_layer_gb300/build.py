@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_layer.so")
-SOURCES = ["router.cu", "expert_gemm.cu", "down.cu", "decode.cu", "decode_layers.cu", "moe_layer.cu", "noalloc.cu"]
+SOURCES = ["router.cu", "expert_gemm.cu", "down.cu", "decode.cu", "decode_layers.cu", "moe_layer.cu", "noalloc.cu",
+           "gqa.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
@@ -33,7 +34,7 @@ def nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "moe_layer.h"))
+    files.extend(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
     return files
 
 

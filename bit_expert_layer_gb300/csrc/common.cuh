@@ -22,7 +22,11 @@ constexpr int SHARED_E = NEXP;   // the shared expert's index in the row tables 
 
 // ----------------------------------------------------------------- device error word
 enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_BOUNDS = 2u };
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s per wait
+// Default time limit of a bounded wait (2 s).  The limit of the waits a launch makes on
+// the work of other threads is a launch parameter (moe_set_wait_limit_ns can shorten it,
+// to exercise the give-up path); the waits of the teardown after a give-up, which let
+// copies and MMAs already in flight land before the CTA exits, always use this one.
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
 
 // ----------------------------------------------------------------- kernel geometry
 // Router (prefill): 128 tokens per CTA (M), the 256 experts on N.
@@ -139,11 +143,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete.  Gives up after WAIT_LIMIT_NS
-// (or as soon as another thread of the CTA has given up, via *abort): records
-// ERRBIT_TIMEOUT in the device error word and returns false.  Never hangs.
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Below this limit (the device timer's resolution, about 1 us) a bounded wait gives up
+// at once if its phase is not already complete.
+constexpr unsigned long long WAIT_LIMIT_IMMEDIATE_NS = 1000ull;
+
+// Wait for the phase of parity `parity` to complete.  Gives up after limit_ns (or as
+// soon as another thread of the CTA has given up, via *abort): records ERRBIT_TIMEOUT in
+// the device error word and returns false.  Never hangs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, unsigned long long limit_ns) {
+  if (limit_ns < WAIT_LIMIT_IMMEDIATE_NS) {
+    if (mbar_test_wait(bar, parity)) return true;
+    atomicOr(err, ERRBIT_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
@@ -151,7 +178,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, ERRBIT_TIMEOUT);
       *abort_flag = 1;
       return false;

@@ -41,6 +41,7 @@
 // mbarriers (one cp.async arrival per thread).  Every wait (tags, copies) gives up after
 // a time limit (error bit, abort flag shared by all CTAs).
 #include "common.cuh"
+#include "decode_tag.h"
 #include "gemm_common.cuh"
 #include "internal.h"
 
@@ -92,17 +93,21 @@ struct alignas(16) DlShared {
   float act_w[DEC_MAX_ACTIVE][DEC_MAX_T];
   int n_active;
   int abort;
+  int last;                                     // this CTA is the last one out of the launch
 };
 static_assert(HS_ROWS >= DEC_MAX_T * 9, "h' staging must hold one batch of 9 experts at T = 8");
+static_assert(DEC_MAX_LAYERS <= (1 << DEC_TAG_LAYER_BITS), "a tag holds the layer in its low bits");
 static_assert(sizeof(DlShared) <= 232448, "shared memory per CTA exceeds 227 KB");
 static_assert(DEC_LT_WORDS == 2ull * DEC_MAX_T * NROW_A && DEC_HT_WORDS == 2ull * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2) &&
                   DEC_XT_WORDS == 2ull * DEC_MAX_T * (HID / 2),
               "tagged table sizes");
 
 struct Ctx {
+  unsigned long long* trace;    // this layer's and CTA's timestamps, or nullptr
   uint32_t tag;                 // current layer's tag
   unsigned* abort_word;         // grid-wide abort flag
   unsigned* err;
+  unsigned long long limit;     // time limit of a bounded wait
 };
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -171,7 +176,7 @@ struct PollClock {
     const unsigned long long now = globaltimer_ns();
     if (t0 == 0) {
       t0 = now;
-    } else if (now - t0 > WAIT_LIMIT_NS) {
+    } else if (cx.limit < WAIT_LIMIT_IMMEDIATE_NS || now - t0 > cx.limit) {
       atomicOr(cx.err, ERRBIT_TIMEOUT);
       atomicExch(cx.abort_word, 1u);
       return false;
@@ -180,6 +185,11 @@ struct PollClock {
     return true;
   }
 };
+
+// Phase timestamp k of this layer and CTA (tracing only).
+__device__ __forceinline__ void stamp(const Ctx& cx, int k) {
+  if (cx.trace != nullptr && threadIdx.x == 0) cx.trace[k] = globaltimer_ns();
+}
 
 // ---- order-preserving float keys (larger float -> larger key); NaN maps below -inf
 __device__ __forceinline__ uint32_t fkey(float v) {
@@ -193,7 +203,7 @@ __device__ __forceinline__ float kfloat(uint32_t k) {
 
 // bounded wait on one of this CTA's bulk-copy barriers, the same outcome in every thread
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, const Ctx& cx, DlShared& s) {
-  bool ok = mbar_wait(smem_u32(bar), parity, cx.err, &s.abort);
+  bool ok = mbar_wait(smem_u32(bar), parity, cx.err, &s.abort, cx.limit);
   if (!ok) atomicExch(cx.abort_word, 1u);
   return __syncthreads_and(ok) != 0;
 }
@@ -321,6 +331,7 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
                  : make_uint4(0, 0, 0, 0);
   }
   if (!__syncthreads_and(ok)) return false;
+  stamp(cx, 1);
   // residual inputs of this CTA's phase-C rows (chunks 2c, 2c+1 of every token)
   if (p.residual && c < DL_CTAS_C) {
 #pragma unroll
@@ -338,6 +349,7 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
     }
   }
   if (!cta_wait(&s.mb_a, l & 1, cx, s)) return false;
+  stamp(cx, 2);
   if (L.norm_w) {
 #pragma unroll
     for (int i = 0; i < CH_PER_THREAD; ++i) {
@@ -427,6 +439,7 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
       st_tagged(p.lt + (static_cast<size_t>(l & 1) * DEC_MAX_T + t) * NROW_A + rr, __float_as_uint(a), cx.tag);
     }
   }
+  stamp(cx, 3);
   return true;
 }
 
@@ -508,6 +521,7 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
     }
   }
   if (!__syncthreads_and(ok)) return false;
+  stamp(cx, 4);
   if (tid < T * TOPK) {
     const int e = s.idx[tid / TOPK][tid % TOPK];
     atomicOr(&s.mask[e >> 5], 1u << (e & 31));
@@ -537,6 +551,7 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
     if (tid < T) s.act_w[n][tid] = s.sig[tid];
   }
   __syncthreads();
+  stamp(cx, 5);
   return true;
 }
 
@@ -553,6 +568,7 @@ __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int 
   const int nb = (my_units + DL_UB - 1) / DL_UB;
   for (int b = 0; b < 2 && b < nb; ++b) issue_units(L, s, b, n_units);
   issue_stage_c(L, s);   // phase C's copies queue behind the first batches
+  stamp(cx, 6);
   // B fragments (token g, this lane's 32 inputs), the same for every unit
   uint4 xb[4];
 #pragma unroll
@@ -565,6 +581,7 @@ __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int 
     const int buf = b & 1;
     if (!cta_wait(&s.mb_b[buf], bphase[buf] & 1, cx, s)) return false;
     ++bphase[buf];
+    if (b == 0) stamp(cx, 7);
 #pragma unroll
     for (int j = 0; j < DL_UB; ++j) {
       const int u = blockIdx.x + (DL_UB * b + j) * G;
@@ -587,6 +604,7 @@ __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int 
 #pragma unroll
       for (int k = 0; k < 4; ++k) s.red[j][warp][lane][k] = d[k];
     }
+    if (b == 0) stamp(cx, 12);
     __syncthreads();
     if (b + 2 < nb) issue_units(L, s, b + 2, n_units);   // buffer b & 1 is free
     if (tid < DL_UB * 32) {
@@ -619,8 +637,10 @@ __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int 
         }
       }
     }
+    if (b == 0) stamp(cx, 13);
     __syncthreads();
   }
+  stamp(cx, 8);
   return true;
 }
 
@@ -652,6 +672,7 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
   const unsigned long long* ht = p.ht + static_cast<size_t>(l & 1) * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2);
   uint32_t* hs = reinterpret_cast<uint32_t*>(&s.gu[0][0]);   // h' rows [expert-in-batch * T + t][256 pairs]
   if (!cta_wait(&s.mb_c, l & 1, cx, s)) return false;
+  stamp(cx, 9);
   float d[4] = {0.f, 0.f, 0.f, 0.f};
   const int eb = HS_ROWS / T;                          // experts per batch
   for (int a0 = 0; a0 < n_act; a0 += eb) {
@@ -691,6 +712,7 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
       }
     }
     if (!__syncthreads_and(ok)) return false;
+    if (a0 == 0) stamp(cx, 10);
     for (int ai = eq; ai < na; ai += 4) {
       const int a = a0 + ai;
       uint4 hb[4];
@@ -719,6 +741,7 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) s.red[0][warp][lane][k] = d[k];
+  stamp(cx, 14);
   __syncthreads();
   if (warp == 0) {
     float q[4] = {0.f, 0.f, 0.f, 0.f};
@@ -732,6 +755,7 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
       const int tok = 2 * c4 + (k & 1);
       if (p.residual && tok < T) q[k] += s.xres[tok][(k < 2) ? g : g + 8];
     }
+    stamp(cx, 15);
     if (l + 1 == p.n_layers) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -755,6 +779,7 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
       }
     }
   }
+  stamp(cx, 11);
   return true;
 }
 
@@ -772,16 +797,22 @@ __global__ void __launch_bounds__(DL_THREADS, 1) decode_layers_kernel(const __gr
     fence_mbar_init();
   }
   __syncthreads();
-  // tags: (launch epoch + 1) * 64 + layer; the epoch advances when a launch ends
+  // tags: dec_tag(launch epoch, layer); the epoch advances when a launch ends
   const uint32_t epoch = *reinterpret_cast<volatile unsigned*>(p.sync + 3);
   Ctx cx;
+  cx.trace = nullptr;
   cx.abort_word = p.sync + 2;
+  cx.limit = p.wait_ns;
   uint32_t bphase[2] = {0u, 0u};
   issue_stage_a(p.layer[0], s);
   for (int l = 0; l < p.n_layers; ++l) {
     const DecLayer& L = p.layer[l];
-    cx.tag = ((epoch + 1u) << 6) + static_cast<uint32_t>(l);
+    cx.tag = dec_tag(epoch, l);
     cx.err = L.err;
+    cx.trace = (p.trace != nullptr && blockIdx.x < DEC_TRACE_CTAS)
+                   ? p.trace + (static_cast<size_t>(l) * DEC_TRACE_CTAS + blockIdx.x) * DEC_TRACE_STAMPS
+                   : nullptr;
+    stamp(cx, 0);
     if (!phase_a(p, L, l, cx, s)) break;
     if (!phase_b_route(p, L, l, cx, s, l == p.n_layers - 1 && blockIdx.x == 0 && p.topk_idx != nullptr)) break;
     if (!phase_b_gateup(p, L, l, cx, s, bphase)) break;
@@ -792,13 +823,27 @@ __global__ void __launch_bounds__(DL_THREADS, 1) decode_layers_kernel(const __gr
   }
   // leaving early: this thread's copies still in flight land before the CTA exits
   asm volatile("cp.async.wait_all;" ::: "memory");
-  // the last CTA out clears the exit count and the abort flag and advances the epoch
+  // the last CTA out clears the exit count and the abort flag and advances the epoch;
+  // at the end of an epoch period it first clears every tagged word (see decode_tag.h)
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    if (atomicAdd(p.sync + 1, 1u) == gridDim.x - 1) {
+    s.last = atomicAdd(p.sync + 1, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s.last) {
+    __threadfence();
+    const uint32_t next = dec_next_epoch(epoch);
+    if (next == 0u) {
+      for (size_t i = threadIdx.x; i < DEC_LT_WORDS; i += DL_THREADS) p.lt[i] = 0ull;
+      for (size_t i = threadIdx.x; i < DEC_HT_WORDS; i += DL_THREADS) p.ht[i] = 0ull;
+      for (size_t i = threadIdx.x; i < DEC_XT_WORDS; i += DL_THREADS) p.xt[i] = 0ull;
+      __threadfence();
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
       atomicExch(p.sync + 2, 0u);
-      atomicAdd(p.sync + 3, 1u);
+      atomicExch(p.sync + 3, next);
       __threadfence();
       atomicExch(p.sync + 1, 0u);
     }
@@ -806,26 +851,36 @@ __global__ void __launch_bounds__(DL_THREADS, 1) decode_layers_kernel(const __gr
 }
 
 cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s) {
-  static int grid = 0;
-  static cudaError_t init_err = cudaSuccess;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0, nsm = 0, per_sm = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(sizeof(DlShared)));
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layers_kernel, DL_THREADS, sizeof(DlShared));
-    if (e == cudaSuccess && per_sm < 1) e = cudaErrorCooperativeLaunchTooLarge;
-    if (e == cudaSuccess && nsm < DL_CTAS_C) e = cudaErrorCooperativeLaunchTooLarge;
-    init_err = e;
-    grid = nsm;   // one CTA per SM: all resident, as the cross-CTA waits require
+  // per device: the kernel's shared-memory attribute is a setting of the current device,
+  // and the grid is that device's SM count
+  constexpr int kMaxDevices = 64;
+  struct DevInit {
+    std::once_flag once;
+    int grid = 0;
+    cudaError_t err = cudaSuccess;
+  };
+  static DevInit init[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DevInit& d = init[dev];
+  std::call_once(d.once, [&d, dev] {
+    int nsm = 0, per_sm = 0;
+    cudaError_t e2 = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e2 == cudaSuccess)
+      e2 = cudaFuncSetAttribute(decode_layers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(DlShared)));
+    if (e2 == cudaSuccess)
+      e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layers_kernel, DL_THREADS, sizeof(DlShared));
+    if (e2 == cudaSuccess && per_sm < 1) e2 = cudaErrorCooperativeLaunchTooLarge;
+    if (e2 == cudaSuccess && nsm < DL_CTAS_C) e2 = cudaErrorCooperativeLaunchTooLarge;
+    d.err = e2;
+    d.grid = nsm;   // one CTA per SM: all resident, as the cross-CTA waits require
   });
-  if (init_err != cudaSuccess) return init_err;
+  if (d.err != cudaSuccess) return d.err;
   void* args[] = {const_cast<DecLayersParams*>(&p)};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(decode_layers_kernel), dim3(grid),
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(decode_layers_kernel), dim3(d.grid),
                                      dim3(DL_THREADS), args, sizeof(DlShared), s);
 }
 

@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   const int ntiles = build_schedule(sched, DN_SCHED_CAP, p.blocks, s_off, s_cnt, DN_MBLK, p.T, p.err, false);
   __syncthreads();
   constexpr int NKB = INTER / 64;   // 8
+  uint32_t p_issued = 0;   // packed-tile producer (warp 0) / activation producer (warp 5): K steps issued
 
   if (warp == 0) {
     if (lane == 0) {
@@ -127,14 +128,12 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const int wrow = (sh ? 0 : ti.e * HID) + ti.mb * GX_BM;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int s = it % DN_NP;
-          if (!mbar_wait_t(PEMPTY(s), ((it / DN_NP) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) { alive = false; break; }
+          if (!mbar_wait_t(PEMPTY(s), ((it / DN_NP) & 1) ^ 1, p.err, abort_flag, p.wait_ns, pc[0], pp)) { alive = false; break; }
           mbar_arrive_expect_tx(PFULL(s), GX_P_BYTES);
           tma_load_2d_hint(smem_u32(smem + OFF_P + s * GX_P_BYTES), mq, PFULL(s), kb * 8, wrow, pol);
         }
       }
-      if (!alive) {
-        for (uint32_t i = (it > DN_NP ? it - DN_NP : 0); i < it; ++i) drain_wait(PFULL(i % DN_NP), (i / DN_NP) & 1);
-      }
+      p_issued = it;
       if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
     }
   } else if (warp == 5) {
@@ -150,16 +149,14 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int s = it % DN_NX;
-          if (!mbar_wait(XEMPTY(s), ((it / DN_NX) & 1) ^ 1, p.err, abort_flag)) { alive = false; break; }
+          if (!mbar_wait(XEMPTY(s), ((it / DN_NX) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) { alive = false; break; }
           const uint32_t st = smem_u32(smem + OFF_X + s * GX_X_BYTES);
           mbar_arrive_expect_tx(XFULL(s), nbox * GX_XBOX * 128);
           for (int j = 0; j < nbox; ++j)
             tma_load_2d_hint(st + j * GX_XBOX * 128, &tm_h, XFULL(s), kb * 64, ti.row0 + j * GX_XBOX, pol);
         }
       }
-      if (!alive) {
-        for (uint32_t i = (it > DN_NX ? it - DN_NX : 0); i < it; ++i) drain_wait(XFULL(i % DN_NX), (i / DN_NX) & 1);
-      }
+      p_issued = it;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -175,14 +172,14 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, N);
         const int buf = tc & 1;
-        if (!mbar_wait_t(ACCE(buf), ((tc >> 1) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
+        if (!mbar_wait_t(ACCE(buf), ((tc >> 1) & 1) ^ 1, p.err, abort_flag, p.wait_ns, pc[0], pp)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * 256;
         bool alive = true;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int sa = it % DN_NA, sx = it % DN_NX;
-          if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, pc[1], pp)) ||
-              (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, pc[2], pp))) {
+          if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, p.wait_ns, pc[1], pp)) ||
+              (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, p.wait_ns, pc[2], pp))) {
             alive = false;
             break;
           }
@@ -240,8 +237,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 #pragma unroll
       for (int kb = 0; kb < NKB; ++kb) {
         const int sp = it % DN_NP, sa = it % DN_NA;
-        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, pc[0], pp) ||
-            !mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag)) {
+        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, p.wait_ns, pc[0], pp) ||
+            !mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) {
           alive = false;
           break;
         }
@@ -279,7 +276,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       const TileInfo ti = sched_tile(sched, tix);
       if (!ti.ok) continue;
       const int buf = tc & 1;
-      const bool got = mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, pc[0], pp);
+      const bool got = mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, p.wait_ns, pc[0], pp);
       if (!__all_sync(0xffffffffu, got)) break;   // tcgen05.ld below needs the whole warp
       tc_fence_after();
       const int fcol = ti.mb * GX_BM + q * 32;    // this warp's first output feature
@@ -343,6 +340,16 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if ((warp == 0 || warp == 5) && lane == 0 && *abort_flag) {
+    // a launch that gave up (whichever role did): the tiles still in flight land before
+    // the CTA's shared memory goes away (the latest phase of each stage)
+    if (warp == 0)
+      for (uint32_t i = (p_issued > DN_NP ? p_issued - DN_NP : 0); i < p_issued; ++i)
+        drain_wait(PFULL(i % DN_NP), (i / DN_NP) & 1);
+    else
+      for (uint32_t i = (p_issued > DN_NX ? p_issued - DN_NX : 0); i < p_issued; ++i)
+        drain_wait(XFULL(i % DN_NX), (i / DN_NX) & 1);
+  }
   if (warp == 1) {
     tc_fence_after();
     if (lane == 0) drain_wait(DRAIN, 0);

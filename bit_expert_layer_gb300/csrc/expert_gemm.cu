@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   __syncthreads();
   constexpr int NKB = HID / 64;
   const bool pp = p.pipe != nullptr;
+  uint32_t p_issued = 0;   // packed-tile producer: K steps whose loads it issued
 
   // Registers by warpgroup (setmaxnreg, executed by all four warps of a group at the
   // top of its branch): the copy and MMA-issue warpgroups 0-1 hand theirs to the dequant
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           const int wrow = (sh ? 0 : ti.e * INTER) + ti.mb * GX_BM;
           for (int kb = 0; kb < NKB; ++kb, ++it) {
             const int s = it % GU_NP;
-            if (!mbar_wait_t(PEMPTY(s), ((it / GU_NP) & 1) ^ 1, p.err, abort_flag, pc[0], pp)) {
+            if (!mbar_wait_t(PEMPTY(s), ((it / GU_NP) & 1) ^ 1, p.err, abort_flag, p.wait_ns, pc[0], pp)) {
               alive = false;
               break;
             }
@@ -160,9 +161,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
             tma_load_2d_hint(st + GX_P_BYTES, mu, PFULL(s), kb * 8, wrow, pol);
           }
         }
-        if (!alive) {
-          for (uint32_t i = (it > GU_NP ? it - GU_NP : 0); i < it; ++i) drain_wait(PFULL(i % GU_NP), (i / GU_NP) & 1);
-        }
+        p_issued = it;
         if (pp) pipe_flush(p.pipe, 4, pc, 1, clock64() - t_role, 5);
       }
     } else if (warp == 1) {
@@ -180,12 +179,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
           // up rows) MMA per K slice instead of a gate and an up MMA of N tokens each
           const bool swp = ti.n_rows <= GU_SWAP_ROWS;
           const uint32_t idesc = swp ? idesc_bf16(128, 2 * GX_BM) : idesc_bf16(128, N);
-          if (!mbar_wait_t(ACCE, (tc & 1) ^ 1, p.err, abort_flag, pc[0], pp)) break;
+          if (!mbar_wait_t(ACCE, (tc & 1) ^ 1, p.err, abort_flag, p.wait_ns, pc[0], pp)) break;
           tc_fence_after();
           bool alive = true;
           for (int kb = 0; kb < NKB; ++kb, ++it) {
             const int sa = it % GU_NA, sx = it % GU_NX;
-            if (!(rdy & 1u) && !mbar_wait_t(READY(it % GU_NR), (it / GU_NR) & 1, p.err, abort_flag, pc[1], pp)) {
+            if (!(rdy & 1u) && !mbar_wait_t(READY(it % GU_NR), (it / GU_NR) & 1, p.err, abort_flag, p.wait_ns, pc[1], pp)) {
               alive = false;
               break;
             }
@@ -241,7 +240,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
         __syncwarp();
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int s = it % GU_NX;
-          alive = __all_sync(0xffffffffu, mbar_wait(XEMPTY(s), ((it / GU_NX) & 1) ^ 1, p.err, abort_flag));
+          alive = __all_sync(0xffffffffu, mbar_wait(XEMPTY(s), ((it / GU_NX) & 1) ^ 1, p.err, abort_flag, p.wait_ns));
           if (!alive) break;
           uint8_t* st = smem + OFF_X + s * GX_X_BYTES;
           for (int q = lane; q < nr * 8; q += 32) {
@@ -310,8 +309,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int sp = it % GU_NP, sa = it % GU_NA, sr = it % GU_NR;
-          if (!mbar_wait_t(PFULL(sp), (it / GU_NP) & 1, p.err, abort_flag, pc[0], pp) ||
-              !mbar_wait(AEMPTY(sa), ((it / GU_NA) & 1) ^ 1, p.err, abort_flag)) {
+          if (!mbar_wait_t(PFULL(sp), (it / GU_NP) & 1, p.err, abort_flag, p.wait_ns, pc[0], pp) ||
+              !mbar_wait(AEMPTY(sa), ((it / GU_NA) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) {
             alive = false;
             break;
           }
@@ -355,7 +354,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
     for (int tix = 0; tix < ntiles; ++tix) {
       const TileInfo ti = sched_tile(sched, tix);
       if (!ti.ok) continue;
-      bool ok = mbar_wait_t(ACCF, tc & 1, p.err, abort_flag, pc[0], pp);
+      bool ok = mbar_wait_t(ACCF, tc & 1, p.err, abort_flag, p.wait_ns, pc[0], pp);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -468,6 +467,12 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   // ------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // a launch that gave up (whichever role did): the packed tiles still in flight land
+    // before the CTA's shared memory goes away (the latest phase of each stage)
+    for (uint32_t i = (p_issued > GU_NP ? p_issued - GU_NP : 0); i < p_issued; ++i)
+      drain_wait(PFULL(i % GU_NP), (i / GU_NP) & 1);
+  }
   if (warp == 1) {
     tc_fence_after();
     if (lane == 0) drain_wait(DRAIN, 0);

@@ -184,10 +184,11 @@ __device__ __forceinline__ uint32_t umma_k64_poll(uint32_t d, uint64_t a, uint64
 //   slot 8, 9  one epilogue thread: waiting for the accumulator; total
 //   slot 10    tiles processed (MMA issuer)
 __device__ __forceinline__ bool mbar_wait_t(uint32_t bar, uint32_t parity, unsigned int* err,
-                                            volatile int* abort_flag, unsigned long long& acc, bool on) {
-  if (!on) return mbar_wait(bar, parity, err, abort_flag);
+                                            volatile int* abort_flag, unsigned long long limit_ns,
+                                            unsigned long long& acc, bool on) {
+  if (!on) return mbar_wait(bar, parity, err, abort_flag, limit_ns);
   const unsigned long long t0 = clock64();
-  const bool r = mbar_wait(bar, parity, err, abort_flag);
+  const bool r = mbar_wait(bar, parity, err, abort_flag, limit_ns);
   acc += clock64() - t0;
   return r;
 }

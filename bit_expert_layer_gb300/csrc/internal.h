@@ -17,6 +17,7 @@ struct RouteParams {
   float* topk_w;             // [T][8]
   int* hist;                 // [nblk][256] per-router-block expert histogram
   unsigned int* err;
+  unsigned long long wait_ns;  // time limit of a bounded wait
 };
 
 struct ScanParams {
@@ -59,6 +60,7 @@ struct GateUpParams {
   unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
   const __nv_bfloat16* x_ilv; // [T][2048] K-interleaved activations, gathered by token
   const int* row_dst;         // [9T] slot id (t*8+k) of each routed permuted row
+  unsigned long long wait_ns; // time limit of a bounded wait
 };
 
 struct DownParams {
@@ -71,6 +73,7 @@ struct DownParams {
   int T;
   unsigned int* err;
   unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
+  unsigned long long wait_ns; // time limit of a bounded wait
 };
 
 struct DecodeParams {
@@ -122,6 +125,9 @@ constexpr int DEC_MAX_LAYERS = 48;   // layers per launch of the fused decode ke
 constexpr size_t DEC_LT_WORDS = 2ull * 8 * 257;
 constexpr size_t DEC_HT_WORDS = 2ull * 65 * 8 * 256;
 constexpr size_t DEC_XT_WORDS = 2ull * 8 * 1024;
+constexpr int DEC_TRACE_STAMPS = 16;           // timestamps per layer and CTA
+constexpr int DEC_TRACE_CTAS = 256;            // CTAs the trace has room for
+constexpr size_t DEC_TRACE_WORDS = static_cast<size_t>(DEC_MAX_LAYERS) * DEC_TRACE_CTAS * DEC_TRACE_STAMPS;
 
 struct DecLayersParams {
   const __nv_bfloat16* x;   // [T][2048] input of the first layer
@@ -136,7 +142,32 @@ struct DecLayersParams {
   unsigned int* sync;       // [4]: [1] exit count, [2] abort flag, [3] launch epoch
   int* topk_idx;            // [T][8] routing of the last layer, or nullptr
   float* topk_w;
+  unsigned long long wait_ns;   // time limit of a bounded wait
+  unsigned long long* trace;    // phase timestamps [layer][CTA][DEC_TRACE_STAMPS], or nullptr
   DecLayer layer[DEC_MAX_LAYERS];
+};
+
+// ---- grouped-query decode attention (gqa.cu)
+constexpr int GQ_HQ = 16;        // query heads
+constexpr int GQ_HKV = 2;        // key/value heads
+constexpr int GQ_G = GQ_HQ / GQ_HKV;
+constexpr int GQ_D = 128;        // head size
+constexpr int GQ_CH = 64;        // cached positions per pipeline stage
+constexpr int GQ_STAGES = 3;
+constexpr int GQ_STAGE_BYTES = 2 * GQ_CH * GQ_D * 2;   // K and V rows of one stage
+constexpr int GQ_MAX_B = 64;     // sequences per call
+constexpr int GQ_MAX_SPLIT = 160;
+
+struct GqaParams {
+  const __nv_bfloat16* q;   // [B][16][128]
+  __nv_bfloat16* out;       // [B][16][128]
+  float* part;              // [B][16][nsplit][128 + 2]: unnormalised O, max (base 2), sum
+  unsigned* ticket;         // [B][2] splits done (the last one merges, then clears it)
+  unsigned* err;
+  int B, S_max, nsplit;
+  float scale_log2;         // log2(e) / sqrt(128)
+  unsigned long long wait_ns;
+  int lens[GQ_MAX_B];       // cached positions per sequence (1..S_max)
 };
 
 // launchers (return the first launch error)
@@ -166,7 +197,16 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const fl
                            __nv_bfloat16* out, int T, int residual, const NextLayerIn& nx, cudaStream_t s);
 cudaError_t launch_decode_router(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s);
+cudaError_t launch_gqa_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const GqaParams& p, cudaStream_t s);
+// A 2-D bf16 tensor map over rows of `cols` elements with a box of 64 x box_rows and the
+// 128-byte swizzle (false, with the failure detail recorded, if encoding fails).
+bool encode_bf16_sw128(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows);
 cudaError_t set_kernel_attributes();
+// The time limit of the bounded device waits of the next launches (moe_set_wait_limit_ns).
+unsigned long long wait_limit_ns();
+// Record the calling thread's failure description that moe_last_error_detail returns:
+// `what`, followed by the CUDA error's name when e is not cudaSuccess.
+void set_error_detail(const char* what, cudaError_t e);
 cudaError_t set_down_attributes();
 
 }  // namespace moe

@@ -8,6 +8,7 @@
 // same for the layer's shape and quantisation, and for pointer alignment.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -22,7 +23,23 @@
 namespace moe {
 cudaError_t set_router_attributes();
 cudaError_t set_gemm_attributes();
+
+namespace {
+std::atomic<unsigned long long> g_wait_ns{WAIT_LIMIT_NS};
+}
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 }  // namespace moe
+
+namespace {
+thread_local char g_detail[256] = "";
+}
+
+void moe::set_error_detail(const char* what, cudaError_t e) {
+  if (e == cudaSuccess)
+    snprintf(g_detail, sizeof g_detail, "%s", what);
+  else
+    snprintf(g_detail, sizeof g_detail, "%s: %s", what, cudaGetErrorString(e));
+}
 
 using namespace moe;
 
@@ -51,14 +68,13 @@ struct moe_layer {
   unsigned long long* dec_lt;      // fused decode: tagged logits, h', layer outputs
   unsigned long long* dec_ht;
   unsigned long long* dec_xt;
+  unsigned long long* dec_trace;   // fused decode: phase timestamps (MOE_DECODE_TRACE=1)
   unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
   CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h, tm_y, tm_hs;
 };
 
 namespace {
-
-thread_local char g_detail[256] = "";
 
 void set_detail(const char* what, cudaError_t e) {
   snprintf(g_detail, sizeof g_detail, "%s: %s", what, cudaGetErrorString(e));
@@ -102,6 +118,16 @@ cudaEvent_t prof_event() {
 bool debug_sync() {
   static const bool on = [] {
     const char* v = getenv("MOE_DEBUG_SYNC");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+// MOE_DECODE_TRACE=1 (read once): the fused decode kernel records the global timer at
+// its phase boundaries (moe_decode_trace).
+bool decode_trace() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_DECODE_TRACE");
     return v && v[0] == '1';
   }();
   return on;
@@ -214,6 +240,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->dec_lt = c.take<unsigned long long>(DEC_LT_WORDS * 8);
   d->dec_ht = c.take<unsigned long long>(DEC_HT_WORDS * 8);
   d->dec_xt = c.take<unsigned long long>(DEC_XT_WORDS * 8);
+  d->dec_trace = c.take<unsigned long long>(DEC_TRACE_WORDS * 8);
   return (c.off + 255) & ~size_t(255);
 }
 
@@ -266,6 +293,18 @@ bool encode_packed(CUtensorMap* m, const void* base, uint64_t words, uint64_t ro
                    CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
+}  // namespace
+
+bool moe::encode_bf16_sw128(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  if (!get_encode()) {
+    snprintf(g_detail, sizeof g_detail, "cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
+  return encode_bf16_rows(m, base, cols, rows, box_rows);
+}
+
+namespace {
+
 bool qmat_ok(const moe_qmat_t& q, moe_status_t* st) {
   if (!q.q || !q.scales || !q.biases) { *st = MOE_ERR_INVALID_ARG; return false; }
   if (!aligned(q.q, 16) || !aligned(q.scales, 16) || !aligned(q.biases, 16)) { *st = MOE_ERR_ALIGNMENT; return false; }
@@ -292,7 +331,8 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   const int nblk = (T + RT_BM - 1) / RT_BM;
   CUtensorMap tm_x;
   if (!encode_bf16_rows(&tm_x, x, HID, T, RT_BM)) return MOE_ERR_CUDA;
-  RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist, L->err};
+  RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist, L->err,
+                 wait_limit_ns()};
   MOE_TRY(timed(K_ROUTER, s, L->err, [&] { return launch_router_prefill(tm_x, L->tm_wr, rp, s); }), "router launch");
   ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->blocks};
   MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
@@ -382,6 +422,8 @@ moe_status_t decode_forward(moe_layer* const* layers, int n, const void* x, int 
     p.sync = L0->dec_sync;
     p.topk_idx = nullptr;
     p.topk_w = nullptr;
+    p.wait_ns = wait_limit_ns();
+    p.trace = decode_trace() ? L0->dec_trace : nullptr;
     for (int i = 0; i < cnt; ++i) p.layer[i] = dec_layer(layers[base + i]);
     MOE_TRY(timed(K_DEC_LAYERS, s, L0->err, [&] { return launch_decode_layers(p, s); }), "decode launch");
   }
@@ -426,14 +468,14 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   GateUpParams gp{L->blocks, L->offsets, L->counts,
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
-                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst};
+                  L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst, wait_limit_ns()};
   const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
   MOE_TRY(timed(K_GATEUP, s, L->err,
                 [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
           "gate/up launch");
   DownParams dp{L->blocks, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
-                pipe_trace() ? L->pipe + 16 : nullptr};
+                pipe_trace() ? L->pipe + 16 : nullptr, wait_limit_ns()};
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
@@ -660,6 +702,16 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 const char* moe_last_error_detail(void) { return g_detail; }
+
+moe_status_t moe_decode_trace(moe_layer_t* L, unsigned long long* out, size_t n_words) {
+  if (!L || !out) return MOE_ERR_INVALID_ARG;
+  if (n_words > DEC_TRACE_WORDS) n_words = DEC_TRACE_WORDS;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(out, L->dec_trace, n_words * 8, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? MOE_OK : cuda_fail("decode trace", e);
+}
+
+void moe_set_wait_limit_ns(unsigned long long ns) { g_wait_ns.store(ns ? ns : WAIT_LIMIT_NS, std::memory_order_relaxed); }
 
 moe_status_t moe_pipeline_counters(moe_layer_t* L, unsigned long long* out) {
   if (!L || !out) return MOE_ERR_INVALID_ARG;

@@ -60,7 +60,6 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_addr_mutex;
 unsigned char* g_addr[kMaxDevices] = {};
-thread_local char g_static_detail[200] = "";
 
 // The array's device address on the current device, looked up on the first call there.
 cudaError_t scratch_address(unsigned char** out) {
@@ -81,6 +80,11 @@ cudaError_t scratch_address(unsigned char** out) {
 
 bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
 
+moe_status_t fail(const char* what, cudaError_t e) {
+  set_error_detail(what, e);
+  return MOE_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -90,9 +94,11 @@ extern "C" moe_status_t moe_decode_forward_static(const moe_weights_t* w, const 
                                                   int residual, moe_stream_t stream) {
   if (!w || !x || !out) return MOE_ERR_INVALID_ARG;
   if (T < 1 || T > DEC_MAX_T) {
-    snprintf(g_static_detail, sizeof g_static_detail,
-             "moe_decode_forward_static: T=%d is outside 1..%d, the limit of its static scratch", T, DEC_MAX_T);
-    fprintf(stderr, "%s\n", g_static_detail);
+    char msg[160];
+    snprintf(msg, sizeof msg, "moe_decode_forward_static: T=%d is outside 1..%d, the limit of its static scratch", T,
+             DEC_MAX_T);
+    set_error_detail(msg, cudaSuccess);
+    fprintf(stderr, "%s\n", msg);
     return MOE_ERR_INVALID_ARG;
   }
   const moe_qmat_t* mats[6] = {&w->gate, &w->up, &w->down, &w->sh_gate, &w->sh_up, &w->sh_down};
@@ -107,11 +113,12 @@ extern "C" moe_status_t moe_decode_forward_static(const moe_weights_t* w, const 
   if (x == out && !residual) return MOE_ERR_INVALID_ARG;
 
   unsigned char* base = nullptr;
-  if (scratch_address(&base) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = scratch_address(&base);
+  if (e != cudaSuccess) return fail("moe_decode_forward_static: scratch address", e);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the error word starts at zero on every call; the tagged tables and the epoch word
-  // start at zero with the array and are left to the kernel, which keeps them valid
-  if (cudaMemsetAsync(base + kLayout.err, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the array starts at zero when the library is loaded: the error word (which collects
+  // the device errors of every call until moe_decode_static_get_error reads it), the
+  // tagged tables and the epoch word; the kernel keeps the tables and the epoch valid
 
   static DecLayersParams p;   // about 9 KB: kept off the stack, filled under the lock
   static std::mutex m;
@@ -128,6 +135,7 @@ extern "C" moe_status_t moe_decode_forward_static(const moe_weights_t* w, const 
   p.sync = reinterpret_cast<unsigned int*>(base + kLayout.sync);
   p.topk_idx = reinterpret_cast<int*>(base + kLayout.topk_idx);
   p.topk_w = reinterpret_cast<float*>(base + kLayout.topk_w);
+  p.wait_ns = wait_limit_ns();
   DecLayer& d = p.layer[0];
   d.router_w = static_cast<const __nv_bfloat16*>(w->router_w);
   d.router_bias = w->router_bias;
@@ -145,6 +153,22 @@ extern "C" moe_status_t moe_decode_forward_static(const moe_weights_t* w, const 
   Q(w->sh_up, d.suq, d.sus, d.sub);
   Q(w->sh_down, d.sdq, d.sds, d.sdb);
   d.err = reinterpret_cast<unsigned int*>(base + kLayout.err);
-  if (launch_decode_layers(p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_decode_layers(p, s);
+  if (e != cudaSuccess) return fail("moe_decode_forward_static: launch", e);
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_decode_static_get_error(void) {
+  unsigned char* base = nullptr;
+  cudaError_t e = scratch_address(&base);
+  if (e != cudaSuccess) return fail("moe_decode_static_get_error: scratch address", e);
+  unsigned int v = 0;
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail("moe_decode_static_get_error: synchronize", e);
+  if ((e = cudaMemcpy(&v, base + kLayout.err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail("moe_decode_static_get_error: read", e);
+  if ((e = cudaMemset(base + kLayout.err, 0, 4)) != cudaSuccess) return fail("moe_decode_static_get_error: clear", e);
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail("moe_decode_static_get_error: synchronize", e);
+  if (v & ERRBIT_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v & ERRBIT_BOUNDS) return MOE_ERR_DEVICE_BOUNDS;
   return MOE_OK;
 }

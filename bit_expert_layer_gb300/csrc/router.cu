@@ -66,30 +66,21 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   constexpr int NKB = HID / 64;
+  int issued = 0;   // TMA producer: K steps whose loads it issued
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_wr);
-    int issued = 0;
     for (int kb = 0; kb < NKB; ++kb) {
       const int s = kb % RT_STAGES;
       const uint32_t ph = (kb / RT_STAGES) & 1;
-      if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, abort_flag)) break;
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, abort_flag, p.wait_ns)) break;
       uint8_t* st = smem + s * RT_STAGE_BYTES;
       mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
       tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kb * 64, m0);
       tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kb * 64, 0);
       issued = kb + 1;
-    }
-    if (*abort_flag) {
-      // drain copies still in flight before the CTA's shared memory goes away
-      for (int kb = (issued > RT_STAGES ? issued - RT_STAGES : 0); kb < issued; ++kb) {
-        const int s = kb % RT_STAGES;
-        const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(full0 + 8 * s, (kb / RT_STAGES) & 1) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
-        }
-      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -97,7 +88,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     for (int kb = 0; kb < NKB; ++kb) {
       const int s = kb % RT_STAGES;
       const uint32_t ph = (kb / RT_STAGES) & 1;
-      if (!mbar_wait(full0 + 8 * s, ph, p.err, abort_flag)) break;
+      if (!mbar_wait(full0 + 8 * s, ph, p.err, abort_flag, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t a = smem_u32(smem + s * RT_STAGE_BYTES);
       const uint32_t b = a + RT_A_BYTES;
@@ -115,7 +106,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   // the other segments' lists in segment order.  Insertion is strictly-greater and the
   // candidates of equal logit arrive in ascending expert order, so ties go to the lowest
   // index exactly as in one pass over all 256 experts.
-  bool ok = mbar_wait(done, 0, p.err, abort_flag);
+  bool ok = mbar_wait(done, 0, p.err, abort_flag, p.wait_ns);
   ok = __syncthreads_and(ok && !*abort_flag) != 0;   // the merge reads every warp's list
   tc_fence_after();
   const int seg = warp >> 2, row = (warp & 3) * 32 + lane;
@@ -185,6 +176,16 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   for (int i = tid; i < NEXP; i += RT_THREADS) p.hist[blockIdx.x * NEXP + i] = hist_s[i];
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // a launch that gave up (whichever thread did): copies still in flight land before
+    // the CTA's shared memory goes away (the latest phase of each stage)
+    for (int kb = (issued > RT_STAGES ? issued - RT_STAGES : 0); kb < issued; ++kb) {
+      const int s = kb % RT_STAGES;
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(full0 + 8 * s, (kb / RT_STAGES) & 1) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     if (lane == 0 && *abort_flag) {

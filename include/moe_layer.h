@@ -88,20 +88,34 @@ typedef struct {
                                          * add the un-normalised x (the form stacked layers need). */
 } moe_weights_t;
 
-/* Bytes of device workspace a layer with this config needs (0 if the config is refused). */
+/* Bytes of device workspace a layer with this config needs (0 if the config is refused).
+ * The workspace holds the routing tables and the intermediates of the path the pages
+ * describe for prefill: the on-GPU routing state, the permuted rows and the per-expert
+ * activations between the grouped GEMMs (aimanavo.com, section "Prefill and decode are not
+ * treated as the same job").  No allocation happens inside the library. */
 size_t moe_workspace_bytes(const moe_config_t* cfg);
 
 /* Validate the config and weights and bind them to `workspace` (device, 256-byte
  * aligned, at least moe_workspace_bytes bytes, owned by the caller and kept alive as
- * long as the layer).  Weights are borrowed for the layer's lifetime.  Synchronises
- * the current device once (to initialise workspace constants).  On success *out
- * receives a layer to free with moe_layer_destroy.
+ * long as the layer).  Weights are borrowed for the layer's lifetime.  Like Lily, which
+ * checks the checkpoint's layout at load time and refuses anything else (aimanavo.com,
+ * section "Only one 4-bit checkpoint of a pinned revision runs"; news.mantis.guru,
+ * section "Rust drives the model, Metal computes"), every shape, quantisation and
+ * alignment check happens here, before any kernel runs.  Synchronises the current device
+ * once (it zeroes the workspace words that must start at zero: the error word and the
+ * decode hand-off tables).  On success *out receives a layer to free with
+ * moe_layer_destroy.
  * Errors: INVALID_ARG (NULL), UNSUPPORTED (shape), ALIGNMENT, WORKSPACE, CUDA. */
 moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weights,
                               void* workspace, size_t workspace_bytes, moe_layer_t** out);
 
 /* Routing only (router logits, softmax, top-8, renormalisation, expert histogram,
- * exclusive-scan offsets and the stable token permutation), all on the device.
+ * exclusive-scan offsets and the stable token permutation), all on the device with no
+ * host synchronisation: the 256 experts scored and 8 kept per token (aimanavo.com,
+ * section "Qwen3.6's 256 experts and two layer kinds make the MLX/Lily gap"), and the
+ * routing kept on the GPU without a per-layer CPU sync (aimanavo.com, section "Prefill
+ * and decode are not treated as the same job"; dzen.guru, section "Where the speed-up
+ * comes from").
  *   x        bf16 [T][2048]
  *   topk_idx int32 [T][8]   experts in rank order
  *   topk_w   fp32  [T][8]   renormalised weights
@@ -113,22 +127,34 @@ moe_status_t moe_route(moe_layer_t* layer, const void* x, int T, int32_t* topk_i
                        int32_t* counts, int32_t* offsets, int32_t* perm, moe_stream_t stream);
 
 /* out[T][2048] (bf16) = the layer applied to x[T][2048] (bf16).  T <= 8 takes the
- * decode path (dequant-GEMV kernels), larger T the prefill path (grouped tcgen05
- * GEMMs).  out must not overlap x.  1 <= T <= max_tokens. */
+ * decode path (a memory-bound dequant-GEMV kernel), larger T the prefill path (grouped
+ * tcgen05 GEMMs with the 4-bit weights dequantised inside the kernel): the two modes the
+ * pages keep apart (aimanavo.com, section "Prefill and decode are not treated as the same
+ * job"; news.mantis.guru, section "Prefill and decode are optimised as different modes").
+ * out must not overlap x.  1 <= T <= max_tokens.
+ * Errors: INVALID_ARG (NULL, T out of range, overlap), ALIGNMENT, CUDA (a launch failed;
+ * moe_last_error_detail says which). */
 moe_status_t moe_forward(moe_layer_t* layer, const void* x, int T, void* out, moe_stream_t stream);
 
-/* out = x + layer(x), the residual form used between stacked layers.  out == x
- * (in place) is allowed; a partial overlap is not. */
+/* out = x + layer(x), the residual form used between stacked layers of the model's
+ * 40-layer stack (aimanavo.com, section "Qwen3.6's 256 experts and two layer kinds make
+ * the MLX/Lily gap").  With norm_w set the layer computes x + MoE(RMSNorm(x)).  out == x
+ * (in place) is allowed; a partial overlap is not.  Errors as moe_forward. */
 moe_status_t moe_forward_residual(moe_layer_t* layer, const void* x, int T, void* out, moe_stream_t stream);
 
 /* x_io <- layer[n-1]( ... layer[0](x_io) ... ) with the residual add after every layer,
- * in place on the device.  All layers must share one workspace. */
+ * in place on the device.  All layers must share one workspace.  For T <= 8 the whole
+ * stack is one persistent decode launch per 48 layers: the counterpart of Lily's
+ * overlapped decode kernels (aimanavo.com, section "Prefill and decode are not treated as
+ * the same job").  Errors as moe_forward. */
 moe_status_t moe_stack_forward(moe_layer_t* const* layers, int n_layers, void* x_io, int T, moe_stream_t stream);
 
 /* The same stack from HOST memory: copies x_host (bf16 [T][2048]) into the shared
  * workspace's I/O buffer, runs the stack and copies the result to out_host, all
  * enqueued on `stream`.  With pinned host buffers the copies are asynchronous and the
- * caller must synchronise the stream before reading out_host. */
+ * caller must synchronise the stream before reading out_host.  (The pages' engine runs
+ * on unified memory, where this step does not exist; it is the end-to-end entry of this
+ * library.)  Errors as moe_forward. */
 moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, const void* x_host, int T,
                                     void* out_host, moe_stream_t stream);
 
@@ -143,15 +169,23 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
  *   weights  as for moe_layer_create (device pointers, borrowed for the call)
  *   x, out   bf16 [T][2048] device pointers; out == x is allowed only with residual
  *   residual 0: out = layer(x); 1: out = x + layer(x) (with norm_w: x + MoE(norm(x)))
- * T above 8 (the array's limit) or below 1 returns MOE_ERR_INVALID_ARG and prints why.
- * The first call on a device looks up the array's device address there (make that
- * first call before any stream capture).  Every call on a device shares the one
- * array and leaves its contents behind; the parts that must start at zero are
- * cleared by each call on its stream.  Calls that overlap on the GPU (other streams,
- * other threads) race on the array and corrupt each other: serialise them.  Device-side
- * error bits of this entry stay in the array and are not reported. */
+ * T above 8 (the array's limit) or below 1 returns MOE_ERR_INVALID_ARG and says why in
+ * moe_last_error_detail.  The first call on a device looks up the array's device address
+ * there (make that first call before any stream capture).  Every call on a device shares
+ * the one array and leaves its contents behind; the parts that must start at zero start
+ * at zero when the library is loaded and the kernel keeps them valid.  Calls that overlap
+ * on the GPU (other streams, other threads) race on the array and corrupt each other:
+ * serialise them.  Device-side errors of these calls (a bounded wait that gave up, an
+ * index out of range) collect in the array's error word until
+ * moe_decode_static_get_error reads it. */
 moe_status_t moe_decode_forward_static(const moe_weights_t* weights, const void* x, int T, void* out,
                                        int residual, moe_stream_t stream);
+
+/* Synchronise the current device, then read and clear the error word of
+ * moe_decode_forward_static's array on that device: MOE_OK if none of its calls since the
+ * last read recorded a device-side error, else MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_BOUNDS
+ * (MOE_ERR_CUDA if the synchronisation or the copy failed). */
+moe_status_t moe_decode_static_get_error(void);
 
 /* Number of kernel launches one moe_forward of T tokens on this layer enqueues
  * (for accounting); 0 for a NULL layer or T out of range. */
@@ -168,6 +202,15 @@ moe_status_t moe_layer_get_error(moe_layer_t* layer);
 
 /* Free the layer object (not the workspace or the weights, which the caller owns). */
 void moe_layer_destroy(moe_layer_t* layer);
+
+/* Time limit, in nanoseconds, of every bounded device-side wait in the launches that
+ * follow (process-wide; 0 restores the default of 2 s; below 1000, the device timer's
+ * resolution, a wait gives up as soon as it finds its data not ready).  A wait that runs out sets
+ * MOE_ERR_TIMEOUT in the error word and ends its launch early without trapping (the
+ * copies and MMAs already in flight still land before a CTA exits), so a very short
+ * limit is how the failure path is exercised on purpose.  The pages have no counterpart:
+ * Lily's Metal kernels are not described at this level. */
+void moe_set_wait_limit_ns(unsigned long long ns);
 
 /* A static string naming a status code. */
 const char* moe_status_string(moe_status_t status);
@@ -186,6 +229,19 @@ const char* moe_last_error_detail(void);
  * thread waiting for the accumulator, [9] its total; [10] tiles processed.
  * Synchronises the device, then zeroes the counters. */
 moe_status_t moe_pipeline_counters(moe_layer_t* layer, unsigned long long* out);
+
+/* Phase timestamps of the fused decode kernel (tracing; only when the environment
+ * variable MOE_DECODE_TRACE=1 is set before the first forward).  For layer l of the most
+ * recent decode launch on the workspace bound to `layer` and CTA c < 256, word
+ * (l * 256 + c) * 16 + k holds the device's global timer (ns) when CTA c passed phase
+ * boundary k: 0 layer start, 1 layer input received, 2 router rows staged, 3 router
+ * logits published, 4 all logits received, 5 expert tables built, 6 weight copies
+ * issued, 7 first gate/up batch landed, 8 gate/up done, 9 down rows staged, 10 first
+ * batch of h' received, 11 layer output published, 12 first gate/up batch computed, 13
+ * its h' published, 14 down products computed, 15 down sums reduced (phases A-C of the
+ * kernel, described in its source).  Synchronises the device and copies
+ * the first n_words words (at most 48 * 256 * 16) to out. */
+moe_status_t moe_decode_trace(moe_layer_t* layer, unsigned long long* out, size_t n_words);
 
 /* Kernel timing (tracing for benchmarks).  While enabled, every kernel this library
  * launches is bracketed by two CUDA events recorded on the launch's own stream. */

@@ -25,6 +25,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
+_SRC_GQA = os.path.join(_HERE, "gqa_oracle.c")
 _LOCK = threading.Lock()
 _LIBS: dict[int, C.CDLL] = {}
 
@@ -38,12 +39,12 @@ def build(mutant: int = 0, force: bool = False) -> str:
     """Compile the oracle (or a planted-mistake variant) with gcc; return the .so path."""
     out = lib_path(mutant)
     if not force and os.path.exists(out) and os.path.getmtime(out) >= max(
-            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "moe_oracle.h"))):
+            os.path.getmtime(_SRC), os.path.getmtime(_SRC_GQA), os.path.getmtime(os.path.join(_HERE, "moe_oracle.h"))):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
-           f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+           f"-DORACLE_MUTANT={int(mutant)}", _SRC, _SRC_GQA, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -95,6 +96,9 @@ def load(mutant: int = 0) -> C.CDLL:
                                              P, P, P, P]
         lib.oracle_token_forward_choice.argtypes = [C.POINTER(Dims), C.POINTER(Weights), P, P, C.c_int, P, P]
         lib.oracle_mutant.restype = C.c_int
+        lib.oracle_gqa_decode.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P, P, C.c_double,
+                                          C.c_int, P, P]
+        lib.oracle_gqa_decode.restype = None
         _LIBS[mutant] = lib
         return lib
 
@@ -233,6 +237,24 @@ class Oracle:
                                              _p(out), _p(w))
         return out, w
 
+    def gqa_decode(self, q, k, v, lens, scale=None, nthreads: int | None = None):
+        """Grouped-query decode attention (gqa_oracle.c): q bf16 bits [B, Hq, D], k and v
+        bf16 bits [B, Hkv, S_max, D], lens [B].  Returns (out, abs_out), float64 [B, Hq, D]."""
+        q = np.ascontiguousarray(q, np.uint16)
+        k = np.ascontiguousarray(k, np.uint16)
+        v = np.ascontiguousarray(v, np.uint16)
+        lens = np.ascontiguousarray(lens, np.int32)
+        B, Hq, D = q.shape
+        _, Hkv, S_max, _ = k.shape
+        assert k.shape == v.shape == (B, Hkv, S_max, D) and lens.shape == (B,)
+        assert Hq % Hkv == 0 and np.all(lens >= 1) and np.all(lens <= S_max)
+        out = np.zeros((B, Hq, D), np.float64)
+        aout = np.zeros((B, Hq, D), np.float64)
+        sc = 1.0 / np.sqrt(D) if scale is None else float(scale)
+        self.lib.oracle_gqa_decode(B, Hq, Hkv, D, S_max, _p(lens), _p(q), _p(k), _p(v), sc,
+                                   nthreads or default_threads(), _p(out), _p(aout))
+        return out, aout
+
     def token_forward(self, L, x_row, experts, wts, residual: bool = False) -> np.ndarray:
         """One token, experts and weights given, unrounded double output [H]."""
         x_row = np.ascontiguousarray(x_row, np.uint16)
@@ -244,21 +266,31 @@ class Oracle:
         return out
 
 
-def valid_choices(oracle: Oracle, dims, logits, tol: float = 1e-4, max_choices: int = 8):
-    """Every top-k expert set that is valid for a near-tie token, from the oracle's own
-    probabilities: the experts whose probability exceeds the k-th by more than
-    ``tol`` times the chosen mass are always in; the slots left are filled from the
-    experts within ``tol`` of the k-th, in every combination.  Returns a list of
-    sorted-by-rank expert lists (the oracle's own choice first)."""
+def valid_sets(ps, order, own, K: int, tol: float = 1e-4, max_choices: int = 8, mutant: int = 0):
+    """The top-K expert sets that count as correct for one token, from its probabilities
+    sorted in descending order (``ps``, with the expert ids ``order`` in the same order)
+    and the oracle's own choice ``own``.
+
+    The near-tie reading of the parity rule: with S the mass of the K largest
+    probabilities and p_K the K-th largest, an expert whose probability exceeds
+    p_K + tol*S must be chosen, and the slots left over may hold any experts whose
+    probability is within tol*S of p_K (both bounds inclusive).  Returns the oracle's
+    own set first, then the other such sets, at most ``max_choices`` in all.
+
+    ``mutant`` plants a mistake for the pin tests (0 = none): 1 drops the factor S from
+    the band, 2 builds the must-choose set with >= instead of >."""
     from itertools import combinations
-    idx, w, gap, ps, order = oracle.route_logits(dims, logits)
-    K = dims.top_k
+    ps = np.asarray(ps, np.float64)
     S = float(np.sum(ps[:K]))
     pk = ps[K - 1]
-    sure = [int(order[r]) for r in range(len(order)) if ps[r] > pk + tol * S]
-    band = [int(order[r]) for r in range(len(order)) if abs(ps[r] - pk) <= tol * S]
+    band_w = tol if mutant == 1 else tol * S
+    if mutant == 2:
+        sure = [int(order[r]) for r in range(len(order)) if ps[r] >= pk + band_w]
+    else:
+        sure = [int(order[r]) for r in range(len(order)) if ps[r] > pk + band_w]
+    band = [int(order[r]) for r in range(len(order)) if abs(ps[r] - pk) <= band_w]
     need = K - len(sure)
-    out = [list(idx)]
+    out = [[int(e) for e in own]]
     if need <= 0:
         return out
     for comb in combinations(band, need):
@@ -268,3 +300,11 @@ def valid_choices(oracle: Oracle, dims, logits, tol: float = 1e-4, max_choices: 
         if len(out) >= max_choices:
             break
     return out
+
+
+def valid_choices(oracle: Oracle, dims, logits, tol: float = 1e-4, max_choices: int = 8):
+    """Every top-k expert set that is valid for a near-tie token (``valid_sets``), from
+    the oracle's own routing of the token's fp32 logits.  Returns a list of expert lists
+    (the oracle's own choice first)."""
+    idx, w, gap, ps, order = oracle.route_logits(dims, logits)
+    return valid_sets(ps, order, idx, dims.top_k, tol, max_choices)

@@ -60,6 +60,12 @@ void oracle_token_forward_choice(const oracle_dims_t* d, const oracle_weights_t*
                                  const int32_t* experts, int residual, uint16_t* out, double* wts_out);
 int oracle_mutant(void);
 
+/* Grouped-query decode attention (gqa_oracle.c): q [B][Hq][D], k and v [B][Hkv][S_max][D]
+ * (bf16 bits), lens [B]; out and abs_out [B][Hq][D] (double). */
+void oracle_gqa_decode(int B, int Hq, int Hkv, int D, int S_max, const int32_t* lens, const uint16_t* q,
+                       const uint16_t* k, const uint16_t* v, double scale, int nthreads, double* out,
+                       double* abs_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,7 +42,7 @@ import numpy as np
 __all__ = [
     "Dims", "QMat", "LayerWeights", "QWEN36_DIMS",
     "bf16_bits_from_f32", "f32_from_bf16_bits",
-    "make_layer", "make_x", "make_skew_bias", "make_stack", "stack_layer",
+    "make_layer", "make_x", "make_skew_bias", "make_stack", "stack_layer", "make_gqa",
 ]
 
 # stream ids (second element of spawn_key)
@@ -194,6 +194,43 @@ def make_stack(n_layers: int, dims: Dims = QWEN36_DIMS, threads: int | None = No
 def make_x(seed: int, T: int, hidden: int = 2048) -> np.ndarray:
     """Activations x[T, hidden] as bf16 bits (uint16), N(0, 1)."""
     return bf16_bits_from_f32(_rng(seed, X_STREAM).normal(0.0, 1.0, size=(T, hidden)).astype(np.float32))
+
+
+GQA_STREAM = 0x7900
+
+
+def make_gqa(seed: int, B: int, S_max: int, lens=None, Hq: int = 16, Hkv: int = 2, D: int = 128,
+             needles: int = 4, needle_scale: float = 1.0, threads: int | None = None):
+    """Inputs of one grouped-query decode-attention step: the new query token of each of
+    B sequences and their key/value caches, as bf16 bits (uint16).
+
+    q [B, Hq, D], k and v [B, Hkv, S_max, D] ~ N(0, 1); lens [B] int32 (all S_max unless
+    given).  The pages give no law for these tensors; N(0, 1) is the plainest reading.
+    ``needles`` planted keys per (sequence, query head) copy that head's query, times
+    ``needle_scale``, into a random cached position of its KV head, so every head has a
+    few keys it attends to sharply and heads sharing a KV head attend to different
+    positions (real attention is peaked rather than uniform).  Rows at or beyond a
+    sequence's length are drawn too (the kernels must not read them)."""
+    B, S_max = int(B), int(S_max)
+    lens = np.full(B, S_max, np.int32) if lens is None else np.asarray(lens, np.int32)
+    g = Hq // Hkv
+    rq = _rng(seed, GQA_STREAM)
+    q = rq.normal(0.0, 1.0, size=(B, Hq, D)).astype(np.float32)
+    k = np.empty((B, Hkv, S_max, D), np.float32)
+    v = np.empty((B, Hkv, S_max, D), np.float32)
+
+    def fill(args):
+        b, j = args
+        r = _rng(seed, GQA_STREAM + 1 + b * Hkv + j)
+        k[b, j] = r.normal(0.0, 1.0, size=(S_max, D))
+        v[b, j] = r.normal(0.0, 1.0, size=(S_max, D))
+        if needles and lens[b] > 0:
+            pos = r.integers(0, lens[b], size=(g, needles))
+            for hh in range(g):
+                k[b, j, pos[hh]] = needle_scale * q[b, j * g + hh]
+    with ThreadPoolExecutor(threads or min(8, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, [(b, j) for b in range(B) for j in range(Hkv)]))
+    return (bf16_bits_from_f32(q), bf16_bits_from_f32(k), bf16_bits_from_f32(v), lens)
 
 
 def expected_touched(T: int, n_experts: int = 256, top_k: int = 8) -> float:

@@ -22,11 +22,15 @@ from oracle import Oracle, valid_choices
 
 GAP_TOL = 1e-4
 W_TOL = 1e-5
-# A layer with an input RMSNorm routes on bf16(x * r): the GPU's fp32 r and the oracle's
-# double r differ by ~1e-7, so about one element in 2e4 rounds to the neighbouring bf16
-# value, which moves a logit by up to 2^-8 * |x_i| * |W_r| (~1e-4) and a weight by a few
-# 1e-5; the bound keeps a decade of headroom.
-W_TOL_NORM = 1e-3
+# A layer with an input RMSNorm routes on xn = bf16(x * r * w): the GPU's fp32 r and the
+# oracle's double r differ by about 1e-7 (relative), so now and then an element of xn lands
+# on the neighbouring bf16 value.  One such element i moves every logit e by
+# delta = ulp(xn_i) * W_r[e, i], at most 2^-7 * |xn_i * W_r[e, i]|, and a renormalised
+# weight by at most delta / 4 (the softmax derivative w_k (1 - w_k) <= 1/4), i.e. at most
+# 2^-9 * |xn_i * W_r[e, i]|.  The bound below covers one such element with
+# |xn_i * W_r[e, i]| up to 0.25 (|xn_i| = 4 against a router weight of 3 standard
+# deviations); the largest difference seen over 40 stacked layers is 7.9e-5 (decode, T=8).
+W_TOL_NORM = 5e-4
 OUT_REL_TOL = 1e-2
 
 
@@ -41,7 +45,9 @@ def check_routing(o: Oracle, L, x: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.nd
     w_tol = W_TOL_NORM if getattr(L, "norm_w", None) is not None else W_TOL
     near = ref["gap"] <= GAP_TOL
     alt = {}
+    near_sets = {}
     flips = 0
+    w_err = 0.0
     for t in range(T):
         g_set = sorted(idx_gpu[t].tolist())
         if not near[t]:
@@ -57,10 +63,13 @@ def check_routing(o: Oracle, L, x: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.nd
                     assert idx_gpu[t, k] == order[k], f"token {t} rank {k}"
             wmap = dict(zip(ref["idx"][t].tolist(), ref["w"][t].tolist()))
             for k in range(K):
-                assert abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])]) <= w_tol, f"token {t} weight {k}"
+                d = abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])])
+                w_err = max(w_err, d)
+                assert d <= w_tol, f"token {t} weight {k}: |diff| {d} > {w_tol}"
         else:
             logits = o.router_logits(L, x[t])
             choices = valid_choices(o, L.dims, logits, GAP_TOL)
+            near_sets[t] = choices
             match = [c for c in choices if sorted(c) == g_set]
             assert match, f"near-tie token {t}: GPU set {g_set} not among the valid sets {choices}"
             if g_set != sorted(ref["idx"][t].tolist()):
@@ -69,8 +78,10 @@ def check_routing(o: Oracle, L, x: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.nd
             else:
                 wmap = dict(zip(ref["idx"][t].tolist(), ref["w"][t].tolist()))
                 for k in range(K):
-                    assert abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])]) <= w_tol
-    return dict(tokens=T, near_ties=int(near.sum()), flips=flips), alt
+                    d = abs(w_gpu[t, k] - wmap[int(idx_gpu[t, k])])
+                    w_err = max(w_err, d)
+                    assert d <= w_tol, f"token {t} weight {k}: |diff| {d} > {w_tol}"
+    return dict(tokens=T, near_ties=int(near.sum()), flips=flips, w_err=w_err, near_sets=near_sets), alt
 
 
 def check_tables(idx_gpu: np.ndarray, counts, offsets, perm, n_experts=256):
@@ -83,10 +94,18 @@ def check_tables(idx_gpu: np.ndarray, counts, offsets, perm, n_experts=256):
 
 
 def check_output(o: Oracle, L, x: np.ndarray, out_gpu: np.ndarray, tokens=None, residual=False, alt=None,
-                 ref_out=None):
+                 ref_out=None, any_of=None):
     """Compares out_gpu (bf16 bits [T, H]) on `tokens` with the oracle.  Returns
-    (max abs error, max abs oracle)."""
+    (max abs error, max abs oracle).
+
+    ``alt``: token -> the valid expert set the GPU chose (from the routing check).
+    ``any_of``: token -> every valid expert set of a near-tie token, for outputs whose
+    routing was computed by a different kernel than the one the routing check read (the
+    decode forward and the decode router sum the logits in different orders, so on a
+    near tie they may pick different valid sets): such a token matches the closest of
+    the oracle's outputs for those sets."""
     alt = alt or {}
+    any_of = any_of or {}
     T = x.shape[0]
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     if ref_out is None:
@@ -97,6 +116,15 @@ def check_output(o: Oracle, L, x: np.ndarray, out_gpu: np.ndarray, tokens=None, 
             ob, _ = o.token_forward_choice(L, x[t], alt[int(t)], residual=residual)
             ref[i] = bf16_to_f64(ob)
     got = bf16_to_f64(out_gpu[tokens])
+    for i, t in enumerate(tokens):
+        if int(t) in any_of:
+            best = None
+            for c in any_of[int(t)]:
+                ob, _ = o.token_forward_choice(L, x[t], c, residual=residual)
+                cand = bf16_to_f64(ob)
+                if best is None or np.max(np.abs(got[i] - cand)) < np.max(np.abs(got[i] - best)):
+                    best = cand
+            ref[i] = best
     err = float(np.max(np.abs(got - ref)))
     scale = float(np.max(np.abs(ref)))
     assert np.all(np.isfinite(got)), "non-finite GPU output"

@@ -1,5 +1,6 @@
 """The C-ABI library loads on a machine without a GPU and exports every entry point
-that include/moe_layer.h declares; host-side validation runs before any CUDA call."""
+that include/moe_layer.h and include/gqa_decode.h declare; host-side validation runs
+before any CUDA call."""
 import ctypes as C
 
 import pytest
@@ -17,6 +18,7 @@ def lib():
 def test_every_declared_symbol_is_exported(lib):
     names = _abi.declared_functions()
     assert "moe_forward" in names and "moe_route" in names and "moe_layer_create" in names
+    assert "gqa_decode_attention" in names and "moe_set_wait_limit_ns" in names
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, missing
 
@@ -81,3 +83,20 @@ def test_status_strings(lib):
     for code in _abi.STATUS:
         assert _abi.moe_status_string(code)
     assert _abi.moe_status_string(99) == "unknown status"
+
+
+def test_gqa_host_checks(lib):
+    """Sizes and pointers are checked on the host before anything reaches the device."""
+    assert _abi.gqa_decode_workspace_bytes(0) == 0 and _abi.gqa_decode_workspace_bytes(65) == 0
+    a, b = _abi.gqa_decode_workspace_bytes(1), _abi.gqa_decode_workspace_bytes(8)
+    assert a > 0 and b > a
+    fake = 1 << 20   # never dereferenced: every call below fails its host check first
+    for args, st in [((fake, fake, fake, [4], 0, 8, fake, fake, b), _abi.MOE_ERR_INVALID_ARG),
+                     ((fake, fake, fake, [9], 1, 8, fake, fake, b), _abi.MOE_ERR_INVALID_ARG),
+                     ((fake, fake, fake, [0], 1, 8, fake, fake, b), _abi.MOE_ERR_INVALID_ARG),
+                     ((fake + 2, fake, fake, [4], 1, 8, fake, fake, b), _abi.MOE_ERR_ALIGNMENT),
+                     ((fake, fake, fake, [4], 1, 8, fake, fake + 16, b), _abi.MOE_ERR_ALIGNMENT),
+                     ((fake, fake, fake, [4], 1, 8, fake, fake, a - 1), _abi.MOE_ERR_WORKSPACE)]:
+        with pytest.raises(_abi.MoEError) as ei:
+            _abi.gqa_decode_attention(*args)
+        assert ei.value.status == st, (args, ei.value.status)

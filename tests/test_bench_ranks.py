@@ -104,3 +104,22 @@ def test_kernel_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.kernel_hash() == h0
     p.write_text(p.read_text() + "constexpr int UNUSED_FOR_TEST = 1;\n")
     assert bench.kernel_hash() != h0
+
+
+def test_gpus_flag_starts_the_ranks():
+    """``bench.py --gpus 2`` without a launcher starts two ranks itself and one JSON line
+    comes out, from rank 0, with n_gpus 2 (the reference arm: no GPU needed)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR",
+                                                             "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--workload", "layer-T32", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2

@@ -61,7 +61,9 @@ def full_check(oracle, L, layer, x, residual=False, sample=None):
     out, r = run(layer, x, residual)
     rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
     check_tables(r["idx"], r["counts"], r["offsets"], r["perm"])
-    err, scale = check_output(oracle, L, x, out, tokens=sample, residual=residual, alt=alt)
+    # at T <= 8 the router entry and the fused decode forward are different kernels
+    any_of = rep["near_sets"] if x.shape[0] <= 8 else None
+    err, scale = check_output(oracle, L, x, out, tokens=sample, residual=residual, alt=alt, any_of=any_of)
     return rep, err, scale
 
 
@@ -86,9 +88,7 @@ def test_ragged_sweep(oracle, host0, dev0, T):
 
 def test_prefill_T512(oracle, host0, dev0):
     x = synth.make_x(0, 512)
-    rng = np.random.default_rng(512)
-    sample = np.unique(np.concatenate([rng.choice(512, 120, replace=False), np.arange(504, 512)]))
-    rep, err, scale = full_check(oracle, host0, dev0, x, sample=sample)
+    rep, err, scale = full_check(oracle, host0, dev0, x)   # every token
     print(f"T=512 {rep} max_err={err:.3e} scale={scale:.3e}")
 
 
@@ -102,7 +102,7 @@ def test_skewed_T4096(oracle, lib):
     counts = r["counts"]
     heavy = np.argsort(-counts)[:3]
     rng = np.random.default_rng(4096)
-    sample = set(rng.choice(4096, 64, replace=False).tolist()) | set(range(4088, 4096))
+    sample = set(rng.choice(4096, 512, replace=False).tolist()) | set(range(4088, 4096))
     for e in heavy:   # tokens from the heaviest experts' last (ragged) tiles
         slots = r["perm"][r["offsets"][e]:r["offsets"][e + 1]]
         sample |= set((slots[-4:] // 8).tolist())
@@ -128,9 +128,7 @@ def test_all_tokens_on_one_expert_set(oracle, lib):
     assert set(np.unique(r["idx"]).tolist()) == set(chosen)
     assert all(r["counts"][e] == 600 for e in chosen)
     rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
-    rng = np.random.default_rng(600)
-    sample = np.unique(np.concatenate([rng.choice(600, 60, replace=False), np.arange(590, 600)]))
-    check_output(oracle, L, x, out, tokens=sample, alt=alt)
+    check_output(oracle, L, x, out, alt=alt)   # every token
 
 
 @pytest.mark.parametrize("T", [1, 8, 40])
@@ -159,7 +157,8 @@ def test_residual_in_place(oracle, host0, dev0, T):
     out = to_host(x)
     r = dev0.route(to_dev(x_np))
     rep, alt = check_routing(oracle, host0, x_np, r["idx"].cpu().numpy(), r["w"].cpu().numpy())
-    check_output(oracle, host0, x_np, out, residual=True, alt=alt)
+    any_of = rep["near_sets"] if T <= 8 else None
+    check_output(oracle, host0, x_np, out, residual=True, alt=alt, any_of=any_of)
 
 
 def test_deterministic(host0, dev0):

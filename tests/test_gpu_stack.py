@@ -1,12 +1,16 @@
 """The stacked form of the layer on the GPU against the oracle: a single layer with its
 input RMSNorm, and the full 40-layer stack (18.2 GB of 4-bit weights) at T=16384
-prefill and T=1 decode, in the launch configuration the benchmark times (one shared
-workspace, in-place residual through moe_stack_forward).
+prefill and T=8 / T=1 decode, in the launch configuration the benchmark times (one
+shared workspace, in-place residual through moe_stack_forward).
 
-Tokens never interact, so the oracle follows a sample of tokens through all 40 layers
-on its own bf16 outputs.  A token whose routing is within 1e-4 of a tie at any layer of
-the oracle's chain is left out of the comparison (its later layers depend on which
-valid choice was made); the test asks that most sampled tokens stay comparable.
+The stack is checked teacher-forced, layer by layer: the layers are also run one at a
+time through the device entry (whose final result must equal the stack entry's bit for
+bit), and at every one of the 40 layers the oracle receives the GPU's own input to that
+layer for a sample of tokens.  Each layer is then held to the single-layer bounds
+(routing exact or a valid near-tie choice, output within 1e-2 of the oracle's largest
+magnitude), so a routing choice that an earlier layer's rounding moved across a narrow
+gap never carries into a later comparison.  A chained comparison (the oracle following
+its own outputs through all 40 layers) stays as a secondary check.
 """
 from __future__ import annotations
 
@@ -50,14 +54,15 @@ def test_layer_with_input_norm(oracle, lib, T):
     assert layer.get_error() == 0
     rep, alt = check_routing(oracle, L, x_np, r["idx"].cpu().numpy(), r["w"].cpu().numpy())
     check_output(oracle, L, x_np, to_host(out), residual=True, alt=alt)
+    print(f"norm layer T={T}: {rep}")
 
 
 def stack_tolerance(scale: float, n_layers: int) -> float:
-    """Output bound after n chained layers.  Each layer's output is the layer tolerance
-    (1e-2 of the scale) away at most, and the residual stream is rounded to bf16 once per
-    layer: where the two sides' unrounded sums straddle a rounding boundary they land one
-    bf16 unit apart, and such one-unit steps add up like a random walk over the layers,
-    about sqrt(n) units of the largest magnitude."""
+    """Bound of the secondary, chained comparison after n layers.  Each layer's output is
+    the layer tolerance (1e-2 of the scale) away at most, and the residual stream is
+    rounded to bf16 once per layer: where the two sides' unrounded sums straddle a
+    rounding boundary they land one bf16 unit apart, and such one-unit steps add up like
+    a random walk over the layers, about sqrt(n) units of the largest magnitude."""
     ulp = 2.0 ** (np.floor(np.log2(scale)) - 7)
     return 1e-2 * scale + np.sqrt(n_layers) * ulp
 
@@ -72,16 +77,55 @@ def _stack_chain(oracle, hosts, x_np):
     return cur, keep
 
 
-def test_full_stack_40_layers(oracle, lib):
+def _teacher_forced(oracle, lib, hosts, layers, x_np, sample, label):
+    """Runs the layers one by one through the device entry on the whole input, keeps each
+    layer's input, output and routing on the sampled tokens, and checks every layer
+    against the oracle on the GPU's own input.  Returns the final device output (all
+    tokens) and the per-layer (max error, scale) list."""
+    cur = to_dev(x_np)
+    per_layer = []
+    near_total = flips_total = 0
+    w_err = 0.0
+    for l, (h, layer) in enumerate(zip(hosts, layers)):
+        inp = to_host(cur)[sample]
+        r = layer.route(cur)
+        nxt = layer.forward(cur, residual=True)
+        torch.cuda.synchronize()
+        assert layer.get_error() == 0, f"{label} layer {l}: device error"
+        idx = r["idx"].cpu().numpy()[sample]
+        w = r["w"].cpu().numpy()[sample]
+        out = to_host(nxt)[sample]
+        rep, alt = check_routing(oracle, h, inp, idx, w)
+        # decode: the router entry and the fused forward are different kernels
+        any_of = rep["near_sets"] if x_np.shape[0] <= 8 else None
+        err, scale = check_output(oracle, h, inp, out, residual=True, alt=alt, any_of=any_of)
+        per_layer.append((err, scale))
+        near_total += rep["near_ties"]
+        flips_total += rep["flips"]
+        w_err = max(w_err, rep["w_err"])
+        cur = nxt
+    worst = max(e / s for e, s in per_layer)
+    print(f"{label}: {len(sample)} tokens x {len(hosts)} layers teacher-forced; near-ties {near_total}, "
+          f"flips {flips_total}, max weight diff {w_err:.2e}, worst layer err/scale {worst:.3e}")
+    print(f"{label} per-layer max err / scale: " +
+          " ".join(f"{l}:{e:.3g}/{s:.3g}" for l, (e, s) in enumerate(per_layer)))
+    return cur, per_layer
+
+
+@pytest.fixture(scope="module")
+def stack40(lib):
     from concurrent.futures import ThreadPoolExecutor
     with ThreadPoolExecutor(4) as ex:
         hosts = list(ex.map(lambda l: synth.stack_layer(l, threads=2), range(40)))
     T = 16384
     ws = lib.new_workspace(T)
     layers = [lib.MoELayer(lib.DeviceWeights(h), T, workspace=ws) for h in hosts]
-    stack = lib.MoEStack(layers)
+    return hosts, layers, lib.MoEStack(layers)
 
-    # prefill T=16384
+
+def test_full_stack_40_layers_prefill(oracle, lib, stack40):
+    hosts, layers, stack = stack40
+    T = 16384
     x_np = synth.make_x(0, T)
     x = to_dev(x_np)
     stack.forward_(x)
@@ -89,33 +133,49 @@ def test_full_stack_40_layers(oracle, lib):
     assert layers[0].get_error() == 0
     got = to_host(x)
     assert np.all(np.isfinite(bf16_to_f64(got)))
+
+    # teacher-forced, every layer, on 72 tokens (64 random, the first and last 4)
     rng = np.random.default_rng(40)
-    sample = np.unique(np.concatenate([rng.choice(T, 110, replace=False), [0, T - 1]]))
-    ref, keep = _stack_chain(oracle, hosts, x_np[sample])
+    sample = np.unique(np.concatenate([rng.choice(T, 64, replace=False), [0, 1, 2, 3, T - 4, T - 3, T - 2, T - 1]]))
+    final, per_layer = _teacher_forced(oracle, lib, hosts, layers, x_np, sample, "stack prefill T=16384")
+    # the stack entry is the layer-by-layer computation, bit for bit
+    assert torch.equal(final.view(torch.int16), x.view(torch.int16))
+
+    # secondary: the oracle chained on its own outputs through all 40 layers
+    sample2 = np.unique(np.concatenate([rng.choice(T, 110, replace=False), [0, T - 1]]))
+    ref, keep = _stack_chain(oracle, hosts, x_np[sample2])
     # about 3% of tokens sit within 1e-4 of a routing tie at each layer, so roughly
     # 0.97^40 = 30% of tokens stay comparable through all 40 layers
     assert keep.sum() >= 12, keep.sum()
     ref_v = bf16_to_f64(ref[keep])
-    err = np.max(np.abs(bf16_to_f64(got[sample][keep]) - ref_v))
-    assert err <= stack_tolerance(np.max(np.abs(ref_v)), len(hosts)), (err, np.max(np.abs(ref_v)))
-    print(f"stack prefill: {int(keep.sum())}/{len(sample)} sampled tokens compared, max err {err:.3e}, "
-          f"scale {np.max(np.abs(ref_v)):.3e}")
-
-    # decode T=1 through the same stack
-    xd_np = synth.make_x(1, 1)
-    xd = to_dev(xd_np)
-    stack.forward_(xd)
-    torch.cuda.synchronize()
-    assert layers[0].get_error() == 0
-    ref, keep = _stack_chain(oracle, hosts, xd_np)
-    if keep[0]:
-        r_v, g_v = bf16_to_f64(ref[0]), bf16_to_f64(to_host(xd)[0])
-        assert np.max(np.abs(g_v - r_v)) <= stack_tolerance(np.max(np.abs(r_v)), len(hosts))
+    err = np.max(np.abs(bf16_to_f64(got[sample2][keep]) - ref_v))
+    scale = np.max(np.abs(ref_v))
+    bound = stack_tolerance(scale, len(hosts))
+    assert err <= bound, (err, scale)
+    ulp = 2.0 ** (np.floor(np.log2(scale)) - 7)
+    print(f"stack prefill chained: {int(keep.sum())}/{len(sample2)} tokens compared, max err {err:.3e} "
+          f"= {err / ulp:.2f} bf16 units at scale {scale:.3e}; 1e-2 * scale = {1e-2 * scale:.3e}, "
+          f"sqrt(40) units = {np.sqrt(40) * ulp:.3e}")
 
     # the first layer alone, routing tables exact on the full T
     r = layers[0].route(to_dev(x_np))
     sub = np.arange(0, T, 64)
     idx = r["idx"].cpu().numpy()
-    rep, _ = check_routing(oracle, hosts[0], x_np[sub], idx[sub], r["w"].cpu().numpy()[sub])
+    check_routing(oracle, hosts[0], x_np[sub], idx[sub], r["w"].cpu().numpy()[sub])
     counts = r["counts"].cpu().numpy()
     assert counts.sum() == 8 * T and np.array_equal(counts, np.bincount(idx.reshape(-1), minlength=256))
+
+
+@pytest.mark.parametrize("T", [8, 1])
+def test_full_stack_40_layers_decode(oracle, lib, stack40, T):
+    """The fused decode kernel (one launch runs all 40 layers) against the layers run one
+    at a time (bit for bit), and every layer teacher-forced against the oracle; no token
+    is left out."""
+    hosts, layers, stack = stack40
+    x_np = synth.make_x(1, T)
+    x = to_dev(x_np)
+    stack.forward_(x)
+    torch.cuda.synchronize()
+    assert layers[0].get_error() == 0
+    final, _ = _teacher_forced(oracle, lib, hosts, layers, x_np, np.arange(T), f"stack decode T={T}")
+    assert torch.equal(final.view(torch.int16), x.view(torch.int16))
