@@ -64,6 +64,9 @@ WORKLOADS = {
     "layer-T32": dict(layers=1, T_prefill=32, T_decode=0, skew=False),
     "decode-T1": dict(layers=40, T_prefill=0, T_decode=1, skew=False),
     "decode-T8": dict(layers=40, T_prefill=0, T_decode=8, skew=False),
+    # grouped-query decode attention alone (the full-attention layers' decode step)
+    "gqa-decode-ctx4K-B8": dict(layers=0, T_prefill=0, T_decode=0, skew=False, gqa=(8, 4096)),
+    "gqa-decode-ctx32K-B8": dict(layers=0, T_prefill=0, T_decode=0, skew=False, gqa=(8, 32768)),
 }
 DEFAULT_WORKLOAD = "stack40-T16384+T1"
 
@@ -391,6 +394,62 @@ def cpu_baseline(hosts, wl, n_layers):
                 cpu=cpu_model())
 
 
+def run_gqa(args, wl):
+    """Grouped-query decode attention alone: one call per step over B sequences of S cached
+    positions (16 query heads, 2 KV heads, head 128), CUDA events around each call on the
+    launching stream, the KV cache (B * 2 * S * 512 bytes) read from HBM every step."""
+    import torch
+
+    import synth
+    from bit_expert_layer_gb300 import _abi
+    from bit_expert_layer_gb300.build import build
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    B, S = wl["gqa"]
+    q, k, v, lens = synth.make_gqa(7, B, S)
+    dv = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    qd, kd, vd = dv(q), dv(k), dv(v)
+    od = torch.empty_like(qd)
+    nws = _abi.gqa_decode_workspace_bytes(B)
+    ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+    lens_l = [int(x) for x in lens]
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    call = lambda: _abi.gqa_decode_attention(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), lens_l, B, S, od.data_ptr(),
+                                             ws.data_ptr(), nws, stream.cuda_stream)
+    for _ in range(args.warmup):
+        call()
+        flush.zero_()
+    torch.cuda.synchronize(dev)
+    evs = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        flush.zero_()
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    assert _abi.gqa_decode_get_error(ws.data_ptr()) == 0
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    peaks = load_peaks()
+    nb = B * 2 * S * 128 * 2 * 2 + 2 * B * 16 * 128 * 2
+    gbs = nb / (ms / 1e3) / 1e9
+    line = dict(metric="GQA decode attention, µs per step", value=1e3 * ms, unit="us/step", n_gpus=1,
+                steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=False, scaling="weak",
+                vs_baseline=None, dtype="bf16", data="synthetic",
+                config=dict(workload=args.workload, B=B, S=S, heads="16 query / 2 KV, head 128",
+                            l2="256 MB L2 flush between steps (outside the events)"),
+                roofline=dict(kernel="gqa_decode", bound="hbm", achieved=gbs, peak=peaks["hbm"], unit="GB/s",
+                              frac=gbs / peaks["hbm"], traffic=None,
+                              algorithmic=f"K and V rows read once: {nb} B per step"),
+                gpu_launches=args.steps)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -636,6 +695,12 @@ def main(argv=None):
     wl = WORKLOADS[args.workload]
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         return spawn_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv))
+    if "gqa" in wl:
+        if args.impl == "reference":
+            print(json.dumps(dict(impl="reference", unavailable="the attention workloads have no CPU-timed arm; "
+                                                                "the default workload carries it")))
+            return 0
+        return run_gqa(args, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -162,23 +162,22 @@ constexpr unsigned long long WAIT_LIMIT_IMMEDIATE_NS = 1000ull;
 
 // Wait for the phase of parity `parity` to complete.  Gives up after limit_ns (or as
 // soon as another thread of the CTA has given up, via *abort): records ERRBIT_TIMEOUT in
-// the device error word and returns false.  Never hangs.
+// the device error word and returns false.  Never hangs.  Under a limit below the timer's
+// resolution the thread is not suspended at all: the wait gives up unless the phase is
+// already complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err,
                                           volatile int* abort_flag, unsigned long long limit_ns) {
-  if (limit_ns < WAIT_LIMIT_IMMEDIATE_NS) {
-    if (mbar_test_wait(bar, parity)) return true;
-    atomicOr(err, ERRBIT_TIMEOUT);
-    *abort_flag = 1;
-    return false;
-  }
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool imm = limit_ns < WAIT_LIMIT_IMMEDIATE_NS;
+  if (imm ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
+    if (!imm) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
+      for (int i = 0; i < 32; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+      if (*abort_flag) return false;
+    }
+    if (imm || globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, ERRBIT_TIMEOUT);
       *abort_flag = 1;
       return false;
@@ -215,6 +214,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The same store with an L2 eviction-priority policy (from l2_policy_*).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                                  uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "l"(policy)
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -7,20 +7,23 @@
 // cooperative launch, and no launch gap or grid-wide barrier sits between them.
 //
 // One CTA per SM (cooperative launch: all CTAs are resident, so they may wait on one
-// another), 16 warps.  Per layer:
+// another): 16 compute warps and 4 copy warps.  Per layer:
 //   phase A  every CTA reads the layer input x, forms its RMSNorm (when the layer has
 //            one) in shared memory, and computes its share of the 256 router logits and
 //            the shared-expert gate logit (8 warps split the 2048 inputs of one row).
 //   phase B  every CTA repeats the top-8 selection from the logits (the same result in
 //            every CTA), builds the list of active experts (the routed ones in id order,
-//            the shared expert last) with a per-token weight column, and computes
-//            gate/up units: 8 features x (gate row, up row) of one active expert, an
-//            m16n8k16 tile whose two row halves are the gate and the up rows of the same
-//            features, so SwiGLU needs no exchange.  The 16 warps split K; fixed-order
-//            reduction; h' = weight * silu(g) * u.
-//   phase C  16 output rows per CTA: the weighted h' columns of every active expert are
-//            accumulated in one MMA accumulator (the combine over the 8 routed + 1
-//            shared experts), fixed-order reduction over 16 warps, residual, bf16 out.
+//            the shared expert last) with a per-token weight column and token mask, and
+//            computes its gate/up units: 8 features x (gate row, up row) of one active
+//            expert, an m16n8k16 tile whose two row halves are the gate and the up rows
+//            of the same features, so SwiGLU needs no exchange.  Two units per round, the
+//            16 warps splitting K; a fixed-order reduction gives h' = weight * silu(g) * u,
+//            published only for the tokens that chose the expert (h' is zero otherwise).
+//   phase C  16 output rows per CTA (128 CTAs): the weighted h' columns of every active
+//            expert, four experts per job, accumulate in one MMA accumulator per warp
+//            (four warps split the K of one expert: the combine over the 8 routed + 1
+//            shared experts), a fixed-order reduction over the 16 warps, residual, bf16
+//            out.  Only the nonzero h' rows are fetched.
 //
 // Hand-off between CTAs without barriers: every value one CTA passes to another (the
 // layer output x, the logits, h') travels as a 64-bit word {32-bit payload, 32-bit tag}
@@ -30,16 +33,25 @@
 // on, one L2 round trip, instead of a grid barrier followed by a read.  The tables are
 // double-buffered by layer parity: a producer can be at most one layer ahead of the
 // slowest consumer of the same buffer, because every layer's phase B needs all logits,
-// its phase C all of h', and its phase A all of x.
+// its phase C all of h', and its phase A all of x.  Each publishing thread issues at most
+// one such word per phase (a thread's exchanges would otherwise wait on one another).
 //
-// Weights move into shared memory by cp.async: 16-byte pieces, consecutive threads on
-// consecutive pieces of a contiguous block (8 KB of gate or up rows, 4 KB of down rows),
-// which streams at the HBM rate, where per-copy costs make small bulk-engine copies slow.
-// Each CTA's gate/up units come in two batches in flight; its router rows and the norm
-// weights of the next layer are copied during phase C, its 16 down rows of the active
-// experts (up to DL_STAGE routed ones) during phase B.  Completion is counted on
-// mbarriers (one cp.async arrival per thread).  Every wait (tags, copies) gives up after
-// a time limit (error bit, abort flag shared by all CTAs).
+// Weights stream through one ring of NSLOT shared-memory slots of 18 KB: a job is one
+// gate/up unit (8 KB of gate rows, 8 KB of up rows, their scales and biases) or the down
+// rows of four experts for the CTA's 16 output rows (4 KB each, with scales and biases).
+// The four copy warps queue the CTA's job list as soon as the routing is known -- its
+// gate/up units, then (once the first round of units has landed) its down rows -- each
+// into a slot the compute warps have released (full / empty mbarriers per slot), so the
+// weights stream while the compute warps work.  Copies are 16-byte cp.async (consecutive
+// threads on consecutive pieces of a contiguous block, which streams at the HBM rate,
+// where per-copy costs make small bulk-engine copies slow), counted on the slot's
+// mbarrier; one copy warp alone issues too slowly to keep up, four do.  The 16-byte chunks
+// of every weight row are stored XOR-swizzled by the row (chunk c of row r at c ^ (r & 7)),
+// so the MMA fragments' loads, eight rows at a time, hit distinct banks.  The copy warps
+// also fetch the next layer's router rows and norm weights.  The compute warps synchronise
+// on a named barrier of their own; the copy warps hand their registers to them
+// (setmaxnreg).  Every wait (tags, copies, slots) gives up after a time limit (error bit,
+// abort flags shared by the CTA's warps and by all CTAs).
 #include "common.cuh"
 #include "decode_tag.h"
 #include "gemm_common.cuh"
@@ -51,36 +63,43 @@ namespace moe {
 
 namespace {
 
-constexpr int DL_THREADS = 512;
+constexpr int DL_THREADS = 512;                // compute threads (16 warps)
 constexpr int DL_WARPS = DL_THREADS / 32;
+constexpr int DL_COPY = 128;                   // copy threads (4 warps) that stream the weights
+constexpr int DL_BLOCK = DL_THREADS + DL_COPY;
+// Registers per thread after the split (setmaxnreg): the copy warpgroup hands registers to
+// the four compute warpgroups.  The split needs DL_BLOCK * (registers at launch) >= its sum;
+// the host checks that before the first launch.
+constexpr int DL_REGS_COMPUTE = 104;
+constexpr int DL_REGS_COPY = 32;
+constexpr int DL_REGS_SPLIT = DL_THREADS * DL_REGS_COMPUTE + DL_COPY * DL_REGS_COPY;   // 57,344
 constexpr int DL_ROWS_C = 16;                 // output rows per CTA in phase C
 constexpr int DL_CTAS_C = HID / DL_ROWS_C;    // 128 CTAs carry phase C
-constexpr int DL_STAGE = 18;                  // routed experts whose down rows are staged in shared memory
 constexpr int NROW_A = NEXP + 1;              // router rows + the shared-expert gate row
 constexpr unsigned DL_POLL_NS = 100;          // pause between polls of a stale tagged word
-constexpr int DQ_WORDS = DL_ROWS_C * INTER / 8;        // 1024 words = 4 KB of packed down rows
-constexpr int DQ_GROUPS = DL_ROWS_C * INTER / GROUP;   // 128 scales (or biases) = 256 B
-// gate/up unit in shared memory: 8 gate rows, 8 up rows (1 KB each), then the scales
-// and biases of both (8 x 32 bf16 each)
+// gate/up unit in a slot: 8 gate rows, 8 up rows (1 KB each), then the scales and biases of
+// both (8 x 32 bf16 each)
 constexpr int U_ROWB = HID / 2;                        // 1024 bytes of packed codes per row
 constexpr int U_SC = 16 * U_ROWB;                      // 16384: gate scales, gate biases, up scales, up biases
-constexpr int U_BYTES = U_SC + 4 * 8 * (HID / GROUP) * 2;   // 18432
-constexpr int DL_UB = 2;                               // units per batch; two batches in flight
-constexpr int HS_ROWS = 2 * DL_UB * U_BYTES / (INTER * 2);  // 72 rows of h' (1 KB) in the same space
+constexpr int SLOT_BYTES = U_SC + 4 * 8 * (HID / GROUP) * 2;   // 18432
+constexpr int NSLOT = 8;                               // weight ring depth
+constexpr int UNITS_PER_ROUND = 2;                     // gate/up units computed together
+// down rows of one expert in a slot: 16 rows x 256 bytes of codes, then 16 x 8 scales and biases
+constexpr int DQ_WORDS = DL_ROWS_C * INTER / 8;        // 1024 words = 4 KB
+constexpr int DQ_GROUPS = DL_ROWS_C * INTER / GROUP;   // 128 scales (or biases) = 256 B
+constexpr int C_EXP_BYTES = DQ_WORDS * 4 + 2 * DQ_GROUPS * 2;   // 4608
+constexpr int C_EXP_PER_JOB = SLOT_BYTES / C_EXP_BYTES;         // 4
 
 struct alignas(16) DlShared {
-  uint8_t gu[2 * DL_UB][U_BYTES];               // phase B: staged units; phase C: h' rows
-  __nv_bfloat16 xn[DEC_MAX_T][HID];             // normalised layer input (natural order)
-  float red[DL_UB][DL_WARPS][32][4];            // K-split partials
-  uint32_t dq[DL_STAGE][DQ_WORDS];              // staged down rows of routed experts
-  uint16_t dsc[DL_STAGE][DQ_GROUPS];
-  uint16_t dbi[DL_STAGE][DQ_GROUPS];
-  uint32_t sdq[DQ_WORDS];                       // staged down rows of the shared expert
-  uint16_t sdsc[DQ_GROUPS];
-  uint16_t sdbi[DQ_GROUPS];
+  uint8_t ring[NSLOT][SLOT_BYTES];              // weight jobs
+  __nv_bfloat16 xn[DEC_MAX_T][HID];             // normalised layer input (natural order); in
+                                                // phase C the h' rows of one down job
+  float red[2][UNITS_PER_ROUND][DL_WARPS][32][4];   // K-split partials of a round (by round parity)
   __nv_bfloat16 rrow[2][HID];                   // this CTA's router rows
   __nv_bfloat16 normw[HID];                     // the layer's norm weights
-  uint64_t mb_a, mb_c, mb_b[2];                 // bulk-copy barriers
+  uint64_t mb_a;                                // router rows / norm weights of the layer landed
+  uint64_t mb_full[NSLOT], mb_empty[NSLOT];     // weight slots: landed / released by the 16 compute warps
+  uint64_t mb_route;                            // the layer's routing tables are built
   float xres[DEC_MAX_T][DL_ROWS_C];             // residual inputs of this CTA's output rows
   float ssp[DEC_MAX_T][8];                      // sum-of-squares partials
   float inv_rms[DEC_MAX_T];
@@ -91,11 +110,18 @@ struct alignas(16) DlShared {
   uint32_t mask[NEXP / 32];                     // experts routed by any token
   int act_e[DEC_MAX_ACTIVE];
   float act_w[DEC_MAX_ACTIVE][DEC_MAX_T];
+  uint8_t tmask[DEC_MAX_ACTIVE];                // tokens routed to each active expert
+  uint8_t rowbase[DEC_MAX_ACTIVE + 1];          // first compact h' row of each active expert
+  uint16_t rowinfo[DEC_MAX_T * (TOPK + 1)];     // compact h' row -> active expert * 8 + token
   int n_active;
   int abort;
   int last;                                     // this CTA is the last one out of the launch
 };
-static_assert(HS_ROWS >= DEC_MAX_T * 9, "h' staging must hold one batch of 9 experts at T = 8");
+static_assert(C_EXP_PER_JOB * 4 == DL_WARPS, "four experts per down job, four warps per expert");
+static_assert(UNITS_PER_ROUND % 2 == 0, "units are computed in pairs");
+constexpr int HS_ROWS = DEC_MAX_T * HID * 2 / (INTER * 2);   // 32 h' rows (1 KB) fit in the xn buffer
+static_assert(C_EXP_PER_JOB * DEC_MAX_T <= HS_ROWS, "the h' rows of one down job fit in the xn buffer");
+static_assert(NSLOT >= 2 * UNITS_PER_ROUND, "two rounds of units in flight");
 static_assert(DEC_MAX_LAYERS <= (1 << DEC_TAG_LAYER_BITS), "a tag holds the layer in its low bits");
 static_assert(sizeof(DlShared) <= 232448, "shared memory per CTA exceeds 227 KB");
 static_assert(DEC_LT_WORDS == 2ull * DEC_MAX_T * NROW_A && DEC_HT_WORDS == 2ull * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2) &&
@@ -138,10 +164,6 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
 // (the barrier counts one arrival per thread of the CTA).
 __device__ __forceinline__ void cp_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void cta_copy(void* dst, const void* src, int bytes) {
-  for (int i = threadIdx.x * 16; i < bytes; i += DL_THREADS * 16)
-    cp16(static_cast<uint8_t*>(dst) + i, static_cast<const uint8_t*>(src) + i);
 }
 
 // ---- tagged words
@@ -201,75 +223,172 @@ __device__ __forceinline__ float kfloat(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// bounded wait on one of this CTA's bulk-copy barriers, the same outcome in every thread
+// Barriers of the 16 compute warps (named barrier 1; the copy warps never join them).
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(DL_THREADS) : "memory"); }
+__device__ __forceinline__ bool cbar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(DL_THREADS)
+      : "memory");
+  return r != 0;
+}
+
+// Barrier of the copy warps (named barrier 2), with an AND of their votes.
+__device__ __forceinline__ bool copy_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(DL_COPY)
+      : "memory");
+  return r != 0;
+}
+
+// bounded wait of the compute warps on one of this CTA's copy barriers, the same outcome
+// in every compute thread
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, const Ctx& cx, DlShared& s) {
   bool ok = mbar_wait(smem_u32(bar), parity, cx.err, &s.abort, cx.limit);
   if (!ok) atomicExch(cx.abort_word, 1u);
-  return __syncthreads_and(ok) != 0;
+  return cbar_and(ok);
 }
 
 // ---------------------------------------------------------------- staging (all threads)
-// Phase A's inputs of layer L: this CTA's router rows and the norm weights.
+// Phase A's inputs of layer L (copy warps): this CTA's router rows and the norm weights.
 __device__ void issue_stage_a(const DecLayer& L, DlShared& s) {
-  const int c = blockIdx.x, G = gridDim.x;
-  for (int sl = 0; sl < 2; ++sl) {
-    const int r = c + sl * G;
-    if (r < NROW_A) cta_copy(s.rrow[sl], r < NEXP ? L.router_w + static_cast<size_t>(r) * HID : L.shared_gate_w, HID * 2);
+  const int c = blockIdx.x, G = gridDim.x, ct = threadIdx.x - DL_THREADS;
+  constexpr int RP = HID * 2 / 16;   // 256 pieces per row
+  for (int k = ct; k < 3 * RP; k += DL_COPY) {
+    const int part = k / RP, off = (k % RP) * 16;
+    if (part < 2) {
+      const int r = c + part * G;
+      if (r < NROW_A)
+        cp16(reinterpret_cast<uint8_t*>(s.rrow[part]) + off,
+             reinterpret_cast<const uint8_t*>(r < NEXP ? L.router_w + static_cast<size_t>(r) * HID : L.shared_gate_w) + off);
+    } else if (L.norm_w) {
+      cp16(reinterpret_cast<uint8_t*>(s.normw) + off, reinterpret_cast<const uint8_t*>(L.norm_w) + off);
+    }
   }
-  if (L.norm_w) cta_copy(s.normw, L.norm_w, HID * 2);
   cp_arrive(&s.mb_a);
 }
 
-// Phase C's weights of layer L for this CTA's 16 output rows: the down rows of the
-// shared expert and of the first DL_STAGE routed experts into shared memory (phase C
-// reads the rows of any further routed experts from memory).
-__device__ void issue_stage_c(const DecLayer& L, DlShared& s) {
-  const int c = blockIdx.x, tid = threadIdx.x;
-  if (c >= DL_CTAS_C) return;
-  const int n_routed = s.n_active - 1;
-  const int n_st = n_routed < DL_STAGE ? n_routed : DL_STAGE;
-  constexpr int PIECES = (DQ_WORDS * 4 + 2 * DQ_GROUPS * 2) / 16;   // 288 per expert
-  for (int k = tid; k < (n_st + 1) * PIECES; k += DL_THREADS) {
-    const int i = k / PIECES, off = k % PIECES;
-    const bool sh = i == n_st;
-    const size_t r0 = (sh ? 0 : static_cast<size_t>(s.act_e[i]) * HID) + static_cast<size_t>(c) * DL_ROWS_C;
-    if (off < DQ_WORDS / 4) {
-      cp16((sh ? s.sdq : s.dq[i]) + off * 4, (sh ? L.sdq : L.dq) + r0 * (INTER / 8) + off * 4);
-    } else if (off < DQ_WORDS / 4 + DQ_GROUPS / 8) {
-      const int o = (off - DQ_WORDS / 4) * 8;
-      cp16((sh ? s.sdsc : s.dsc[i]) + o, (sh ? L.sds : L.ds) + r0 * (INTER / GROUP) + o);
-    } else {
-      const int o = (off - DQ_WORDS / 4 - DQ_GROUPS / 8) * 8;
-      cp16((sh ? s.sdbi : s.dbi[i]) + o, (sh ? L.sdb : L.db) + r0 * (INTER / GROUP) + o);
-    }
-  }
-  cp_arrive(&s.mb_c);
+// This CTA's weight jobs of a layer: n_units gate/up units (unit blockIdx.x + i * G of
+// the layer's n_active * 64), then (phase-C CTAs) ceil(n_active / 4) jobs of down rows.
+struct Jobs {
+  int nb;      // gate/up units of this CTA
+  int nc;      // down jobs of this CTA
+  int n;       // nb + nc
+  uint32_t j0; // ring position of the layer's first job
+};
+
+__device__ __forceinline__ Jobs layer_jobs(const DlShared& s, uint32_t j0) {
+  const int G = gridDim.x;
+  const int n_units = s.n_active * (INTER / 8);
+  Jobs J;
+  J.nb = blockIdx.x < n_units ? (n_units - 1 - static_cast<int>(blockIdx.x)) / G + 1 : 0;
+  J.nc = blockIdx.x < DL_CTAS_C ? (s.n_active + C_EXP_PER_JOB - 1) / C_EXP_PER_JOB : 0;
+  J.n = J.nb + J.nc;
+  J.j0 = j0;
+  return J;
 }
 
-// Gate/up batch b of this CTA (units blockIdx.x + (DL_UB*b + j) * G) into buffer b & 1:
-// per unit 8 KB of gate rows, 8 KB of up rows, 4 x 512 B of scales and biases.
-__device__ void issue_units(const DecLayer& L, DlShared& s, int b, int n_units) {
-  const int tid = threadIdx.x, G = gridDim.x, buf = b & 1;
-  constexpr int SB = 8 * (HID / GROUP) * 2;   // 512 B of scales (or biases) for 8 rows
-  for (int j = 0; j < DL_UB; ++j) {
-    const int u = blockIdx.x + (DL_UB * b + j) * G;
-    if (u >= n_units) break;
+// Copy job j (copy warps): its 16-byte pieces into slot (j0 + j) % NSLOT, chunk c of row r
+// at c ^ (r & 7), then one arrival per copy thread on the slot's barrier.
+__device__ void issue_job(const DecLayer& L, DlShared& s, const Jobs& J, int j) {
+  const int ct = threadIdx.x - DL_THREADS, G = gridDim.x;
+  const int slot = static_cast<int>((J.j0 + j) % NSLOT);
+  uint8_t* dst = s.ring[slot];
+  if (j < J.nb) {
+    const int u = blockIdx.x + j * G;
     const int a = u / (INTER / 8), f0 = (u % (INTER / 8)) * 8;
     const int e = s.act_e[a];
     const bool sh = e == NEXP;
     const size_t row = (sh ? 0 : static_cast<size_t>(e) * INTER) + f0;
-    uint8_t* dst = s.gu[buf * DL_UB + j];
-    static_assert(8 * U_ROWB == DL_THREADS * 16, "one 16-byte piece of each 8-row block per thread");
-    cp16(dst + tid * 16, reinterpret_cast<const uint8_t*>((sh ? L.sgq : L.gq) + row * (HID / 8)) + tid * 16);
-    cp16(dst + 8 * U_ROWB + tid * 16, reinterpret_cast<const uint8_t*>((sh ? L.suq : L.uq) + row * (HID / 8)) + tid * 16);
-    if (tid < 4 * SB / 16) {
-      const int part = tid / (SB / 16), o = (tid % (SB / 16)) * 16;
-      const uint16_t* src = part == 0 ? (sh ? L.sgs : L.gs) : part == 1 ? (sh ? L.sgb : L.gb)
-                          : part == 2 ? (sh ? L.sus : L.us) : (sh ? L.sub : L.ub);
-      cp16(dst + U_SC + part * SB + o, reinterpret_cast<const uint8_t*>(src + row * (HID / GROUP)) + o);
+    const uint8_t* gsrc = reinterpret_cast<const uint8_t*>((sh ? L.sgq : L.gq) + row * (HID / 8));
+    const uint8_t* usrc = reinterpret_cast<const uint8_t*>((sh ? L.suq : L.uq) + row * (HID / 8));
+    constexpr int RP = 8 * U_ROWB / 16;         // 512 pieces of 8 rows
+    constexpr int SB = 8 * (HID / GROUP) * 2;   // 512 B of scales (or biases) for 8 rows
+    for (int k = ct; k < 2 * RP + 4 * SB / 16; k += DL_COPY) {
+      if (k < 2 * RP) {
+        const int m = k / RP, q = k % RP;        // matrix (gate, up), piece
+        const int r = q >> 6, c = q & 63;        // row r of the 8, chunk c of its 64
+        cp16(dst + m * 8 * U_ROWB + r * U_ROWB + ((c ^ (r & 7)) << 4), (m ? usrc : gsrc) + q * 16);
+      } else {
+        const int q = k - 2 * RP;
+        const int part = q / (SB / 16), o = (q % (SB / 16)) * 16;
+        const uint16_t* src = part == 0 ? (sh ? L.sgs : L.gs) : part == 1 ? (sh ? L.sgb : L.gb)
+                            : part == 2 ? (sh ? L.sus : L.us) : (sh ? L.sub : L.ub);
+        cp16(dst + U_SC + part * SB + o, reinterpret_cast<const uint8_t*>(src + row * (HID / GROUP)) + o);
+      }
+    }
+  } else {
+    const int a0 = (j - J.nb) * C_EXP_PER_JOB;
+    const int ne = min(C_EXP_PER_JOB, s.n_active - a0);
+    constexpr int PIECES = C_EXP_BYTES / 16;   // 288 per expert
+    for (int k = ct; k < ne * PIECES; k += DL_COPY) {
+      const int i = k / PIECES, off = k % PIECES;
+      const int e = s.act_e[a0 + i];
+      const bool sh = e == NEXP;
+      const size_t r0 = (sh ? 0 : static_cast<size_t>(e) * HID) + static_cast<size_t>(blockIdx.x) * DL_ROWS_C;
+      uint8_t* d = dst + i * C_EXP_BYTES;
+      if (off < DQ_WORDS / 4) {                 // codes: 16 rows x 16 chunks
+        const int r = off >> 4, c = off & 15;
+        cp16(d + r * (INTER / 2) + ((c ^ (r & 7)) << 4),
+             reinterpret_cast<const uint8_t*>((sh ? L.sdq : L.dq) + r0 * (INTER / 8)) + off * 16);
+      } else if (off < DQ_WORDS / 4 + DQ_GROUPS / 8) {
+        const int o = (off - DQ_WORDS / 4) * 8;
+        cp16(d + DQ_WORDS * 4 + o * 2, (sh ? L.sds : L.ds) + r0 * (INTER / GROUP) + o);
+      } else {
+        const int o = (off - DQ_WORDS / 4 - DQ_GROUPS / 8) * 8;
+        cp16(d + DQ_WORDS * 4 + DQ_GROUPS * 2 + o * 2, (sh ? L.sdb : L.db) + r0 * (INTER / GROUP) + o);
+      }
     }
   }
-  cp_arrive(&s.mb_b[buf]);
+  cp_arrive(&s.mb_full[slot]);
+}
+
+// The copy warps' work for one layer: every job of this CTA in order, each into a slot the
+// compute warps have released, then the next layer's phase-A inputs.  False if a wait gave up.
+__device__ bool copy_layer(const DecLayersParams& p, int l, const Ctx& cx, DlShared& s, const Jobs& J) {
+  for (int j = 0; j < J.n; ++j) {
+    const uint32_t q = J.j0 + static_cast<uint32_t>(j);
+    const uint32_t q0 = J.j0 + static_cast<uint32_t>(min(J.nb, UNITS_PER_ROUND) - 1);
+    if (j == J.nb && J.nb > 0 && q0 + NSLOT >= J.j0 + static_cast<uint32_t>(J.nb)) {
+      // the down rows are needed only after every gate/up unit: let the first round of
+      // units land before their copies compete for the memory bandwidth (when the first
+      // round's last slot has been reused already, that round has long landed)
+      if (!copy_bar_and(mbar_wait(smem_u32(&s.mb_full[q0 % NSLOT]), (q0 / NSLOT) & 1, cx.err, &s.abort, cx.limit)))
+        return false;
+    }
+    // the slot's previous job has been released (its first use needs no wait)
+    if (!copy_bar_and(mbar_wait(smem_u32(&s.mb_empty[q % NSLOT]), ((q / NSLOT) & 1) ^ 1, cx.err, &s.abort,
+                                cx.limit)))
+      return false;
+    issue_job(p.layer[l], s, J, j);
+  }
+  if (l + 1 < p.n_layers) issue_stage_a(p.layer[l + 1], s);
+  return true;
+}
+
+// This thread's bounded wait for job j's data (no barrier: the caller's next compute barrier
+// makes the outcome uniform); a give-up raises the grid's abort flag.
+__device__ __forceinline__ bool wait_job(const Jobs& J, int j, const Ctx& cx, DlShared& s) {
+  const uint32_t q = J.j0 + static_cast<uint32_t>(j);
+  const bool ok = mbar_wait(smem_u32(&s.mb_full[q % NSLOT]), (q / NSLOT) & 1, cx.err, &s.abort, cx.limit);
+  if (!ok) atomicExch(cx.abort_word, 1u);
+  return ok;
+}
+// this warp is done with job j's slot (16 arrivals free it for the copy warps)
+__device__ __forceinline__ void release_job(const Jobs& J, int j, DlShared& s) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&s.mb_empty[(J.j0 + static_cast<uint32_t>(j)) % NSLOT]));
 }
 
 // ---------------------------------------------------------------- phase A
@@ -330,7 +449,7 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
                               static_cast<uint32_t>(e[i][2]), static_cast<uint32_t>(e[i][3]))
                  : make_uint4(0, 0, 0, 0);
   }
-  if (!__syncthreads_and(ok)) return false;
+  if (!cbar_and(ok)) return false;
   stamp(cx, 1);
   // residual inputs of this CTA's phase-C rows (chunks 2c, 2c+1 of every token)
   if (p.residual && c < DL_CTAS_C) {
@@ -365,14 +484,14 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
       for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       if (lane == 0 && t < T) s.ssp[t][warp & 7] = ss;
     }
-    __syncthreads();
+    cbar();
     if (tid < T) {
       float ss = 0.0f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) ss += s.ssp[tid][j];
       s.inv_rms[tid] = 1.0f / sqrtf(ss / static_cast<float>(HID) + 1e-6f);
     }
-    __syncthreads();
+    cbar();
   }
 #pragma unroll
   for (int i = 0; i < CH_PER_THREAD; ++i) {
@@ -392,7 +511,7 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
     }
     *reinterpret_cast<uint4*>(&s.xn[t][k]) = o;
   }
-  __syncthreads();
+  cbar();
 
   // router rows: 8 warps per row, each 256 inputs (8 per lane)
   const int slot = warp >> 3, ks = (warp & 7) * 256 + lane * 8;
@@ -420,14 +539,16 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
   }
 #pragma unroll
   for (int t = 0; t < DEC_MAX_T; ++t) {
+    if (t < T) {   // uniform
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+      for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+    }
   }
   if (lane == 0) {
 #pragma unroll
     for (int t = 0; t < DEC_MAX_T; ++t) s.rpart[warp][t] = acc[t];
   }
-  __syncthreads();
+  cbar();
   if (tid < 2 * DEC_MAX_T) {
     const int sl = tid / DEC_MAX_T, t = tid % DEC_MAX_T;
     const int rr = c + sl * G;
@@ -453,6 +574,7 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
   const int T = p.T;
   for (int i = tid; i < DEC_MAX_ACTIVE * DEC_MAX_T; i += DL_THREADS) (&s.act_w[0][0])[i] = 0.0f;
   if (tid < NEXP / 32) s.mask[tid] = 0u;
+  if (tid < DEC_MAX_ACTIVE) s.tmask[tid] = 0;
   bool ok = true;
   if (warp < T) {
     const int t = warp;
@@ -520,13 +642,13 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
       }
     }
   }
-  if (!__syncthreads_and(ok)) return false;
+  if (!cbar_and(ok)) return false;
   stamp(cx, 4);
   if (tid < T * TOPK) {
     const int e = s.idx[tid / TOPK][tid % TOPK];
     atomicOr(&s.mask[e >> 5], 1u << (e & 31));
   }
-  __syncthreads();
+  cbar();
   // position of expert e in the active list = number of routed ids below it
   auto pos = [&](int e) {
     int n = __popc(s.mask[e >> 5] & ((1u << (e & 31)) - 1u));
@@ -534,8 +656,11 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
     return n;
   };
   if (tid < T * TOPK) {
+    // weight column and token mask of the active expert (the shared one's are set below)
     const int t = tid / TOPK, e = s.idx[t][tid % TOPK];
-    s.act_w[pos(e)][t] = s.w[t][tid % TOPK];
+    const int a = pos(e);
+    s.act_w[a][t] = s.w[t][tid % TOPK];
+    atomicOr(reinterpret_cast<unsigned*>(&s.tmask[0]) + (a >> 2), (1u << t) << (8 * (a & 3)));
   } else if (tid >= DL_THREADS - NEXP) {
     const int e = tid - (DL_THREADS - NEXP);
     if ((s.mask[e >> 5] >> (e & 31)) & 1u) s.act_e[pos(e)] = e;
@@ -547,98 +672,117 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
     if (tid == 0) {
       s.act_e[n] = NEXP;
       s.n_active = n + 1;
+      atomicOr(reinterpret_cast<unsigned*>(&s.tmask[0]) + (n >> 2), ((1u << T) - 1u) << (8 * (n & 3)));
     }
     if (tid < T) s.act_w[n][tid] = s.sig[tid];
   }
-  __syncthreads();
+  cbar();
   stamp(cx, 5);
   return true;
 }
 
+// Gate/up units, four per round (warp quarter wg = warp / 4 takes unit 4r + wg of the round,
+// its four warps split K into quarters of 512); the K partials are reduced in a fixed order
+// and h' = weight * silu(g) * u is published as tagged words.
 __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int l, const Ctx& cx, DlShared& s,
-                               uint32_t (&bphase)[2]) {
+                               const Jobs& J) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c4 = lane & 3;
   const int T = p.T, G = gridDim.x;
   const int kbase = warp * (HID / DL_WARPS);           // 128 inputs per warp
-  const int wo = kbase / 8 + 4 * c4;                   // word offset in a gate/up row
-  const int gi = (kbase + 32 * c4) / GROUP;            // quantisation group
-  const int n_units = s.n_active * (INTER / 8);
-  const int my_units = blockIdx.x < n_units ? (n_units - 1 - blockIdx.x) / G + 1 : 0;
-  const int nb = (my_units + DL_UB - 1) / DL_UB;
-  for (int b = 0; b < 2 && b < nb; ++b) issue_units(L, s, b, n_units);
-  issue_stage_c(L, s);   // phase C's copies queue behind the first batches
-  stamp(cx, 6);
+  const int ch = kbase / 32 + c4;                      // this lane's 16-byte chunk of a row
+  const int gi = (kbase + 32 * c4) / GROUP;            // its quantisation group
+  unsigned long long* ht = p.ht + static_cast<size_t>(l & 1) * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2);
   // B fragments (token g, this lane's 32 inputs), the same for every unit
   uint4 xb[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    xb[j] = make_uint4(0, 0, 0, 0);
-    if (g < T) xb[j] = interleave8(*reinterpret_cast<const uint4*>(&s.xn[g][kbase + 32 * c4 + 8 * j]));
+  for (int k = 0; k < 4; ++k) {
+    xb[k] = make_uint4(0, 0, 0, 0);
+    if (g < T) xb[k] = interleave8(*reinterpret_cast<const uint4*>(&s.xn[g][kbase + 32 * c4 + 8 * k]));
   }
-  unsigned long long* ht = p.ht + static_cast<size_t>(l & 1) * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2);
-  for (int b = 0; b < nb; ++b) {
-    const int buf = b & 1;
-    if (!cta_wait(&s.mb_b[buf], bphase[buf] & 1, cx, s)) return false;
-    ++bphase[buf];
-    if (b == 0) stamp(cx, 7);
+  const int nr = (J.nb + UNITS_PER_ROUND - 1) / UNITS_PER_ROUND;
+  for (int r = 0; r < nr; ++r) {
+    const int jlo = r * UNITS_PER_ROUND, jhi = min(J.nb, jlo + UNITS_PER_ROUND);
+    bool ok = true;
+    for (int jj = jlo; jj < jhi && ok; ++jj) ok = wait_job(J, jj, cx, s);
+    ok = __all_sync(0xffffffffu, ok);   // the warp computes together or not at all
+    if (r == 0) stamp(cx, 7);
+    float (*red)[DL_WARPS][32][4] = s.red[r & 1];
+    // every warp: its 128 inputs of each unit of the round, two units at a time with their
+    // MMAs interleaved (two independent accumulator chains)
 #pragma unroll
-    for (int j = 0; j < DL_UB; ++j) {
-      const int u = blockIdx.x + (DL_UB * b + j) * G;
-      if (u >= n_units) break;
-      const uint8_t* U = s.gu[buf * DL_UB + j];
-      const uint4 wg = *reinterpret_cast<const uint4*>(U + g * U_ROWB + wo * 4);
-      const uint4 wu = *reinterpret_cast<const uint4*>(U + (8 + g) * U_ROWB + wo * 4);
-      const uint16_t* sc = reinterpret_cast<const uint16_t*>(U + U_SC);
-      const __nv_bfloat162 mg = bf2h(sc[g * 32 + gi]), ag = bf2h(sc[256 + g * 32 + gi]);
-      const __nv_bfloat162 mu = bf2h(sc[512 + g * 32 + gi]), au = bf2h(sc[768 + g * 32 + gi]);
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t gw[4] = {wg.x, wg.y, wg.z, wg.w};
-      const uint32_t uw[4] = {wu.x, wu.y, wu.z, wu.w};
+    for (int u2 = 0; u2 < UNITS_PER_ROUND; u2 += 2) {
+      if (!ok || jlo + u2 >= jhi) break;
+      const bool two = jlo + u2 + 1 < jhi;                 // uniform
+      uint32_t gw[2][4], uw[2][4];
+      __nv_bfloat162 mg[2], ag[2], mu[2], au[2];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const uint8_t* U = s.ring[(J.j0 + jlo + u2 + (two ? v : 0)) % NSLOT];
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(U + U_SC);
+        const uint4 wgt = *reinterpret_cast<const uint4*>(U + g * U_ROWB + ((ch ^ g) << 4));
+        const uint4 wup = *reinterpret_cast<const uint4*>(U + (8 + g) * U_ROWB + ((ch ^ g) << 4));
+        gw[v][0] = wgt.x; gw[v][1] = wgt.y; gw[v][2] = wgt.z; gw[v][3] = wgt.w;
+        uw[v][0] = wup.x; uw[v][1] = wup.y; uw[v][2] = wup.z; uw[v][3] = wup.w;
+        mg[v] = bf2h(sc[g * 32 + gi]);
+        ag[v] = bf2h(sc[256 + g * 32 + gi]);
+        mu[v] = bf2h(sc[512 + g * 32 + gi]);
+        au[v] = bf2h(sc[768 + g * 32 + gi]);
+      }
+      float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint4 o0 = dequant8(gw[k], mg, ag), o1 = dequant8(uw[k], mu, au);
-        mma16816(d, o0.x, o1.x, o0.y, o1.y, xb[k].x, xb[k].y);
-        mma16816(d, o0.z, o1.z, o0.w, o1.w, xb[k].z, xb[k].w);
-      }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) s.red[j][warp][lane][k] = d[k];
-    }
-    if (b == 0) stamp(cx, 12);
-    __syncthreads();
-    if (b + 2 < nb) issue_units(L, s, b + 2, n_units);   // buffer b & 1 is free
-    if (tid < DL_UB * 32) {
-      const int j = tid >> 5, ln = tid & 31;
-      const int u = blockIdx.x + (DL_UB * b + j) * G;   // warp-uniform
-      if (u < n_units) {
-        float q[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < DL_WARPS; ++w)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) q[k] += s.red[j][w][ln][k];
-        // q[0], q[1]: gate of feature f0 + ln/4 for tokens 2(ln%4), 2(ln%4)+1; q[2], q[3]: up
-        const int a = u / (INTER / 8), fi = ln >> 2, t0 = 2 * (ln & 3);
-        float hv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float gv = q[h], uv = q[2 + h];
-          hv[h] = gv / (1.0f + __expf(-gv)) * uv * s.act_w[a][t0 + h];
-        }
-        // interleaved pair (2i, 2i+1) of the unit holds features (i, i + 4)
-        const float h0 = __shfl_down_sync(0xffffffffu, hv[0], 16);
-        const float h1 = __shfl_down_sync(0xffffffffu, hv[1], 16);
-        if (fi < 4) {
-          const size_t pair = (u % (INTER / 8)) * 4 + fi;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            if (t0 + h < T)
-              st_tagged(ht + (static_cast<size_t>(a) * DEC_MAX_T + t0 + h) * (INTER / 2) + pair,
-                        pack_bf16x2(hv[h], h ? h1 : h0), cx.tag);
+        for (int v = 0; v < 2; ++v) {
+          const uint4 o0 = dequant8(gw[v][k], mg[v], ag[v]), o1 = dequant8(uw[v][k], mu[v], au[v]);
+          mma16816(d[v], o0.x, o1.x, o0.y, o1.y, xb[k].x, xb[k].y);
+          mma16816(d[v], o0.z, o1.z, o0.w, o1.w, xb[k].z, xb[k].w);
         }
       }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) red[u2][warp][lane][k] = d[0][k];
+      if (two) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) red[u2 + 1][warp][lane][k] = d[1][k];
+      }
     }
-    if (b == 0) stamp(cx, 13);
-    __syncthreads();
+    for (int jj = jlo; jj < jhi; ++jj) release_job(J, jj, s);
+    if (r == 0) stamp(cx, 12);
+    // one barrier per round: every warp's partials are written (and every wait succeeded);
+    // the partials are double-buffered by round parity, so the next round's writes cannot
+    // meet this round's reduction
+    if (!cbar_and(ok)) return false;
+    // warp ui reduces unit ui of the round in a fixed order (the next round's partials are
+    // written only after its copy wait, which every thread reaches after this)
+    if (warp < UNITS_PER_ROUND && jlo + warp < jhi) {
+      const int u = blockIdx.x + (jlo + warp) * G;
+      float q[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < DL_WARPS; ++w)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] += red[warp][w][lane][k];
+      // q[0], q[1]: gate of feature f0 + lane/4 for tokens 2(lane%4), 2(lane%4)+1; q[2], q[3]: up
+      const int a = u / (INTER / 8), fi = lane >> 2, t0 = 2 * (lane & 3);
+      float hv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float gv = q[h], uv = q[2 + h];
+        hv[h] = gv / (1.0f + __expf(-gv)) * uv * s.act_w[a][t0 + h];
+      }
+      // interleaved pair (2i, 2i+1) of the unit holds features (i, i + 4): lanes 0-15 (features
+      // 0-3) publish token t0, lanes 16-31 (features 4-7) token t0 + 1, one word each, and
+      // only for tokens that chose the expert
+      const float other0 = __shfl_down_sync(0xffffffffu, hv[0], 16);   // for lanes 0-15
+      const float other1 = __shfl_up_sync(0xffffffffu, hv[1], 16);     // for lanes 16-31
+      const bool lo = fi < 4;
+      const int t = lo ? t0 : t0 + 1;
+      if (t < T && ((s.tmask[a] >> t) & 1u)) {
+        const size_t pair = (u % (INTER / 8)) * 4 + (fi & 3);
+        st_tagged(ht + (static_cast<size_t>(a) * DEC_MAX_T + t) * (INTER / 2) + pair,
+                  lo ? pack_bf16x2(hv[0], other0) : pack_bf16x2(other1, hv[1]), cx.tag);
+      }
+    }
+    if (r == 0) stamp(cx, 13);
   }
   stamp(cx, 8);
   return true;
@@ -658,35 +802,66 @@ __device__ __forceinline__ void down_mma(float (&d)[4], uint4 w0, uint4 w1, uint
   }
 }
 
-__device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, const Ctx& cx, DlShared& s) {
+// Down rows, four experts per job: warp quarter wg takes expert 4i + wg of job i, its four
+// warps split K (512) into quarters; every warp keeps its accumulator across the jobs, and
+// the 16 warps' partials are reduced once, in a fixed order.
+__device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, const Ctx& cx, DlShared& s,
+                        const Jobs& J) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c4 = lane & 3;
-  const int ks = warp & 3, eq = warp >> 2;
+  const int wg = warp >> 2, kq = warp & 3;
   const int T = p.T;
   if (blockIdx.x >= DL_CTAS_C) return true;            // uniform per CTA
+  // compact h' rows of each active expert (the shared expert: every token): h' is zero for a
+  // token that did not choose the expert, so those rows are neither published nor read
+  if (warp == 0) {
+    // exclusive scan of the token counts over the (at most 65) active experts, 32 at a time
+    const int n = s.n_active;
+    int carry = 0;
+    for (int a0 = 0; a0 < n; a0 += 32) {
+      const int a = a0 + lane;
+      const uint32_t tm = a < n ? s.tmask[a] : 0u;
+      const int c = __popc(tm);
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (a < n) {
+        const int base = carry + incl - c;
+        s.rowbase[a] = static_cast<uint8_t>(base);
+        int k = base;
+        for (int t = 0; t < T; ++t)
+          if ((tm >> t) & 1u) s.rowinfo[k++] = static_cast<uint16_t>(a * DEC_MAX_T + t);
+        if (a == n - 1) s.rowbase[n] = static_cast<uint8_t>(base + c);
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  cbar();
   const int r0 = blockIdx.x * DL_ROWS_C + g, r1 = r0 + 8;
-  const int n_act = s.n_active, n_routed = n_act - 1;
-  const int n_st = n_routed < DL_STAGE ? n_routed : DL_STAGE;
-  const int wo = ks * 16 + 4 * c4;                     // word offset in a down row (64 words)
-  const int gi = (ks * 128 + 32 * c4) / GROUP;         // quantisation group (8 per row)
   const unsigned long long* ht = p.ht + static_cast<size_t>(l & 1) * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2);
-  uint32_t* hs = reinterpret_cast<uint32_t*>(&s.gu[0][0]);   // h' rows [expert-in-batch * T + t][256 pairs]
-  if (!cta_wait(&s.mb_c, l & 1, cx, s)) return false;
-  stamp(cx, 9);
+  uint32_t* hs = reinterpret_cast<uint32_t*>(&s.xn[0][0]);   // h' rows [expert in job * T + t][256 pairs]
+  const int ch = kq * 4 + c4;                         // this lane's 16-byte chunk of a down row
+  const int gi = (kq * 128 + 32 * c4) / GROUP;        // its quantisation group (8 per row)
   float d[4] = {0.f, 0.f, 0.f, 0.f};
-  const int eb = HS_ROWS / T;                          // experts per batch
-  for (int a0 = 0; a0 < n_act; a0 += eb) {
-    const int na = n_act - a0 < eb ? n_act - a0 : eb;
-    // h' of experts a0 .. a0+na-1, tokens < T, from the tagged table into shared memory
-    const int n_pairs = na * T * (INTER / 2);
+  const int n_act = s.n_active;
+  int i = 0;
+  while (i < J.nc) {
+    // a batch of jobs whose compact h' rows (only tokens that chose the expert) fit in hs
+    const int lo = s.rowbase[i * C_EXP_PER_JOB];
+    int i2 = i + 1;
+    while (i2 < J.nc && s.rowbase[min((i2 + 1) * C_EXP_PER_JOB, n_act)] - lo <= HS_ROWS) ++i2;
+    const int n_pairs = (s.rowbase[min(i2 * C_EXP_PER_JOB, n_act)] - lo) * (INTER / 2);
     bool ok = true;
     constexpr int PG = 4;   // pieces of 2 words per thread polled together
     for (int g0 = 2 * tid; g0 < n_pairs && ok; g0 += PG * 2 * DL_THREADS) {
       unsigned long long w[PG][2];
       auto src = [&](int k) {
-        const int i0 = g0 + k * 2 * DL_THREADS;
-        const int row = i0 / (INTER / 2), pr = i0 % (INTER / 2);
-        return ht + (static_cast<size_t>(a0 + row / T) * DEC_MAX_T + row % T) * (INTER / 2) + pr;
+        const int q0 = g0 + k * 2 * DL_THREADS;
+        const int ri = s.rowinfo[lo + q0 / (INTER / 2)], pr = q0 % (INTER / 2);
+        return ht + static_cast<size_t>(ri) * (INTER / 2) + pr;   // ri = active expert * 8 + token
       };
 #pragma unroll
       for (int k = 0; k < PG; ++k)
@@ -706,77 +881,64 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
       }
 #pragma unroll
       for (int k = 0; k < PG; ++k) {
-        const int i0 = g0 + k * 2 * DL_THREADS;
-        if (i0 < n_pairs)
-          *reinterpret_cast<uint2*>(hs + i0) = make_uint2(static_cast<uint32_t>(w[k][0]), static_cast<uint32_t>(w[k][1]));
+        const int q0 = g0 + k * 2 * DL_THREADS;
+        if (q0 < n_pairs)
+          *reinterpret_cast<uint2*>(hs + q0) = make_uint2(static_cast<uint32_t>(w[k][0]), static_cast<uint32_t>(w[k][1]));
       }
     }
-    if (!__syncthreads_and(ok)) return false;
-    if (a0 == 0) stamp(cx, 10);
-    for (int ai = eq; ai < na; ai += 4) {
-      const int a = a0 + ai;
-      uint4 hb[4];
+    if (!cbar_and(ok)) return false;
+    if (i == 0) stamp(cx, 10);
+    // the batch's jobs, each as soon as its data is in; one barrier at the end of the batch
+    bool okc = true;
+    if (i == 0) stamp(cx, 9);
+    for (; i < i2; ++i) {
+      const int j = J.nb + i;
+      const int a = i * C_EXP_PER_JOB + wg;
+      if (okc) okc = __all_sync(0xffffffffu, wait_job(J, j, cx, s));
+      if (okc && a < n_act) {
+        // B fragments: token g's h' row if it chose the expert, else zero
+        const uint32_t tm = s.tmask[a];
+        const bool on = g < T && ((tm >> g) & 1u);
+        const int hr = s.rowbase[a] - lo + __popc(tm & ((1u << g) - 1u));
+        uint4 hb[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        hb[j] = (g < T) ? *reinterpret_cast<const uint4*>(hs + (ai * T + g) * (INTER / 2) + ks * 64 + 16 * c4 + 4 * j)
-                        : make_uint4(0, 0, 0, 0);
-      const bool sh = a == n_routed;
-      if (sh || a < n_st) {
-        const uint32_t* q = sh ? s.sdq : s.dq[a];
-        const uint16_t* sc = sh ? s.sdsc : s.dsc[a];
-        const uint16_t* bi = sh ? s.sdbi : s.dbi[a];
-        const uint4 w0 = *reinterpret_cast<const uint4*>(q + g * (INTER / 8) + wo);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(q + (g + 8) * (INTER / 8) + wo);
+        for (int k = 0; k < 4; ++k)
+          hb[k] = on ? *reinterpret_cast<const uint4*>(hs + hr * (INTER / 2) + kq * 64 + 16 * c4 + 4 * k)
+                     : make_uint4(0, 0, 0, 0);
+        const uint8_t* D = s.ring[(J.j0 + j) % NSLOT] + wg * C_EXP_BYTES;
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(D + DQ_WORDS * 4);
+        const uint16_t* bi = sc + DQ_GROUPS;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(D + g * (INTER / 2) + ((ch ^ g) << 4));
+        const uint4 w1 = *reinterpret_cast<const uint4*>(D + (g + 8) * (INTER / 2) + ((ch ^ g) << 4));
         down_mma(d, w0, w1, sc[g * (INTER / GROUP) + gi], sc[(g + 8) * (INTER / GROUP) + gi],
                  bi[g * (INTER / GROUP) + gi], bi[(g + 8) * (INTER / GROUP) + gi], hb);
-      } else {   // beyond the staging capacity: straight from memory
-        const size_t rw0 = static_cast<size_t>(s.act_e[a]) * HID + r0, rw1 = rw0 + 8;
-        const uint4 w0 = ldg_nc_v4(L.dq + rw0 * (INTER / 8) + wo);
-        const uint4 w1 = ldg_nc_v4(L.dq + rw1 * (INTER / 8) + wo);
-        down_mma(d, w0, w1, __ldg(L.ds + rw0 * (INTER / GROUP) + gi), __ldg(L.ds + rw1 * (INTER / GROUP) + gi),
-                 __ldg(L.db + rw0 * (INTER / GROUP) + gi), __ldg(L.db + rw1 * (INTER / GROUP) + gi), hb);
       }
+      release_job(J, j, s);
     }
-    __syncthreads();   // the h' rows are rewritten by the next batch
+    if (!cbar_and(okc)) return false;   // the batch's h' rows are free
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) s.red[0][warp][lane][k] = d[k];
+  for (int k = 0; k < 4; ++k) s.red[0][0][warp][lane][k] = d[k];
   stamp(cx, 14);
-  __syncthreads();
-  if (warp == 0) {
-    float q[4] = {0.f, 0.f, 0.f, 0.f};
+  cbar();
+  // warp k sums component k of the 16 warps' accumulators (row r0 or r1, token 2c or 2c+1)
+  if (warp < 4) {
+    const int k = warp;
+    float q = 0.f;
 #pragma unroll
-    for (int w = 0; w < DL_WARPS; ++w)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) q[k] += s.red[0][w][lane][k];
-    // q[0]: (row r0, token 2c), q[1]: (r0, 2c+1), q[2]: (r1, 2c), q[3]: (r1, 2c+1)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int tok = 2 * c4 + (k & 1);
-      if (p.residual && tok < T) q[k] += s.xres[tok][(k < 2) ? g : g + 8];
-    }
-    stamp(cx, 15);
+    for (int w = 0; w < DL_WARPS; ++w) q += s.red[0][0][w][lane][k];
+    const int tok = 2 * c4 + (k & 1);
+    const int row = (k < 2) ? r0 : r1;
+    if (p.residual && tok < T) q += s.xres[tok][(k < 2) ? g : g + 8];
+    if (k == 0) stamp(cx, 15);
     if (l + 1 == p.n_layers) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = 2 * c4 + (k & 1);
-        if (tok < T) p.out[static_cast<size_t>(tok) * HID + ((k < 2) ? r0 : r1)] = __float2bfloat16_rn(q[k]);
-      }
+      if (tok < T) p.out[static_cast<size_t>(tok) * HID + row] = __float2bfloat16_rn(q);
     } else {
       // the next layer's input, as tagged pairs of adjacent rows (lanes g and g + 1)
       unsigned long long* xt = p.xt + static_cast<size_t>((l + 1) & 1) * DEC_MAX_T * (HID / 2);
-      const uint32_t tag = cx.tag + 1u;
-      float nb[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) nb[k] = __shfl_down_sync(0xffffffffu, q[k], 4);
-      if ((g & 1) == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = 2 * c4 + (k & 1);
-          const int row = (k < 2) ? r0 : r1;
-          if (tok < T) st_tagged(xt + static_cast<size_t>(tok) * (HID / 2) + row / 2, pack_bf16x2(q[k], nb[k]), tag);
-        }
-      }
+      const float nb = __shfl_down_sync(0xffffffffu, q, 4);
+      if ((g & 1) == 0 && tok < T)
+        st_tagged(xt + static_cast<size_t>(tok) * (HID / 2) + row / 2, pack_bf16x2(q, nb), cx.tag + 1u);
     }
   }
   stamp(cx, 11);
@@ -785,14 +947,16 @@ __device__ bool phase_c(const DecLayersParams& p, const DecLayer& L, int l, cons
 
 }  // namespace
 
-__global__ void __launch_bounds__(DL_THREADS, 1) decode_layers_kernel(const __grid_constant__ DecLayersParams p) {
+__global__ void __launch_bounds__(DL_BLOCK, 1) decode_layers_kernel(const __grid_constant__ DecLayersParams p) {
   extern __shared__ __align__(128) uint8_t dl_smem[];
   DlShared& s = *reinterpret_cast<DlShared*>(dl_smem);
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&s.mb_a), DL_THREADS);   // one cp.async arrival per thread
-    mbar_init(smem_u32(&s.mb_c), DL_THREADS);
-    mbar_init(smem_u32(&s.mb_b[0]), DL_THREADS);
-    mbar_init(smem_u32(&s.mb_b[1]), DL_THREADS);
+    mbar_init(smem_u32(&s.mb_a), DL_COPY);      // one cp.async arrival per copy thread
+    for (int k = 0; k < NSLOT; ++k) {
+      mbar_init(smem_u32(&s.mb_full[k]), DL_COPY);
+      mbar_init(smem_u32(&s.mb_empty[k]), DL_WARPS);
+    }
+    mbar_init(smem_u32(&s.mb_route), 1);
     s.abort = 0;
     fence_mbar_init();
   }
@@ -803,23 +967,43 @@ __global__ void __launch_bounds__(DL_THREADS, 1) decode_layers_kernel(const __gr
   cx.trace = nullptr;
   cx.abort_word = p.sync + 2;
   cx.limit = p.wait_ns;
-  uint32_t bphase[2] = {0u, 0u};
-  issue_stage_a(p.layer[0], s);
-  for (int l = 0; l < p.n_layers; ++l) {
-    const DecLayer& L = p.layer[l];
-    cx.tag = dec_tag(epoch, l);
-    cx.err = L.err;
-    cx.trace = (p.trace != nullptr && blockIdx.x < DEC_TRACE_CTAS)
-                   ? p.trace + (static_cast<size_t>(l) * DEC_TRACE_CTAS + blockIdx.x) * DEC_TRACE_STAMPS
-                   : nullptr;
-    stamp(cx, 0);
-    if (!phase_a(p, L, l, cx, s)) break;
-    if (!phase_b_route(p, L, l, cx, s, l == p.n_layers - 1 && blockIdx.x == 0 && p.topk_idx != nullptr)) break;
-    if (!phase_b_gateup(p, L, l, cx, s, bphase)) break;
-    if (l + 1 < p.n_layers) {
-      issue_stage_a(p.layer[l + 1], s);
+  uint32_t jpos = 0;   // ring position of the next job
+  static_assert(DL_THREADS % 128 == 0 && DL_COPY == 128, "whole warpgroups for the register split");
+  if (threadIdx.x < DL_THREADS) {
+    // ------------------------------------------------ compute warps
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(DL_REGS_COMPUTE));
+    bool done = true;
+    for (int l = 0; l < p.n_layers; ++l) {
+      const DecLayer& L = p.layer[l];
+      cx.tag = dec_tag(epoch, l);
+      cx.err = L.err;
+      cx.trace = (p.trace != nullptr && blockIdx.x < DEC_TRACE_CTAS)
+                     ? p.trace + (static_cast<size_t>(l) * DEC_TRACE_CTAS + blockIdx.x) * DEC_TRACE_STAMPS
+                     : nullptr;
+      stamp(cx, 0);
+      done = false;
+      if (!phase_a(p, L, l, cx, s)) break;
+      if (!phase_b_route(p, L, l, cx, s, l == p.n_layers - 1 && blockIdx.x == 0 && p.topk_idx != nullptr)) break;
+      if (threadIdx.x == 0) mbar_arrive(smem_u32(&s.mb_route));   // the copy warps may start
+      const Jobs J = layer_jobs(s, jpos);
+      stamp(cx, 6);
+      if (!phase_b_gateup(p, L, l, cx, s, J)) break;
+      if (!phase_c(p, L, l, cx, s, J)) break;
+      jpos += static_cast<uint32_t>(J.n);
+      done = true;
     }
-    if (!phase_c(p, L, l, cx, s)) break;
+    if (!done && threadIdx.x == 0) s.abort = 1;   // the copy warps stop waiting
+  } else {
+    // ------------------------------------------------ copy warps
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(DL_REGS_COPY));
+    issue_stage_a(p.layer[0], s);
+    for (int l = 0; l < p.n_layers; ++l) {
+      cx.err = p.layer[l].err;
+      if (!copy_bar_and(mbar_wait(smem_u32(&s.mb_route), l & 1, cx.err, &s.abort, cx.limit))) break;
+      const Jobs J = layer_jobs(s, jpos);
+      if (!copy_layer(p, l, cx, s, J)) break;
+      jpos += static_cast<uint32_t>(J.n);
+    }
   }
   // leaving early: this thread's copies still in flight land before the CTA exits
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -835,9 +1019,9 @@ __global__ void __launch_bounds__(DL_THREADS, 1) decode_layers_kernel(const __gr
     __threadfence();
     const uint32_t next = dec_next_epoch(epoch);
     if (next == 0u) {
-      for (size_t i = threadIdx.x; i < DEC_LT_WORDS; i += DL_THREADS) p.lt[i] = 0ull;
-      for (size_t i = threadIdx.x; i < DEC_HT_WORDS; i += DL_THREADS) p.ht[i] = 0ull;
-      for (size_t i = threadIdx.x; i < DEC_XT_WORDS; i += DL_THREADS) p.xt[i] = 0ull;
+      for (size_t i = threadIdx.x; i < DEC_LT_WORDS; i += DL_BLOCK) p.lt[i] = 0ull;
+      for (size_t i = threadIdx.x; i < DEC_HT_WORDS; i += DL_BLOCK) p.ht[i] = 0ull;
+      for (size_t i = threadIdx.x; i < DEC_XT_WORDS; i += DL_BLOCK) p.xt[i] = 0ull;
       __threadfence();
       __syncthreads();
     }
@@ -872,8 +1056,13 @@ cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s) {
       e2 = cudaFuncSetAttribute(decode_layers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(sizeof(DlShared)));
     if (e2 == cudaSuccess)
-      e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layers_kernel, DL_THREADS, sizeof(DlShared));
+      e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layers_kernel, DL_BLOCK, sizeof(DlShared));
     if (e2 == cudaSuccess && per_sm < 1) e2 = cudaErrorCooperativeLaunchTooLarge;
+    // the register split inside the kernel draws on the registers allocated at launch: a
+    // build whose allocation is smaller than the split is refused here (it would stall)
+    cudaFuncAttributes fa;
+    if (e2 == cudaSuccess) e2 = cudaFuncGetAttributes(&fa, decode_layers_kernel);
+    if (e2 == cudaSuccess && fa.numRegs * DL_BLOCK < DL_REGS_SPLIT) e2 = cudaErrorInvalidConfiguration;
     if (e2 == cudaSuccess && nsm < DL_CTAS_C) e2 = cudaErrorCooperativeLaunchTooLarge;
     d.err = e2;
     d.grid = nsm;   // one CTA per SM: all resident, as the cross-CTA waits require
@@ -881,7 +1070,7 @@ cudaError_t launch_decode_layers(const DecLayersParams& p, cudaStream_t s) {
   if (d.err != cudaSuccess) return d.err;
   void* args[] = {const_cast<DecLayersParams*>(&p)};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(decode_layers_kernel), dim3(d.grid),
-                                     dim3(DL_THREADS), args, sizeof(DlShared), s);
+                                     dim3(DL_BLOCK), args, sizeof(DlShared), s);
 }
 
 }  // namespace moe

@@ -44,11 +44,16 @@ constexpr int STG_BUF = 32 * STG_ROW;                // one 32 x 32 staging tile
 static_assert(4 * DN_STG_BUFS * STG_BUF == DN_STG_BYTES, "staging size");
 }  // namespace
 
+// kLimit: the bounded waits take their time limit from the launch (p.wait_ns) instead of
+// the default; the launcher picks that instance only for a non-default limit, so the
+// default instance keeps the limit a compile-time constant.
+template <bool kLimit>
 __global__ void __launch_bounds__(DN_THREADS, 1)
     down_kernel(const __grid_constant__ CUtensorMap tm_qd, const __grid_constant__ CUtensorMap tm_sqd,
                 const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_y,
                 DownParams p) {
   extern __shared__ uint8_t smem_raw[];
+  const unsigned long long wlim = kLimit ? p.wait_ns : WAIT_LIMIT_NS;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* misc = smem + OFF_MISC;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                       // 40 barriers
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const int wrow = (sh ? 0 : ti.e * HID) + ti.mb * GX_BM;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int s = it % DN_NP;
-          if (!mbar_wait_t(PEMPTY(s), ((it / DN_NP) & 1) ^ 1, p.err, abort_flag, p.wait_ns, pc[0], pp)) { alive = false; break; }
+          if (!mbar_wait_t(PEMPTY(s), ((it / DN_NP) & 1) ^ 1, p.err, abort_flag, wlim, pc[0], pp)) { alive = false; break; }
           mbar_arrive_expect_tx(PFULL(s), GX_P_BYTES);
           tma_load_2d_hint(smem_u32(smem + OFF_P + s * GX_P_BYTES), mq, PFULL(s), kb * 8, wrow, pol);
         }
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const int nbox = (ti.n_rows + GX_XBOX - 1) / GX_XBOX;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int s = it % DN_NX;
-          if (!mbar_wait(XEMPTY(s), ((it / DN_NX) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) { alive = false; break; }
+          if (!mbar_wait(XEMPTY(s), ((it / DN_NX) & 1) ^ 1, p.err, abort_flag, wlim)) { alive = false; break; }
           const uint32_t st = smem_u32(smem + OFF_X + s * GX_X_BYTES);
           mbar_arrive_expect_tx(XFULL(s), nbox * GX_XBOX * 128);
           for (int j = 0; j < nbox; ++j)
@@ -172,14 +177,14 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         const int N = max(16, (ti.n_rows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(128, N);
         const int buf = tc & 1;
-        if (!mbar_wait_t(ACCE(buf), ((tc >> 1) & 1) ^ 1, p.err, abort_flag, p.wait_ns, pc[0], pp)) break;
+        if (!mbar_wait_t(ACCE(buf), ((tc >> 1) & 1) ^ 1, p.err, abort_flag, wlim, pc[0], pp)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * 256;
         bool alive = true;
         for (int kb = 0; kb < NKB; ++kb, ++it) {
           const int sa = it % DN_NA, sx = it % DN_NX;
-          if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, p.wait_ns, pc[1], pp)) ||
-              (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, p.wait_ns, pc[2], pp))) {
+          if ((!(rdy & 1u) && !mbar_wait_t(AFULL(sa), (it / DN_NA) & 1, p.err, abort_flag, wlim, pc[1], pp)) ||
+              (!(rdy & 2u) && !mbar_wait_t(XFULL(sx), (it / DN_NX) & 1, p.err, abort_flag, wlim, pc[2], pp))) {
             alive = false;
             break;
           }
@@ -237,8 +242,8 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 #pragma unroll
       for (int kb = 0; kb < NKB; ++kb) {
         const int sp = it % DN_NP, sa = it % DN_NA;
-        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, p.wait_ns, pc[0], pp) ||
-            !mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) {
+        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, wlim, pc[0], pp) ||
+            !mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag, wlim)) {
           alive = false;
           break;
         }
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
       const TileInfo ti = sched_tile(sched, tix);
       if (!ti.ok) continue;
       const int buf = tc & 1;
-      const bool got = mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, p.wait_ns, pc[0], pp);
+      const bool got = mbar_wait_t(ACCF(buf), (tc >> 1) & 1, p.err, abort_flag, wlim, pc[0], pp);
       if (!__all_sync(0xffffffffu, got)) break;   // tcgen05.ld below needs the whole warp
       tc_fence_after();
       const int fcol = ti.mb * GX_BM + q * 32;    // this warp's first output feature
@@ -368,12 +373,17 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s) {
-  down_kernel<<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, ymap, p);
+  if (p.wait_ns == WAIT_LIMIT_NS)
+    down_kernel<false><<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, ymap, p);
+  else
+    down_kernel<true><<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, ymap, p);
   return cudaGetLastError();
 }
 
 cudaError_t set_down_attributes() {
-  return cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DN_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(down_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, DN_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(down_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, DN_SMEM);
+  return e;
 }
 
 }  // namespace moe

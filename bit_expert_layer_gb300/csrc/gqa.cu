@@ -9,9 +9,10 @@
 // every key and value row crosses HBM once and feeds all 8 heads.
 //
 // One new query token per sequence; per (sequence b, KV head g) the cached positions are
-// split over `nsplit` CTAs (flash-decoding).  A CTA streams its positions in chunks of 64
-// keys (K and V, 32 KB per stage, loaded by TMA with the 128-byte swizzle) through a ring of
-// GQ_STAGES stages; 4 consumer warps take 16 keys each per stage:
+// split over `nsplit` CTAs (flash-decoding), one CTA per SM.  A CTA streams its positions in
+// chunks of 128 keys (K and V, 64 KB per stage, four TMA boxes of 16 KB with the 128-byte
+// swizzle: few, large copies, since each bulk copy has a fixed cost) through a ring of
+// GQ_STAGES stages; 8 consumer warps take 16 keys each per stage:
 //   S^T = Q K^T   mma.sync m16n8k16: A = the 8 query heads (rows 8..15 zero), B = K rows
 //                 (ldmatrix), fp32 scores
 //   online softmax in base 2 per head (running max and sum), probabilities rounded to
@@ -33,10 +34,14 @@ namespace moe {
 
 namespace {
 
-constexpr int GQ_STAGE_K = 0;                          // K: two boxes of 64 keys x 64 dims
-constexpr int GQ_STAGE_V = 2 * GQ_CH * 64 * 2;         // V: the same, 16 KB further
+constexpr int GQ_STAGE_K = 0;                          // K: two boxes of GQ_CH keys x 64 dims
+constexpr int GQ_STAGE_V = 2 * GQ_CH * 64 * 2;         // V: the same, after K
 constexpr int GQ_SMEM = GQ_STAGES * GQ_STAGE_BYTES + 1024 /* align */ + 256 /* barriers */;
-constexpr int GQ_WARPS = 4;                            // consumers; warp 4 is the TMA producer
+constexpr int GQ_WARPS = GQ_CH / 16;                  // consumers (16 keys each); the last warp is the TMA producer
+constexpr int GQ_PS = GQ_D + 4;   // floats per partial row: O[128], max (base 2), sum, 2 unused (16-byte rows)
+constexpr int GQ_FS_OFF = GQ_STAGE_BYTES;   // merge weights [8][GQ_MAX_SPLIT] in the second stage
+static_assert(GQ_WARPS * GQ_G * (GQ_D + 2) * 4 <= GQ_FS_OFF, "warp-merge scratch fits the first stage");
+static_assert(GQ_FS_OFF + GQ_G * GQ_MAX_SPLIT * 4 <= GQ_STAGES * GQ_STAGE_BYTES, "split weights fit the stages");
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
   // rows 8..15 of A (a1, a3) are zero: the 8 query heads of a group fill rows 0..7
@@ -228,7 +233,6 @@ __global__ void __launch_bounds__((GQ_WARPS + 1) * 32)
   }
   __syncthreads();
   // 128 threads: head h = tid / 16, dims 8 (tid % 16) .. +7; this split's partial
-  const size_t part_stride = GQ_D + 2;
   if (tid < GQ_G * 16) {
     const int h = tid >> 4, d0 = (tid & 15) * 8;
     float M = -INFINITY;
@@ -242,13 +246,10 @@ __global__ void __launch_bounds__((GQ_WARPS + 1) * 32)
 #pragma unroll
       for (int i = 0; i < 8; ++i) O[i] += f * wo[(w * GQ_G + h) * GQ_D + d0 + i];
     }
-    float* dst = p.part + ((static_cast<size_t>(b) * GQ_HQ + g * GQ_G + h) * p.nsplit + split) * part_stride;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[d0 + i] = O[i];
-    if (d0 == 0) {
-      dst[GQ_D] = M;
-      dst[GQ_D + 1] = L;
-    }
+    float* dst = p.part + ((static_cast<size_t>(b) * GQ_HQ + g * GQ_G + h) * p.nsplit + split) * GQ_PS;
+    *reinterpret_cast<float4*>(dst + d0) = make_float4(O[0], O[1], O[2], O[3]);
+    *reinterpret_cast<float4*>(dst + d0 + 4) = make_float4(O[4], O[5], O[6], O[7]);
+    if (d0 == 0) *reinterpret_cast<float2*>(dst + GQ_D) = make_float2(M, L);
   }
   __threadfence();   // publish the partial before the ticket is taken
   __syncthreads();
@@ -257,24 +258,64 @@ __global__ void __launch_bounds__((GQ_WARPS + 1) * 32)
   __syncthreads();
   if (!*s_last) return;
   __threadfence();
-  // the last CTA of (b, g): merge the splits in split order
+  // The last CTA of (b, g) merges the splits.  Every load below is independent of the
+  // others, so they are issued together rather than as one chain of L2 round trips:
+  // (1) the 16 threads of head h read the splits' (max, sum) pairs, split j, j + 16, ...
+  //     each, and reduce the maximum and the rescaled sum across the 16;
+  // (2) each thread sums its 8 dims of O over the splits with the weights from (1).
+  const int ns = p.nsplit;
+  float* fs = reinterpret_cast<float*>(smem + GQ_FS_OFF);   // [8][GQ_MAX_SPLIT] split weights
+  float L = 0.0f;
+  if (tid < GQ_G * 16) {
+    const int h = tid >> 4, j = tid & 15;
+    const float* src = p.part + (static_cast<size_t>(b) * GQ_HQ + g * GQ_G + h) * ns * GQ_PS;
+    float2 ml[GQ_MAX_SPLIT / 16];
+#pragma unroll
+    for (int i = 0; i < GQ_MAX_SPLIT / 16; ++i)
+      ml[i] = (j + 16 * i < ns) ? __ldcg(reinterpret_cast<const float2*>(src + (j + 16 * i) * GQ_PS + GQ_D))
+                                : make_float2(-INFINITY, 0.0f);
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < GQ_MAX_SPLIT / 16; ++i)
+      if (ml[i].y > 0.0f) M = fmaxf(M, ml[i].x);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+#pragma unroll
+    for (int i = 0; i < GQ_MAX_SPLIT / 16; ++i) {
+      const float f = (ml[i].y > 0.0f) ? exp2f(ml[i].x - M) : 0.0f;   // empty splits weigh nothing
+      L += f * ml[i].y;
+      if (j + 16 * i < ns) fs[h * GQ_MAX_SPLIT + j + 16 * i] = f;
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  }
+  __syncthreads();
   if (tid < GQ_G * 16) {
     const int h = tid >> 4, d0 = (tid & 15) * 8;
-    const float* src = p.part + (static_cast<size_t>(b) * GQ_HQ + g * GQ_G + h) * p.nsplit * part_stride;
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.nsplit; ++sp) {
-      const float l = __ldcg(src + sp * part_stride + GQ_D + 1);
-      if (l > 0.0f) M = fmaxf(M, __ldcg(src + sp * part_stride + GQ_D));
-    }
-    float L = 0.0f, O[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int sp = 0; sp < p.nsplit; ++sp) {
-      const float* ps = src + sp * part_stride;
-      const float l = __ldcg(ps + GQ_D + 1);
-      if (!(l > 0.0f)) continue;
-      const float f = exp2f(__ldcg(ps + GQ_D) - M);
-      L += f * l;
+    const float* src = p.part + (static_cast<size_t>(b) * GQ_HQ + g * GQ_G + h) * ns * GQ_PS + d0;
+    const float* fh = fs + h * GQ_MAX_SPLIT;
+    float O[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    int sp = 0;
+    for (; sp + 4 <= ns; sp += 4) {   // four splits' loads in flight at once
+      float4 a[4], c[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) O[i] += f * __ldcg(ps + d0 + i);
+      for (int u = 0; u < 4; ++u) {
+        a[u] = __ldcg(reinterpret_cast<const float4*>(src + (sp + u) * GQ_PS));
+        c[u] = __ldcg(reinterpret_cast<const float4*>(src + (sp + u) * GQ_PS + 4));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float f = fh[sp + u];
+        O[0] += f * a[u].x, O[1] += f * a[u].y, O[2] += f * a[u].z, O[3] += f * a[u].w;
+        O[4] += f * c[u].x, O[5] += f * c[u].y, O[6] += f * c[u].z, O[7] += f * c[u].w;
+      }
+    }
+    for (; sp < ns; ++sp) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(src + sp * GQ_PS));
+      const float4 c = __ldcg(reinterpret_cast<const float4*>(src + sp * GQ_PS + 4));
+      const float f = fh[sp];
+      O[0] += f * a.x, O[1] += f * a.y, O[2] += f * a.z, O[3] += f * a.w;
+      O[4] += f * c.x, O[5] += f * c.y, O[6] += f * c.z, O[7] += f * c.w;
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     if (!(L > 0.0f)) atomicOr(p.err, ERRBIT_BOUNDS);   // no key at all: cannot happen for len >= 1
@@ -305,7 +346,7 @@ cudaError_t launch_gqa_decode(const CUtensorMap& tm_k, const CUtensorMap& tm_v, 
 namespace moe {
 namespace {
 
-constexpr size_t GQ_PART_FLOATS_PER_SEQ = static_cast<size_t>(GQ_HQ) * GQ_MAX_SPLIT * (GQ_D + 2);
+constexpr size_t GQ_PART_FLOATS_PER_SEQ = static_cast<size_t>(GQ_HQ) * GQ_MAX_SPLIT * GQ_PS;
 
 struct GqaWorkspace {
   unsigned* err;
@@ -373,9 +414,9 @@ extern "C" moe_status_t gqa_decode_attention(const void* q, const void* k, const
   p.err = w.err;
   p.B = B;
   p.S_max = S_max;
-  // two CTAs per SM over all (sequence, KV head) pairs, no more splits than chunks
-  const int target = 2 * sm_count();
-  int ns = (target + 2 * B - 1) / (2 * B);
+  // one CTA per SM over all (sequence, KV head) pairs in a single wave, no more splits
+  // than chunks
+  int ns = sm_count() / (GQ_HKV * B);
   const int chunks = (max_len + GQ_CH - 1) / GQ_CH;
   ns = ns < chunks ? ns : chunks;
   ns = ns < GQ_MAX_SPLIT ? ns : GQ_MAX_SPLIT;

@@ -152,7 +152,7 @@ constexpr int GQ_HQ = 16;        // query heads
 constexpr int GQ_HKV = 2;        // key/value heads
 constexpr int GQ_G = GQ_HQ / GQ_HKV;
 constexpr int GQ_D = 128;        // head size
-constexpr int GQ_CH = 64;        // cached positions per pipeline stage
+constexpr int GQ_CH = 128;       // cached positions per pipeline stage
 constexpr int GQ_STAGES = 3;
 constexpr int GQ_STAGE_BYTES = 2 * GQ_CH * GQ_D * 2;   // K and V rows of one stage
 constexpr int GQ_MAX_B = 64;     // sequences per call
@@ -161,7 +161,7 @@ constexpr int GQ_MAX_SPLIT = 160;
 struct GqaParams {
   const __nv_bfloat16* q;   // [B][16][128]
   __nv_bfloat16* out;       // [B][16][128]
-  float* part;              // [B][16][nsplit][128 + 2]: unnormalised O, max (base 2), sum
+  float* part;              // [B][16][nsplit][132]: unnormalised O[128], max (base 2), sum, 2 unused
   unsigned* ticket;         // [B][2] splits done (the last one merges, then clears it)
   unsigned* err;
   int B, S_max, nsplit;
