@@ -87,6 +87,27 @@ constexpr int DN_STG_BYTES = 4 * DN_STG_BUFS * 32 * 32 * 2;
 // + alignment slack, barriers and words (1 KB), staging, row tables
 constexpr int DN_SMEM = DN_RINGS + 1024 + 1024 + DN_STG_BYTES + GX_TAB_BYTES + 16 + DN_SCHED_CAP * 16;
 static_assert(GU_SMEM <= 232448 && DN_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
+// down GEMM of the small token blocks (at most GX_SMALL rows: an expert's partial last
+// block), operands swapped: rings of packed tiles (256 weight rows, 8 KB), dequantised
+// weights (256 rows, 32 KB) and activation rows (128 rows, 16 KB)
+constexpr int GX_SMALL = 128;
+// Token counts up to which the small blocks go to the swapped kernel: a swapped K step (4
+// MMAs of 256 columns) takes about twice as long as a K step of a few columns, so halving
+// the steps pays only while most blocks are small (measured: T = 32 and 512 faster, 4096
+// and 16384 slower)
+constexpr int DS_MAX_T = 1024;
+constexpr int DS_NP = 8;
+constexpr int DS_NW = 3;
+constexpr int DS_NH = 3;
+constexpr int DS_P_STAGE = 2 * GX_P_BYTES;
+constexpr int DS_W_STAGE = 2 * GX_A_BYTES;
+constexpr int DS_H_STAGE = GX_SMALL * 64 * 2;
+constexpr int DS_PAIRS = HID / (2 * GX_BM);          // 8 pairs of row blocks (256 features)
+constexpr int DS_SCHED_CAP = 64;                     // at most 257 small blocks x 8 pairs: 14 per CTA on 152 SMs
+// + alignment slack, barriers and words (1 KB), row tables (16-byte rounded), schedule
+constexpr int DS_SMEM = DS_NP * DS_P_STAGE + DS_NW * DS_W_STAGE + DS_NH * DS_H_STAGE + 1024 + 1024 +
+                        (GX_TAB_BYTES + 15) / 16 * 16 + DS_SCHED_CAP * 16;
+static_assert(DS_SMEM <= 232448, "shared memory per CTA exceeds 227 KB");
 constexpr int DN_THREADS = 512;   // 16 warps: producers, MMA, 8 dequant, 4 epilogue, one spare
 constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
 

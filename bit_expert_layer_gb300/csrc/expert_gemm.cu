@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ntiles = build_schedule(sched, GU_SCHED_CAP, p.blocks, s_off, s_cnt, GU_MBLK, p.T, p.err);
+  const int ntiles = build_schedule(sched, GU_SCHED_CAP, p.blocks, s_off, s_cnt, GU_MBLK, p.T, p.err, true, BLOCKS_ALL);
   __syncthreads();
   constexpr int NKB = HID / 64;
   const bool pp = p.pipe != nullptr;

@@ -12,16 +12,18 @@ struct TileInfo {
   bool ok;   // tables consistent: every role skips a bad tile the same way
 };
 
-// Tile `tile` = token block tile / mblk of the ordered list built by route_scan_kernel
-// (entry: expert | (block index << 9)) x weight row block tile % mblk.  The offsets and
-// counts live in shared memory (stage_tables).
+// The ordered token-block list built by route_scan_kernel: blocks[0] = its length n,
+// blocks[1] = n_big, the number of blocks of more than GX_SMALL rows (they come first:
+// every full block, then the partial blocks largest first), entries from blocks[2]
+// (expert | (block index << 9)).  Tile `tile` = token block b0 + tile / mblk x weight row
+// block tile % mblk.  The offsets and counts live in shared memory (stage_tables).
 __device__ __forceinline__ TileInfo tile_info(const int* blocks, const int* offsets, const int* counts, int tile,
-                                              int mblk, int T) {
-  const int j = tile / mblk;
-  const int v = __ldg(blocks + 1 + j);
+                                              int mblk, int T, int b0 = 0) {
+  const int j = b0 + tile / mblk;
+  const int v = __ldg(blocks + 2 + j);
   TileInfo ti;
   ti.e = v & 511;
-  ti.mb = tile - j * mblk;
+  ti.mb = tile - (j - b0) * mblk;
   const int nb = v >> 9;
   const int e = ti.e <= NEXP ? ti.e : 0;
   ti.row0 = offsets[e] + nb * GX_BN;
@@ -39,24 +41,30 @@ __device__ __forceinline__ TileInfo tile_info(const int* blocks, const int* offs
 // per CTA: the straight order measured faster).  A record is {expert, row block, first row, rows};
 // rows = 0 marks a tile whose tables are inconsistent, which every role skips.  More
 // tiles than `cap` is a bounds error (the host sizes the grid so that it cannot
-// happen).  Returns the number of records.
+// happen).  `part` picks the blocks: all of them, the big ones (more than GX_SMALL rows)
+// or the small ones.  Returns the number of records.
+enum BlockPart { BLOCKS_ALL, BLOCKS_BIG, BLOCKS_SMALL };
 __device__ __forceinline__ int build_schedule(int4* sched, int cap, const int* blocks, const int* s_off,
                                               const int* s_cnt, int mblk, int T, unsigned int* err,
-                                              bool snake = true) {
-  int nblocks = __ldg(blocks);
+                                              bool snake, BlockPart part) {
+  int nblocks = __ldg(blocks), nbig = __ldg(blocks + 1);
   // at most ceil(8T / 256) + min(8T, 256) routed blocks and ceil(T / 256) shared ones
-  if (nblocks < 0 || nblocks > (8 * T + GX_BN - 1) / GX_BN + min(8 * T, NEXP) + (T + GX_BN - 1) / GX_BN) {
+  if (nblocks < 0 || nblocks > (8 * T + GX_BN - 1) / GX_BN + min(8 * T, NEXP) + (T + GX_BN - 1) / GX_BN ||
+      nbig < 0 || nbig > nblocks) {
     if (threadIdx.x == 0) atomicOr(err, ERRBIT_BOUNDS);
     nblocks = 0;
+    nbig = 0;
   }
-  const int total = nblocks * mblk;
+  const int b0 = part == BLOCKS_SMALL ? nbig : 0;
+  const int b1 = part == BLOCKS_BIG ? nbig : nblocks;
+  const int total = (b1 - b0) * mblk;
   const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
   const int rounds = total / g, rem = total - rounds * g;
   const int n = rounds + (((snake && (rounds & 1)) ? g - 1 - b : b) < rem ? 1 : 0);
   if (n > cap && threadIdx.x == 0) atomicOr(err, ERRBIT_BOUNDS);
   const int m = min(n, cap);
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
-    const TileInfo ti = tile_info(blocks, s_off, s_cnt, i * g + ((snake && (i & 1)) ? g - 1 - b : b), mblk, T);
+    const TileInfo ti = tile_info(blocks, s_off, s_cnt, i * g + ((snake && (i & 1)) ? g - 1 - b : b), mblk, T, b0);
     sched[i] = ti.ok ? make_int4(ti.e, ti.mb, ti.row0, ti.n_rows) : make_int4(0, 0, 0, 0);
   }
   return m;

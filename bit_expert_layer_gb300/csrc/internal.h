@@ -27,7 +27,7 @@ struct ScanParams {
   int* base;          // [nblk][256] first permuted row of (block, expert)
   int* counts;        // [257]: 256 experts + shared (= T)
   int* offsets;       // [258]: exclusive scan; [256] = 8T, [257] = 9T
-  int* blocks;        // [0] = number of token blocks, then the blocks (see route_scan_kernel)
+  int* blocks;        // [0] = number of token blocks, [1] = those of > GX_SMALL rows, then the blocks (see route_scan_kernel)
 };
 
 struct ScatterParams {
@@ -47,7 +47,7 @@ struct ScatterParams {
 };
 
 struct GateUpParams {
-  const int* blocks;     // token blocks: [0] = count, then expert | (block << 9)
+  const int* blocks;     // token blocks: [0] = count, [1] = blocks of > GX_SMALL rows, then expert | (block << 9)
   const int* offsets;    // [258]
   const int* counts;     // [257]
   const uint16_t* g_scales; const uint16_t* g_biases;    // [256][512][32]
@@ -64,7 +64,7 @@ struct GateUpParams {
 };
 
 struct DownParams {
-  const int* blocks;     // token blocks: [0] = count, then expert | (block << 9)
+  const int* blocks;     // token blocks: [0] = count, [1] = blocks of > GX_SMALL rows, then expert | (block << 9)
   const int* offsets;
   const int* counts;
   const uint16_t* d_scales; const uint16_t* d_biases;    // [256][2048][8]
@@ -74,6 +74,7 @@ struct DownParams {
   unsigned int* err;
   unsigned long long* pipe;   // 16 pipeline-trace counters, or nullptr
   unsigned long long wait_ns; // time limit of a bounded wait
+  int small_apart;            // down_kernel: 1 = leave the small blocks to down_swap_kernel
 };
 
 struct DecodeParams {
@@ -207,6 +208,8 @@ unsigned long long wait_limit_ns();
 // Record the calling thread's failure description that moe_last_error_detail returns:
 // `what`, followed by the CUDA error's name when e is not cudaSuccess.
 void set_error_detail(const char* what, cudaError_t e);
+cudaError_t launch_down_swap(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap, const DownParams& p,
+                             int grid, cudaStream_t s);
 cudaError_t set_down_attributes();
 
 }  // namespace moe

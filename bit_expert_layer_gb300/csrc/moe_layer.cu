@@ -84,13 +84,13 @@ void set_detail(const char* what, cudaError_t e) {
 // While enabled, every launch is bracketed by two CUDA events on its own stream; the
 // durations are resolved (and the record cleared) by moe_profiler_read.
 enum KernelId {
-  K_ROUTER, K_SCAN, K_SCATTER, K_GATEUP, K_DOWN, K_COMBINE, K_DEC_ROUTER, K_DEC_LAYERS, K_NORM,
+  K_ROUTER, K_SCAN, K_SCATTER, K_GATEUP, K_DOWN, K_COMBINE, K_DEC_ROUTER, K_DEC_LAYERS, K_NORM, K_DOWN_SWAP,
   K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {"router_prefill", "route_scan",    "route_scatter",
                                            "gateup",         "down",          "combine",
                                            "decode_router",  "decode_layers",
-                                           "rmsnorm"};
+                                           "rmsnorm",        "down_swap"};
 struct ProfRec {
   int id;
   cudaEvent_t a, b;
@@ -191,7 +191,9 @@ bool schedules_fit(int Tm, int num_sms) {
     const long long t = gemm_tiles_bound(Tm, mblk), g = gemm_grid(Tm, mblk, num_sms);
     return (t + g - 1) / g;
   };
-  return per_cta(GU_MBLK) <= GU_SCHED_CAP && per_cta(DN_MBLK) <= DN_SCHED_CAP;
+  // the small blocks: at most one per expert and the shared expert
+  const long long small = (NEXP + 1) * DS_PAIRS, gs = small < num_sms ? small : num_sms;
+  return per_cta(GU_MBLK) <= GU_SCHED_CAP && per_cta(DN_MBLK) <= DN_SCHED_CAP && (small + gs - 1) / gs <= DS_SCHED_CAP;
 }
 
 struct Carver {
@@ -219,7 +221,7 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->base = c.take<int>(nblk * NEXP * 4);
   d->counts = c.take<int>((NEXP + 1) * 4);
   d->offsets = c.take<int>((NEXP + 2) * 4);
-  d->blocks = c.take<int>((gemm_tiles_bound(Tm, 1) + 1) * 4);
+  d->blocks = c.take<int>((gemm_tiles_bound(Tm, 1) + 2) * 4);
   d->topk_idx = c.take<int>(static_cast<size_t>(Tm) * TOPK * 4);
   d->topk_w = c.take<float>(static_cast<size_t>(Tm) * TOPK * 4);
   d->row_dst = c.take<int>(rows * 4);
@@ -476,7 +478,14 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
   DownParams dp{L->blocks, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
                 pipe_trace() ? L->pipe + 16 : nullptr, wait_limit_ns()};
+  dp.small_apart = T <= DS_MAX_T ? 1 : 0;
   MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
+  if (dp.small_apart) {
+    // the small token blocks (at most one per expert), operands swapped
+    const int grid_ds = L->num_sms < (NEXP + 1) * DS_PAIRS ? L->num_sms : (NEXP + 1) * DS_PAIRS;
+    MOE_TRY(timed(K_DOWN_SWAP, s, L->err, [&] { return launch_down_swap(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_ds, s); }),
+            "down (small blocks) launch");
+  }
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
                   NextLayerIn nx{};
@@ -658,7 +667,7 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
 
 int moe_forward_launches(const moe_layer_t* L, int T) {
   if (!L || T < 1 || T > L->cfg.max_tokens) return 0;
-  return T <= DEC_MAX_T ? 1 : 6 + (L->w.norm_w ? 1 : 0);
+  return T <= DEC_MAX_T ? 1 : 6 + (T <= DS_MAX_T ? 1 : 0) + (L->w.norm_w ? 1 : 0);
 }
 
 int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, int T) {

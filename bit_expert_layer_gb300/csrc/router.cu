@@ -258,8 +258,9 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   // one expert; every tile is a block x one row block of the weights): all full blocks
   // first (expert order, the shared expert last), then each expert's partial last block,
   // largest first (ties: lower expert first).  The GEMMs deal their tiles in this order,
-  // so the smallest tiles are the last ones dealt and the CTAs' loads even out.  Entry:
-  // expert | (block index << 9).
+  // so the smallest tiles are the last ones dealt and the CTAs' loads even out.  Entries
+  // expert | (block index << 9) from blocks[2]; blocks[0] = their number, blocks[1] = the
+  // number of blocks of more than GX_SMALL rows.
   __shared__ int s_part[NEXP + 1];
   const int full = c / GX_BN, part = c % GX_BN;
   if (lead) s_part[e] = part;
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   }
   const int full_routed = sc[NEXP - 1], full_sh = p.T / GX_BN;
   const int n_full = full_routed + full_sh;
-  int* blk = p.blocks + 1;
+  int* blk = p.blocks + 2;
   if (lead)
     for (int k = 0; k < full; ++k) blk[sc[e] - full + k] = e | (k << 9);
   for (int k = threadIdx.x; k < full_sh; k += blockDim.x) blk[full_routed + k] = NEXP | (k << 9);
@@ -292,11 +293,15 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   if (lead && part > 0) blk[n_full + prank(e)] = e | (full << 9);
   if (threadIdx.x == NEXP && s_part[NEXP] > 0) blk[n_full + prank(NEXP)] = NEXP | (full_sh << 9);
   const int np = __syncthreads_count(lead && part > 0) + (s_part[NEXP] > 0);
+  // the big blocks (more than GX_SMALL rows): every full block and the partial blocks
+  // above GX_SMALL rows, which the order puts right after them
+  const int np_big = __syncthreads_count(lead && part > GX_SMALL) + (s_part[NEXP] > GX_SMALL);
   if (threadIdx.x == 0) {
     p.counts[NEXP] = p.T;
     p.offsets[NEXP] = 8 * p.T;
     p.offsets[NEXP + 1] = 9 * p.T;
     p.blocks[0] = n_full + np;
+    p.blocks[1] = n_full + np_big;
   }
 }
 
