@@ -243,12 +243,10 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 #pragma unroll
       for (int kb = 0; kb < NKB; ++kb) {
         const int sp = it % DN_NP, sa = it % DN_NA;
-        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, wlim, pc[0], pp) ||
-            !mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag, wlim)) {
+        if (!mbar_wait_t(PFULL(sp), (it / DN_NP) & 1, p.err, abort_flag, wlim, pc[0], pp)) {
           alive = false;
           break;
         }
-        ++it;
         const __nv_bfloat162 ms = bf2((kb & 1) ? (sw[kb >> 1] >> 16) : sw[kb >> 1]);
         const __nv_bfloat162 mbv = bf2((kb & 1) ? (bw[kb >> 1] >> 16) : bw[kb >> 1]);
         // this thread's 16-byte half of the row, stored 32-byte swizzled (half c at c ^ bit 2 of the row)
@@ -258,11 +256,21 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
         // async-proxy access, so the generic reads are fenced before the release
         fence_proxy_async_smem();
         mbar_arrive(PEMPTY(sp));
+        // dequantise into registers before waiting for the weight stage (two stages only):
+        // the stores alone then sit between the MMAs that free it and the MMAs that read it
+        // again (measured 1.5% faster; in the gate/up GEMM the same order was slower)
+        const uint4 d0 = dequant8(w.x, ms, mbv), d1 = dequant8(w.y, ms, mbv), d2 = dequant8(w.z, ms, mbv),
+                    d3 = dequant8(w.w, ms, mbv);
+        if (!mbar_wait(AEMPTY(sa), ((it / DN_NA) & 1) ^ 1, p.err, abort_flag, wlim)) {
+          alive = false;
+          break;
+        }
+        ++it;
         uint8_t* A = smem + OFF_A + sa * GX_A_BYTES;
-        st_shared_v4(A + sw128_off(r, 4 * hw + 0), dequant8(w.x, ms, mbv));
-        st_shared_v4(A + sw128_off(r, 4 * hw + 1), dequant8(w.y, ms, mbv));
-        st_shared_v4(A + sw128_off(r, 4 * hw + 2), dequant8(w.z, ms, mbv));
-        st_shared_v4(A + sw128_off(r, 4 * hw + 3), dequant8(w.w, ms, mbv));
+        st_shared_v4(A + sw128_off(r, 4 * hw + 0), d0);
+        st_shared_v4(A + sw128_off(r, 4 * hw + 1), d1);
+        st_shared_v4(A + sw128_off(r, 4 * hw + 2), d2);
+        st_shared_v4(A + sw128_off(r, 4 * hw + 3), d3);
         fence_proxy_async_smem();
         mbar_arrive(AFULL(sa));
       }
