@@ -116,17 +116,23 @@ def test_skewed_T4096(oracle, lib):
           f"max_err={err:.3e} scale={scale:.3e}")
 
 
-def test_all_tokens_on_one_expert_set(oracle, lib):
+@pytest.mark.parametrize("T", [128, 129, 384, 385, 600, 1024, 1025])
+def test_all_tokens_on_one_expert_set(oracle, lib, T):
+    """Every token on the same 8 experts (and the shared one), so each of them holds T
+    rows: blocks of exactly 128 and 129 rows (the largest small block, run with the
+    operands swapped up to T = 1024, and the smallest big one), a full block plus such a
+    partial block, and T on both sides of the token count above which the small blocks
+    stay in the ordinary down GEMM."""
     L = synth.make_layer(7)
     chosen = [3, 17, 40, 77, 100, 150, 200, 255]
     bias = np.zeros(256, np.float32)
     bias[chosen] = 20.0
     L.router_bias = bias
-    layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=1024)
-    x = synth.make_x(7, 600)
+    layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=1100)
+    x = synth.make_x(7, T)
     out, r = run(layer, x)
     assert set(np.unique(r["idx"]).tolist()) == set(chosen)
-    assert all(r["counts"][e] == 600 for e in chosen)
+    assert all(r["counts"][e] == T for e in chosen)
     rep, alt = check_routing(oracle, L, x, r["idx"], r["w"])
     check_output(oracle, L, x, out, alt=alt)   # every token
 
