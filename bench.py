@@ -541,14 +541,20 @@ def run_ours(args, wl):
             pass
     clocks = ClockSampler(gpu_id)
     time.sleep(0.3)
-    _abi.moe_profiler_read()
-    _abi.moe_profiler_enable(True)
     t0 = ev()
     t1 = ev()
     t0.record(stream)
     for _ in range(args.steps):
         step(True)
     t1.record(stream)
+    torch.cuda.synchronize(dev)
+    # the same steps again with the library's per-launch events on (every launch bracketed
+    # by two CUDA events on its stream): the per-kernel times and the roofline come from
+    # this pass, the step time above from a pass without that instrumentation
+    _abi.moe_profiler_read()
+    _abi.moe_profiler_enable(True)
+    for _ in range(args.steps):
+        step(False)
     torch.cuda.synchronize(dev)
     _abi.moe_profiler_enable(False)
     if world > 1:
@@ -617,7 +623,9 @@ def run_ours(args, wl):
         roof = dict(kernel="gateup", bound="tensor", achieved=achieved, peak=bf16_peak, unit="TFLOP/s",
                     frac=achieved / bf16_peak, traffic=tb,
                     algorithmic=f"{GATEUP_FLOP_PER_ROW} FLOP x 9T rows per launch (T={Tp})",
-                    peak_source=bf16_src)
+                    peak_source=bf16_src,
+                    launch_time=f"{1e3 * gu_ms / gu_n:.1f} us: mean of {gu_n} gate/up launches, each between two "
+                                f"CUDA events on its stream, in a second pass of the timed steps")
     dec = None
     dec_roof = None
     if Td:
