@@ -204,9 +204,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
 // below run on the q = 0 threads, every thread reaching the barriers.
 constexpr int SCAN_Q = 4;
 __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p) {
-  __shared__ int sc[NEXP];
+  __shared__ int sc[NEXP];      // inclusive scan of the experts' row counts
+  __shared__ int sf[NEXP];      // inclusive scan of their numbers of full blocks
+  __shared__ int s_wtot[2][NEXP / 32];
   __shared__ int s_seg[SCAN_Q][NEXP];
-  const int e = threadIdx.x % NEXP, q = threadIdx.x / NEXP;
+  __shared__ int s_part[NEXP + 1];   // each expert's partial block (the shared expert last)
+  const int e = threadIdx.x % NEXP, q = threadIdx.x / NEXP, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool lead = q == 0;
   const int per_q = (p.nblk + SCAN_Q - 1) / SCAN_Q;
   const int b_lo = q * per_q, b_hi = min(p.nblk, b_lo + per_q);
@@ -227,15 +230,40 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
     pre += (j < q) ? s_seg[j][e] : 0;
     c += s_seg[j][e];
   }
-  // block-wide inclusive scan (Hillis-Steele) of the counts
-  if (lead) sc[e] = c;
-  __syncthreads();
-  for (int off = 1; off < NEXP; off <<= 1) {
-    const int v = (lead && e >= off) ? sc[e - off] : 0;
-    __syncthreads();
-    if (lead) sc[e] += v;
-    __syncthreads();
+  // block-wide inclusive scans of the counts and of the numbers of full blocks: warp
+  // shuffles over 32 experts, then the 8 warp totals (the lead threads are warps 0-7)
+  const int full = c / GX_BN, part = c % GX_BN;
+  if (lead) {
+    int ic = c, ifl = full;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ic, o), f = __shfl_up_sync(0xffffffffu, ifl, o);
+      if (lane >= o) {
+        ic += a;
+        ifl += f;
+      }
+    }
+    if (lane == 31) {
+      s_wtot[0][warp] = ic;
+      s_wtot[1][warp] = ifl;
+    }
+    __syncwarp();
+    sc[e] = ic;
+    sf[e] = ifl;
+    s_part[e] = part;
   }
+  if (threadIdx.x == 0) s_part[NEXP] = p.T % GX_BN;
+  __syncthreads();
+  if (lead && warp > 0) {
+    int ac = 0, af = 0;
+    for (int w = 0; w < warp; ++w) {
+      ac += s_wtot[0][w];
+      af += s_wtot[1][w];
+    }
+    sc[e] += ac;
+    sf[e] += af;
+  }
+  __syncthreads();
   const int excl = sc[e] - c;
   // first permuted row of (block, expert): the expert's offset plus earlier blocks' counts
   int run = excl + pre;
@@ -253,7 +281,6 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
     p.counts[e] = c;
     p.offsets[e] = excl;
   }
-  __syncthreads();   // every thread has read sc
   // Token blocks of the grouped GEMMs (a block = up to 256 consecutive permuted rows of
   // one expert; every tile is a block x one row block of the weights): all full blocks
   // first (expert order, the shared expert last), then each expert's partial last block,
@@ -261,23 +288,11 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   // so the smallest tiles are the last ones dealt and the CTAs' loads even out.  Entries
   // expert | (block index << 9) from blocks[2]; blocks[0] = their number, blocks[1] = the
   // number of blocks of more than GX_SMALL rows.
-  __shared__ int s_part[NEXP + 1];
-  const int full = c / GX_BN, part = c % GX_BN;
-  if (lead) s_part[e] = part;
-  if (threadIdx.x == 0) s_part[NEXP] = p.T % GX_BN;
-  if (lead) sc[e] = full;
-  __syncthreads();
-  for (int off = 1; off < NEXP; off <<= 1) {
-    const int v = (lead && e >= off) ? sc[e - off] : 0;
-    __syncthreads();
-    if (lead) sc[e] += v;
-    __syncthreads();
-  }
-  const int full_routed = sc[NEXP - 1], full_sh = p.T / GX_BN;
+  const int full_routed = sf[NEXP - 1], full_sh = p.T / GX_BN;
   const int n_full = full_routed + full_sh;
   int* blk = p.blocks + 2;
   if (lead)
-    for (int k = 0; k < full; ++k) blk[sc[e] - full + k] = e | (k << 9);
+    for (int k = 0; k < full; ++k) blk[sf[e] - full + k] = e | (k << 9);
   for (int k = threadIdx.x; k < full_sh; k += blockDim.x) blk[full_routed + k] = NEXP | (k << 9);
   // rank of a partial block among all partial blocks (four independent counts in flight)
   auto prank = [&](int x) {
@@ -307,34 +322,41 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
 
 __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams p) {
   constexpr int SLOTS = RT_BM * TOPK;   // 1024 slots per router block
-  __shared__ int idx_s[SLOTS];
   __shared__ int wh[8][NEXP];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slot0 = b * SLOTS;
   const int nslots = min(SLOTS, p.T * TOPK - slot0);
   const int n8 = 8 * p.T;
   if (blockIdx.y == 0) {
-  for (int i = tid; i < SLOTS; i += SC_THREADS) {
-    int e = (i < nslots) ? p.topk_idx[slot0 + i] : -1;
-    if (e >= NEXP || e < -1) {   // never index shared memory with a bad expert id
-      atomicOr(p.err, ERRBIT_BOUNDS);
-      e = -1;
-    }
-    idx_s[i] = e;
+  // this thread's four slots (warp * 128 + j * 32 + lane, the order of pass 3), their
+  // routing weights and its expert's block base: every global read up front
+  int ev[4];
+  float wv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int sl = warp * 128 + j * 32 + lane;
+    ev[j] = (sl < nslots) ? __ldg(p.topk_idx + slot0 + sl) : -1;
+    wv[j] = (sl < nslots) ? __ldg(p.topk_w + slot0 + sl) : 0.0f;
   }
+  const int base_e = __ldg(p.base + b * NEXP + tid);
   for (int i = tid; i < 8 * NEXP; i += SC_THREADS) (&wh[0][0])[i] = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (ev[j] >= NEXP || ev[j] < -1) {   // never index shared memory with a bad expert id
+      atomicOr(p.err, ERRBIT_BOUNDS);
+      ev[j] = -1;
+    }
+  }
   __syncthreads();
   // pass 1: histogram of each warp's 128 consecutive slots
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int e = idx_s[warp * 128 + j * 32 + lane];
-    if (e >= 0) atomicAdd(&wh[warp][e], 1);
-  }
+  for (int j = 0; j < 4; ++j)
+    if (ev[j] >= 0) atomicAdd(&wh[warp][ev[j]], 1);
   __syncthreads();
   // pass 2: per expert, each warp's first global row (block base + earlier warps)
   {
     const int e = tid;
-    int run = p.base[b * NEXP + e];
+    int run = base_e;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const int c = wh[w][e];
@@ -347,7 +369,7 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int s = warp * 128 + j * 32 + lane;
-    const int e = idx_s[s];
+    const int e = ev[j];
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     int pos = -1;
@@ -361,7 +383,7 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
     }
     if (pos >= 0) {
       p.row_dst[pos] = slot0 + s;
-      p.row_w[pos] = p.topk_w[slot0 + s];
+      p.row_w[pos] = wv[j];
     }
     if (s < nslots) p.slot_row[slot0 + s] = pos;   // -1 for a slot that failed validation
   }
@@ -372,18 +394,27 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   constexpr int TPC = RT_BM / SC_SPLIT;   // tokens of this CTA
   const int t0 = b * RT_BM + blockIdx.y * TPC;
   const uint4* gsv = reinterpret_cast<const uint4*>(p.shared_gate_w);
+  // the shared-gate vector is the same for every token: read once per warp; a token's
+  // eight x chunks are all requested before any is used
+  uint4 gw[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) gw[c] = ldg_nc_v4(gsv + lane + 32 * c);
+#pragma unroll 1
   for (int tl = warp; tl < TPC; tl += SC_THREADS / 32) {
     const int t = t0 + tl;
     if (t >= p.T) break;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(t) * HID);
-    uint4 v[8];
+    uint4 cur[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) cur[c] = ldg_nc_v4(src + lane + 32 * c);
+    uint4* dst = reinterpret_cast<uint4*>(p.x_ilv + static_cast<size_t>(t) * HID);
     // the summation order of row_dot (chunk lane + 32c is "thread" lane of "warp" c), so
     // the combine, which computes this dot for the next stacked layer, gets the same bits
     float dot = 0.0f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint4 raw = ldg_nc_v4(src + lane + 32 * c);
-      const uint4 g = ldg_nc_v4(gsv + lane + 32 * c);
+      const uint4 raw = cur[c];
+      const uint4 g = gw[c];
       float d = 0.0f;
       d = fmaf(bf16lo(raw.x), bf16lo(g.x), d);
       d = fmaf(bf16hi(raw.x), bf16hi(g.x), d);
@@ -396,16 +427,13 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
       dot += d;
-      v[c] = interleave8(raw);
+      dst[lane + 32 * c] = interleave8(raw);
     }
     if (lane == 0) {
       const int srow = n8 + t;
       p.row_dst[srow] = srow;
       p.row_w[srow] = 1.0f / (1.0f + expf(-dot));
     }
-    uint4* dst = reinterpret_cast<uint4*>(p.x_ilv + static_cast<size_t>(t) * HID);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) dst[lane + 32 * c] = v[c];
   }
 }
 
