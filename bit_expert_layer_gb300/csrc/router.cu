@@ -199,6 +199,190 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
 }
 
+// router_split_kernel: the same routing for T <= RS_MAX_T, where one CTA per 128 tokens
+// leaves most SMs idle and each CTA streams the whole 1 MB router matrix.  Grid (token
+// block b, expert segment g = 0..3): each CTA computes the logits of its 64 experts (MMA
+// N = 64, 24 KB per K step) and keeps its segment's top 8 per token with the same
+// strictly-greater insertion over ascending experts as router_prefill_kernel's segment
+// warps, writing them to the workspace.  The last of a block's four CTAs (an atomic
+// ticket, no waiting) takes the four lists in segment order -- the same insertions as
+// router_prefill_kernel's merge, so the same top 8 -- and writes the ids, the weights and
+// the block's histogram.  Four warps: warp 0 also issues the TMA loads, warp 1 the MMAs.
+__global__ void __launch_bounds__(RS_THREADS, 1)
+    router_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wr64,
+                        RouteParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* misc = smem + RS_STAGES * RS_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                 // full[8] empty[8] done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  int* s_last = reinterpret_cast<int*>(misc + 264);
+  float* bias_s = reinterpret_cast<float*>(misc + 512);               // [64]
+  int* hist_s = reinterpret_cast<int*>(misc + 1024);                  // [256]
+  static_assert(1024 + NEXP * 4 <= 2048 && RS_SMEM >= RS_STAGES * RS_STAGE_BYTES + 2048 + 1024, "router smem");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x, g = blockIdx.y, m0 = b * RT_BM;
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[RS_STAGES]), done = smem_u32(&bars[2 * RS_STAGES]);
+
+  if (tid == 0) {
+    for (int s = 0; s < RS_STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < 64) bias_s[tid] = p.router_bias ? p.router_bias[64 * g + tid] : 0.0f;
+  for (int i = tid; i < NEXP; i += RS_THREADS) hist_s[i] = 0;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr int NKB = HID / 64;
+  int issued = 0;   // TMA producer: K steps whose loads it issued
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer: the block's x rows and this segment's 64 router rows
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_wr64);
+    for (int kb = 0; kb < NKB; ++kb) {
+      const int s = kb % RS_STAGES;
+      const uint32_t ph = (kb / RS_STAGES) & 1;
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, abort_flag, p.wait_ns)) break;
+      uint8_t* st = smem + s * RS_STAGE_BYTES;
+      mbar_arrive_expect_tx(full0 + 8 * s, RS_STAGE_BYTES);
+      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kb * 64, m0);
+      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr64, full0 + 8 * s, kb * 64, 64 * g);
+      issued = kb + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    const uint32_t id_r = idesc_bf16(128, 64);
+    for (int kb = 0; kb < NKB; ++kb) {
+      const int s = kb % RS_STAGES;
+      const uint32_t ph = (kb / RS_STAGES) & 1;
+      if (!mbar_wait(full0 + 8 * s, ph, p.err, abort_flag, p.wait_ns)) break;
+      tc_fence_after();
+      const uint32_t a = smem_u32(smem + s * RS_STAGE_BYTES);
+      const uint32_t bb = a + RT_A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + kk * 32), id_r, (kb | kk) != 0);
+      umma_commit(empty0 + 8 * s);
+    }
+    umma_commit(done);   // also covers an early exit: all issued MMAs complete first
+  }
+  __syncwarp();
+
+  // ---- this segment's top 8 per token: warp w reads TMEM lane quarter w (32 tokens)
+  bool ok = mbar_wait(done, 0, p.err, abort_flag, p.wait_ns);
+  ok = __syncthreads_and(ok && !*abort_flag) != 0;
+  tc_fence_after();
+  const int t = m0 + tid;
+  float tv[TOPK];
+  int ti[TOPK];
+#pragma unroll
+  for (int k = 0; k < TOPK; ++k) { tv[k] = -INFINITY; ti[k] = NEXP; }
+  auto insert = [&](float v, int e) {
+    if (v > tv[TOPK - 1]) {          // strictly greater: equal logits keep the lower index
+      tv[TOPK - 1] = v;
+      ti[TOPK - 1] = e;
+#pragma unroll
+      for (int k = TOPK - 1; k > 0; --k) {
+        if (tv[k] > tv[k - 1]) {
+          const float fv = tv[k]; tv[k] = tv[k - 1]; tv[k - 1] = fv;
+          const int iv = ti[k]; ti[k] = ti[k - 1]; ti[k - 1] = iv;
+        }
+      }
+    }
+  };
+  if (ok) {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      uint32_t r[32];
+      tmem_ld32(lane_base + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) insert(__uint_as_float(r[j]) + bias_s[c * 32 + j], 64 * g + c * 32 + j);
+    }
+  }
+  if (t < p.T) {
+    int2* dst = p.cand + (static_cast<size_t>(t) * 4 + g) * TOPK;
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) dst[k] = make_int2(__float_as_int(tv[k]), ti[k]);
+  }
+  // TMEM is done with: free it before the merge
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // a launch that gave up: copies still in flight land before shared memory goes away
+    for (int kb = (issued > RS_STAGES ? issued - RS_STAGES : 0); kb < issued; ++kb) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(full0 + 8 * (kb % RS_STAGES), (kb / RS_STAGES) & 1) &&
+             globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    if (lane == 0 && *abort_flag) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+    __syncwarp();
+    tmem_dealloc(tmem, 64);
+  }
+  __threadfence();   // publish this segment's lists before taking the ticket
+  __syncthreads();
+  if (tid == 0) *s_last = (atomicAdd(p.ticket + b, 1u) == 3u);
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  // ---- the block's last CTA: the four segments' lists in segment order
+  if (t < p.T) {
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) { tv[k] = -INFINITY; ti[k] = NEXP; }
+    const int2* src = p.cand + static_cast<size_t>(t) * 4 * TOPK;
+#pragma unroll 1
+    for (int sg = 0; sg < 4; ++sg) {
+      int2 c8[TOPK];
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) c8[k] = __ldcg(src + sg * TOPK + k);
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k) insert(__int_as_float(c8[k].x), c8[k].y);
+    }
+    // fewer than 8 ordered logits (NaN input): record it and route to expert 0 ..
+    if (ti[TOPK - 1] >= NEXP) {
+      atomicOr(p.err, ERRBIT_BOUNDS);
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k)
+        if (ti[k] >= NEXP) { ti[k] = k; tv[k] = tv[0]; }
+    }
+    float ex[TOPK], sum = 0.0f;
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) { ex[k] = expf(tv[k] - tv[0]); sum += ex[k]; }
+    const float inv = 1.0f / sum;
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) {
+      p.topk_idx[t * TOPK + k] = ti[k];
+      p.topk_w[t * TOPK + k] = ex[k] * inv;
+      atomicAdd(&hist_s[ti[k]], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < NEXP; i += RS_THREADS) p.hist[b * NEXP + i] = hist_s[i];
+  if (tid == 0) p.ticket[b] = 0u;   // ready for the next launch (every CTA of the block took its ticket)
+}
+
 // 1024 threads: thread (q, e) = expert e's router blocks of quarter q (the per-expert
 // sums and prefixes over the blocks run four ways in parallel); the per-expert steps
 // below run on the q = 0 threads, every thread reaching the barriers.
@@ -463,6 +647,13 @@ cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm
   return cudaGetLastError();
 }
 
+cudaError_t launch_router_split(const CUtensorMap& tm_x, const CUtensorMap& tm_wr64, const RouteParams& p,
+                                cudaStream_t s) {
+  const int nblk = (p.T + RT_BM - 1) / RT_BM;
+  router_split_kernel<<<dim3(nblk, 4), RS_THREADS, RS_SMEM, s>>>(tm_x, tm_wr64, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
   route_scan_kernel<<<1, SCAN_Q * NEXP, 0, s>>>(p);
   return cudaGetLastError();
@@ -474,7 +665,9 @@ cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
 }
 
 cudaError_t set_router_attributes() {
-  return cudaFuncSetAttribute(router_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(router_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(router_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RS_SMEM);
+  return e;
 }
 
 }  // namespace moe
