@@ -39,13 +39,14 @@ constexpr int RT_SEGS = 4;                          // expert segments scanned b
 constexpr int RT_CAND_BYTES = (RT_SEGS - 1) * 8 * RT_BM * 8;   // top-8 lists of segments 1-3
 constexpr int RT_SMEM = RT_STAGES * RT_STAGE_BYTES + 1024 + 3072 + RT_CAND_BYTES;
 constexpr int RT_THREADS = 128 * RT_SEGS;
-// router for T <= RS_MAX_T: one CTA per (128-token block, 64-expert segment), 24 KB stages
-constexpr int RS_MAX_T = 4096;
-constexpr int RS_STAGES = 8;
-constexpr int RS_B_BYTES = 64 * 64 * 2;             //  8 KB  router tile (64 experts)
-constexpr int RS_STAGE_BYTES = RT_A_BYTES + RS_B_BYTES;
-constexpr int RS_SMEM = RS_STAGES * RS_STAGE_BYTES + 1024 + 2048;
-constexpr int RS_THREADS = 128;
+// router for T <= RC_MAX_T: a cluster of RC_SPLIT CTAs per 128-token block, each over a
+// quarter of K (48 KB stages); the partial logits meet in distributed shared memory
+constexpr int RC_MAX_T = 4096;
+constexpr int RC_SPLIT = 4;
+constexpr int RC_STAGES = 4;
+constexpr int RC_ROW = NEXP + 4;                    // floats per received partial row
+constexpr int RC_SMEM = RC_STAGES * RT_STAGE_BYTES + 1024 + 8192 + 1024;
+constexpr int RC_THREADS = 128;
 
 
 // Grouped expert GEMMs: 128 weight rows (M) x up to 256 tokens (N) per tile, K step 64

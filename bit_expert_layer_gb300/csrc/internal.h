@@ -18,8 +18,6 @@ struct RouteParams {
   int* hist;                 // [nblk][256] per-router-block expert histogram
   unsigned int* err;
   unsigned long long wait_ns;  // time limit of a bounded wait
-  int2* cand;                // router_split_kernel: [T][4 segments][8] (logit bits, expert)
-  unsigned* ticket;          // router_split_kernel: [nblk] segments done (the last merges, then clears)
 };
 
 struct ScanParams {
@@ -174,8 +172,8 @@ struct GqaParams {
 };
 
 // launchers (return the first launch error)
-cudaError_t launch_router_split(const CUtensorMap& tm_x, const CUtensorMap& tm_wr64, const RouteParams& p,
-                                cudaStream_t s);
+cudaError_t launch_router_cluster(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
+                                  cudaStream_t s);
 cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
                                   cudaStream_t s);
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* xn, int T,

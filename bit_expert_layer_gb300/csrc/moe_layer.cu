@@ -53,8 +53,6 @@ struct moe_layer {
   unsigned int* err;
   unsigned int* dec_counter;
   int *hist, *base, *counts, *offsets, *blocks;
-  int2* rs_cand;                   // split router: per-segment top-8 lists (T <= RS_MAX_T)
-  unsigned* rs_ticket;             // split router: per-block segment tickets
   int* topk_idx;
   float* topk_w;
   int* row_dst;
@@ -73,7 +71,7 @@ struct moe_layer {
   unsigned long long* dec_trace;   // fused decode: phase timestamps (MOE_DECODE_TRACE=1)
   unsigned long long* pipe;   // 32 pipeline-trace counters (gate/up 0..15, down 16..31)
   // TMA descriptors of the weights and of the workspace buffers
-  CUtensorMap tm_wr, tm_wr64, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h, tm_y, tm_hs;
+  CUtensorMap tm_wr, tm_qg, tm_qu, tm_sqg, tm_squ, tm_qd, tm_sqd, tm_h, tm_y, tm_hs;
 };
 
 namespace {
@@ -226,8 +224,6 @@ size_t carve(int Tm, uint8_t* base, moe_layer* L) {
   d->blocks = c.take<int>((gemm_tiles_bound(Tm, 1) + 2) * 4);
   d->topk_idx = c.take<int>(static_cast<size_t>(Tm) * TOPK * 4);
   d->topk_w = c.take<float>(static_cast<size_t>(Tm) * TOPK * 4);
-  d->rs_cand = c.take<int2>(static_cast<size_t>(Tm < RS_MAX_T ? Tm : RS_MAX_T) * 4 * TOPK * 8);
-  d->rs_ticket = c.take<unsigned>((RS_MAX_T / RT_BM) * 4);
   d->row_dst = c.take<int>(rows * 4);
   d->row_w = c.take<float>(rows * 4);
   d->slot_row = c.take<int>(static_cast<size_t>(Tm) * TOPK * 4);
@@ -338,12 +334,12 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   CUtensorMap tm_x;
   if (!encode_bf16_rows(&tm_x, x, HID, T, RT_BM)) return MOE_ERR_CUDA;
   RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist, L->err,
-                 wait_limit_ns(), L->rs_cand, L->rs_ticket};
-  // up to RS_MAX_T tokens the four 64-expert segments of a token block run in CTAs of
-  // their own (four times the CTAs, a quarter of the router matrix each)
+                 wait_limit_ns()};
+  // up to RC_MAX_T tokens a token block's contraction is cut in four K quarters, one CTA
+  // of a cluster each (four times the CTAs, a quarter of the K steps each)
   MOE_TRY(timed(K_ROUTER, s, L->err,
                 [&] {
-                  return T <= RS_MAX_T ? launch_router_split(tm_x, L->tm_wr64, rp, s)
+                  return T <= RC_MAX_T ? launch_router_cluster(tm_x, L->tm_wr, rp, s)
                                        : launch_router_prefill(tm_x, L->tm_wr, rp, s);
                 }),
           "router launch");
@@ -577,7 +573,6 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
   if ((e = cudaMemset(L->err, 0, 256)) != cudaSuccess || (e = cudaMemset(L->dec_counter, 0, 256)) != cudaSuccess ||
       (e = cudaMemset(L->pipe, 0, 32 * 8)) != cudaSuccess ||
       (e = cudaMemset(L->dec_sync, 0, 256)) != cudaSuccess ||
-      (e = cudaMemset(L->rs_ticket, 0, (RS_MAX_T / RT_BM) * 4)) != cudaSuccess ||
       (e = cudaMemset(L->dec_lt, 0, DEC_LT_WORDS * 8)) != cudaSuccess ||
       (e = cudaMemset(L->dec_ht, 0, DEC_HT_WORDS * 8)) != cudaSuccess ||
       (e = cudaMemset(L->dec_xt, 0, DEC_XT_WORDS * 8)) != cudaSuccess ||
@@ -586,7 +581,6 @@ moe_status_t moe_layer_create(const moe_config_t* cfg, const moe_weights_t* weig
 
   const int Tm = cfg->max_tokens;
   bool ok = encode_bf16_rows(&L->tm_wr, weights->router_w, HID, NEXP, NEXP) &&
-            encode_bf16_rows(&L->tm_wr64, weights->router_w, HID, NEXP, 64) &&
             encode_packed(&L->tm_qg, weights->gate.q, HID / 8, static_cast<uint64_t>(NEXP) * INTER) &&
             encode_packed(&L->tm_qu, weights->up.q, HID / 8, static_cast<uint64_t>(NEXP) * INTER) &&
             encode_packed(&L->tm_sqg, weights->sh_gate.q, HID / 8, SH_INTER) &&

@@ -199,35 +199,66 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
 }
 
-// router_split_kernel: the same routing for T <= RS_MAX_T, where one CTA per 128 tokens
-// leaves most SMs idle and each CTA streams the whole 1 MB router matrix.  Grid (token
-// block b, expert segment g = 0..3): each CTA computes the logits of its 64 experts (MMA
-// N = 64, 24 KB per K step) and keeps its segment's top 8 per token with the same
-// strictly-greater insertion over ascending experts as router_prefill_kernel's segment
-// warps, writing them to the workspace.  The last of a block's four CTAs (an atomic
-// ticket, no waiting) takes the four lists in segment order -- the same insertions as
-// router_prefill_kernel's merge, so the same top 8 -- and writes the ids, the weights and
-// the block's histogram.  Four warps: warp 0 also issues the TMA loads, warp 1 the MMAs.
-__global__ void __launch_bounds__(RS_THREADS, 1)
-    router_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wr64,
-                        RouteParams p) {
+// router_cluster_kernel: the same routing for T <= RC_MAX_T, where one CTA per 128
+// tokens would leave most SMs idle.  The contraction over the 2048 hidden columns is cut
+// in RC_SPLIT = 4 quarters: a cluster of four CTAs per token block, CTA r accumulating
+// quarter r of K for all 256 experts (MMA N = 256, 8 K steps).  The partial logits move
+// through distributed shared memory -- CTA r sends the rows of tokens 32j..32j+31 to
+// CTA j -- and CTA j adds the four partials in quarter order (a fixed order, so the
+// result does not depend on timing), adds the bias and keeps the top 8 of each of its 32
+// tokens as router_prefill_kernel does: four 64-expert segments (one warp each) with
+// strictly-greater insertion over ascending experts, merged in segment order.  Rank 0
+// clears the block's histogram row before the first cluster barrier; every CTA adds its
+// tokens' counts after the second.  Every thread passes both cluster barriers on every
+// path (a launch that gave up included), so no CTA waits for a peer that has left.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+// Every thread of every CTA of the cluster arrives; writes before it (shared::cluster and
+// global) are visible to every thread of the cluster after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1)
+    router_cluster_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wr,
+                          RouteParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* misc = smem + RS_STAGES * RS_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                 // full[8] empty[8] done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
-  int* s_last = reinterpret_cast<int*>(misc + 264);
-  float* bias_s = reinterpret_cast<float*>(misc + 512);               // [64]
-  int* hist_s = reinterpret_cast<int*>(misc + 1024);                  // [256]
-  static_assert(1024 + NEXP * 4 <= 2048 && RS_SMEM >= RS_STAGES * RS_STAGE_BYTES + 2048 + 1024, "router smem");
+  uint8_t* misc = smem + RC_STAGES * RT_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);                  // full[4] empty[4] done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
+  float* bias_s = reinterpret_cast<float*>(misc + 256);                // [256]
+  int* hist_s = reinterpret_cast<int*>(misc + 256 + NEXP * 4);         // [256]
+  float* cand_v = reinterpret_cast<float*>(misc + 256 + NEXP * 8);     // [3 segments][8][32 tokens]
+  int* cand_e = reinterpret_cast<int*>(cand_v + 3 * TOPK * 32);
+  // the four partials of this CTA's 32 tokens, [quarter][token][RC_ROW], over the stage
+  // buffers once every MMA of the cluster is done (row stride 1040 bytes: the 16-byte
+  // accesses of 8 consecutive tokens fall in distinct banks)
+  float* recv = reinterpret_cast<float*>(smem);
+  static_assert(RC_SPLIT * 32 * RC_ROW * 4 <= RC_STAGES * RT_STAGE_BYTES, "partials fit the stage buffers");
+  static_assert(256 + NEXP * 8 + 2 * 3 * TOPK * 32 * 4 + 1024 <= RC_SMEM - RC_STAGES * RT_STAGE_BYTES, "router smem");
+  static_assert(RC_THREADS == 128 && NEXP == 4 * 64 && RT_BM == RC_SPLIT * 32, "one warp per token quarter / segment");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x, g = blockIdx.y, m0 = b * RT_BM;
-  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[RS_STAGES]), done = smem_u32(&bars[2 * RS_STAGES]);
-
+  const int b = blockIdx.x, m0 = b * RT_BM;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[RC_STAGES]), done = smem_u32(&bars[2 * RC_STAGES]);
   if (tid == 0) {
-    for (int s = 0; s < RS_STAGES; ++s) {
+    for (int s = 0; s < RC_STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -235,57 +266,96 @@ __global__ void __launch_bounds__(RS_THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < 64) bias_s[tid] = p.router_bias ? p.router_bias[64 * g + tid] : 0.0f;
-  for (int i = tid; i < NEXP; i += RS_THREADS) hist_s[i] = 0;
+  for (int i = tid; i < NEXP; i += RC_THREADS) {
+    bias_s[i] = p.router_bias ? p.router_bias[i] : 0.0f;
+    hist_s[i] = 0;
+    if (rank == 0) p.hist[b * NEXP + i] = 0;   // the other CTAs add to it after the cluster barriers
+  }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 64);
+    tmem_alloc(smem_u32(tmem_slot), 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  constexpr int NKB = HID / 64;
+  constexpr int NK = HID / 64 / RC_SPLIT;   // K steps of this CTA's quarter
+  const int kb0 = static_cast<int>(rank) * NK;
   int issued = 0;   // TMA producer: K steps whose loads it issued
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer: the block's x rows and this segment's 64 router rows
+    // ---- TMA producer: the block's x rows and all 256 router rows, K quarter `rank`
     tma_prefetch_desc(&tm_x);
-    tma_prefetch_desc(&tm_wr64);
-    for (int kb = 0; kb < NKB; ++kb) {
-      const int s = kb % RS_STAGES;
-      const uint32_t ph = (kb / RS_STAGES) & 1;
-      if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, abort_flag, p.wait_ns)) break;
-      uint8_t* st = smem + s * RS_STAGE_BYTES;
-      mbar_arrive_expect_tx(full0 + 8 * s, RS_STAGE_BYTES);
-      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kb * 64, m0);
-      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr64, full0 + 8 * s, kb * 64, 64 * g);
-      issued = kb + 1;
+    tma_prefetch_desc(&tm_wr);
+    for (int i = 0; i < NK; ++i) {
+      const int s = i % RC_STAGES;
+      if (!mbar_wait(empty0 + 8 * s, ((i / RC_STAGES) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) break;
+      uint8_t* st = smem + s * RT_STAGE_BYTES;
+      mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
+      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, (kb0 + i) * 64, m0);
+      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, (kb0 + i) * 64, 0);
+      issued = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
-    const uint32_t id_r = idesc_bf16(128, 64);
-    for (int kb = 0; kb < NKB; ++kb) {
-      const int s = kb % RS_STAGES;
-      const uint32_t ph = (kb / RS_STAGES) & 1;
-      if (!mbar_wait(full0 + 8 * s, ph, p.err, abort_flag, p.wait_ns)) break;
+    const uint32_t id_r = idesc_bf16(128, 256);
+    for (int i = 0; i < NK; ++i) {
+      const int s = i % RC_STAGES;
+      if (!mbar_wait(full0 + 8 * s, (i / RC_STAGES) & 1, p.err, abort_flag, p.wait_ns)) break;
       tc_fence_after();
-      const uint32_t a = smem_u32(smem + s * RS_STAGE_BYTES);
+      const uint32_t a = smem_u32(smem + s * RT_STAGE_BYTES);
       const uint32_t bb = a + RT_A_BYTES;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + kk * 32), id_r, (kb | kk) != 0);
+        umma_bf16(tmem, sdesc_sw128(a + kk * 32), sdesc_sw128(bb + kk * 32), id_r, (i | kk) != 0);
       umma_commit(empty0 + 8 * s);
     }
     umma_commit(done);   // also covers an early exit: all issued MMAs complete first
   }
   __syncwarp();
-
-  // ---- this segment's top 8 per token: warp w reads TMEM lane quarter w (32 tokens)
   bool ok = mbar_wait(done, 0, p.err, abort_flag, p.wait_ns);
   ok = __syncthreads_and(ok && !*abort_flag) != 0;
+  if (!ok) {
+    // a launch that gave up: copies and MMAs still in flight finish before the stage
+    // buffers are handed to the peers (the latest phase of each stage; bounded waits)
+    if (warp == 0 && lane == 0)
+      for (int i = (issued > RC_STAGES ? issued - RC_STAGES : 0); i < issued; ++i) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (!mbar_try_wait(full0 + 8 * (i % RC_STAGES), (i / RC_STAGES) & 1) &&
+               globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+        }
+      }
+    if (warp == 1 && lane == 0) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+      }
+    }
+    __syncwarp();
+  }
   tc_fence_after();
-  const int t = m0 + tid;
+  // ---- every CTA of the cluster is done with its stage buffers
+  cluster_sync();
+  if (ok) {
+    // warp w holds TMEM lanes 32w..32w+31 = tokens 32w.. of the block, owned by CTA w
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t dst = mapa_shared(smem_u32(recv + (rank * 32 + lane) * RC_ROW), static_cast<uint32_t>(warp));
+#pragma unroll 1
+    for (int c = 0; c < NEXP / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(lane_base + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_cluster_v4(dst + (c * 32 + 4 * j) * 4, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    }
+  }
+  tc_fence_before();
+  // ---- every partial has arrived
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+  // ---- warp g = expert segment g, lane = token 32 rank + lane of the block
   float tv[TOPK];
   int ti[TOPK];
 #pragma unroll
@@ -303,63 +373,35 @@ __global__ void __launch_bounds__(RS_THREADS, 1)
       }
     }
   };
-  if (ok) {
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int t = m0 + static_cast<int>(rank) * 32 + lane;
+  const int seg = warp;
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      uint32_t r[32];
-      tmem_ld32(lane_base + c * 32, r);
-      tmem_ld_wait();
+  for (int e4 = 0; e4 < 64; e4 += 4) {
+    const int e = seg * 64 + e4;
+    float4 acc = *reinterpret_cast<const float4*>(recv + lane * RC_ROW + e);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) insert(__uint_as_float(r[j]) + bias_s[c * 32 + j], 64 * g + c * 32 + j);
+    for (int q = 1; q < RC_SPLIT; ++q) {   // quarters in order
+      const float4 v = *reinterpret_cast<const float4*>(recv + (q * 32 + lane) * RC_ROW + e);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    insert(acc.x + bias_s[e], e);
+    insert(acc.y + bias_s[e + 1], e + 1);
+    insert(acc.z + bias_s[e + 2], e + 2);
+    insert(acc.w + bias_s[e + 3], e + 3);
+  }
+  if (seg > 0) {
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) {
+      cand_v[((seg - 1) * TOPK + k) * 32 + lane] = tv[k];
+      cand_e[((seg - 1) * TOPK + k) * 32 + lane] = ti[k];
     }
   }
-  if (t < p.T) {
-    int2* dst = p.cand + (static_cast<size_t>(t) * 4 + g) * TOPK;
-#pragma unroll
-    for (int k = 0; k < TOPK; ++k) dst[k] = make_int2(__float_as_int(tv[k]), ti[k]);
-  }
-  // TMEM is done with: free it before the merge
-  tc_fence_before();
   __syncthreads();
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    // a launch that gave up: copies still in flight land before shared memory goes away
-    for (int kb = (issued > RS_STAGES ? issued - RS_STAGES : 0); kb < issued; ++kb) {
-      const unsigned long long t0 = globaltimer_ns();
-      while (!mbar_try_wait(full0 + 8 * (kb % RS_STAGES), (kb / RS_STAGES) & 1) &&
-             globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
-      }
-    }
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    if (lane == 0 && *abort_flag) {
-      const unsigned long long t0 = globaltimer_ns();
-      while (!mbar_try_wait(done, 0) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
-      }
-    }
-    __syncwarp();
-    tmem_dealloc(tmem, 64);
-  }
-  __threadfence();   // publish this segment's lists before taking the ticket
-  __syncthreads();
-  if (tid == 0) *s_last = (atomicAdd(p.ticket + b, 1u) == 3u);
-  __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  // ---- the block's last CTA: the four segments' lists in segment order
-  if (t < p.T) {
-#pragma unroll
-    for (int k = 0; k < TOPK; ++k) { tv[k] = -INFINITY; ti[k] = NEXP; }
-    const int2* src = p.cand + static_cast<size_t>(t) * 4 * TOPK;
+  if (seg == 0 && t < p.T) {
 #pragma unroll 1
-    for (int sg = 0; sg < 4; ++sg) {
-      int2 c8[TOPK];
+    for (int sg = 0; sg < 3; ++sg)
 #pragma unroll
-      for (int k = 0; k < TOPK; ++k) c8[k] = __ldcg(src + sg * TOPK + k);
-#pragma unroll
-      for (int k = 0; k < TOPK; ++k) insert(__int_as_float(c8[k].x), c8[k].y);
-    }
+      for (int k = 0; k < TOPK; ++k) insert(cand_v[(sg * TOPK + k) * 32 + lane], cand_e[(sg * TOPK + k) * 32 + lane]);
     // fewer than 8 ordered logits (NaN input): record it and route to expert 0 ..
     if (ti[TOPK - 1] >= NEXP) {
       atomicOr(p.err, ERRBIT_BOUNDS);
@@ -379,8 +421,8 @@ __global__ void __launch_bounds__(RS_THREADS, 1)
     }
   }
   __syncthreads();
-  for (int i = tid; i < NEXP; i += RS_THREADS) p.hist[b * NEXP + i] = hist_s[i];
-  if (tid == 0) p.ticket[b] = 0u;   // ready for the next launch (every CTA of the block took its ticket)
+  for (int i = tid; i < NEXP; i += RC_THREADS)
+    if (hist_s[i] != 0) atomicAdd(p.hist + b * NEXP + i, hist_s[i]);
 }
 
 // 1024 threads: thread (q, e) = expert e's router blocks of quarter q (the per-expert
@@ -647,10 +689,10 @@ cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_split(const CUtensorMap& tm_x, const CUtensorMap& tm_wr64, const RouteParams& p,
-                                cudaStream_t s) {
+cudaError_t launch_router_cluster(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
+                                  cudaStream_t s) {
   const int nblk = (p.T + RT_BM - 1) / RT_BM;
-  router_split_kernel<<<dim3(nblk, 4), RS_THREADS, RS_SMEM, s>>>(tm_x, tm_wr64, p);
+  router_cluster_kernel<<<dim3(nblk, RC_SPLIT), RC_THREADS, RC_SMEM, s>>>(tm_x, tm_wr, p);
   return cudaGetLastError();
 }
 
@@ -666,7 +708,7 @@ cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
 
 cudaError_t set_router_attributes() {
   cudaError_t e = cudaFuncSetAttribute(router_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(router_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RS_SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RC_SMEM);
   return e;
 }
 
