@@ -142,6 +142,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
+// ----------------------------------------------------------------- dependent launch
+// The prefill kernels are launched with programmatic stream serialisation: the next
+// kernel of the stream is launched as the CTAs of the one before it finish, before that
+// kernel's memory writes are flushed, and sets up its barriers and TMEM meanwhile.
+// grid_dep_wait() holds the calling thread until every earlier kernel of the stream has
+// completed and its writes are visible; each kernel calls it, in every thread, before its
+// first access to memory that another kernel writes or reads (activations, routing
+// tables, workspace).  (No kernel signals its dependents early: CTAs of the next kernel
+// that wait on SMs while this one runs measured slower than letting them in at exit.)
+// Launched without the attribute, the wait does nothing.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

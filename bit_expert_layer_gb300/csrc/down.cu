@@ -64,7 +64,6 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   int* s_cnt = s_off + (NEXP + 2);
   constexpr int SCHED_OFF = (1024 + DN_STG_BYTES + GX_TAB_BYTES + 15) / 16 * 16;
   int4* sched = reinterpret_cast<int4*>(misc + SCHED_OFF);   // [DN_SCHED_CAP] this CTA's tiles
-  stage_tables(s_off, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -109,6 +108,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();   // the routing tables and activations come from the kernels before this one
+  stage_tables(s_off, p.offsets, p.counts);
+  __syncthreads();
   const int ntiles = build_schedule(sched, DN_SCHED_CAP, p.blocks, s_off, s_cnt, DN_MBLK, p.T, p.err, false,
                                     p.small_apart ? BLOCKS_BIG : BLOCKS_ALL);
   __syncthreads();
@@ -424,7 +426,6 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   int* s_off = reinterpret_cast<int*>(misc + 1024);                   // row tables (GX_TAB_BYTES)
   int* s_cnt = s_off + (NEXP + 2);
   int4* sched = reinterpret_cast<int4*>(misc + 1024 + (GX_TAB_BYTES + 15) / 16 * 16);   // [DS_SCHED_CAP]
-  stage_tables(s_off, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -469,6 +470,9 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();   // the routing tables and activations come from the kernels before this one
+  stage_tables(s_off, p.offsets, p.counts);
+  __syncthreads();
   const int ntiles =
       build_schedule(sched, DS_SCHED_CAP, p.blocks, s_off, s_cnt, DS_PAIRS, p.T, p.err, false, BLOCKS_SMALL);
   __syncthreads();
@@ -685,20 +689,14 @@ __global__ void __launch_bounds__(DN_THREADS, 1)
 
 cudaError_t launch_down(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap,
                         const CUtensorMap& ymap, const DownParams& p, int grid, cudaStream_t s) {
-  if (p.wait_ns == WAIT_LIMIT_NS)
-    down_kernel<false><<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, ymap, p);
-  else
-    down_kernel<true><<<grid, DN_THREADS, DN_SMEM, s>>>(qd, sqd, hmap, ymap, p);
-  return cudaGetLastError();
+  return launch_pdl(p.wait_ns == WAIT_LIMIT_NS ? down_kernel<false> : down_kernel<true>, grid, DN_THREADS, DN_SMEM,
+                    s, qd, sqd, hmap, ymap, p);
 }
 
 cudaError_t launch_down_swap(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap, const DownParams& p,
                              int grid, cudaStream_t s) {
-  if (p.wait_ns == WAIT_LIMIT_NS)
-    down_swap_kernel<false><<<grid, DN_THREADS, DS_SMEM, s>>>(qd, sqd, hmap, p);
-  else
-    down_swap_kernel<true><<<grid, DN_THREADS, DS_SMEM, s>>>(qd, sqd, hmap, p);
-  return cudaGetLastError();
+  return launch_pdl(p.wait_ns == WAIT_LIMIT_NS ? down_swap_kernel<false> : down_swap_kernel<true>, grid, DN_THREADS,
+                    DS_SMEM, s, qd, sqd, hmap, p);
 }
 
 cudaError_t set_down_attributes() {

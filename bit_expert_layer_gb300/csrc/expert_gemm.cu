@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   int* s_tok = reinterpret_cast<int*>(misc + 512 + GX_TAB_BYTES);   // [GU_GW][GU_GROWS] token ids
   int4* sched = reinterpret_cast<int4*>(s_tok + GU_GW * GU_GROWS);   // [GU_SCHED_CAP] this CTA's tiles
   uint8_t* stg = misc + STG_OFF;                                       // [4 warps][GU_STG_BUFS][32][32] bf16
-  stage_tables(s_off, p.offsets, p.counts);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = smem_u32(bars);
@@ -125,6 +124,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();   // the routing tables and activations come from the kernels before this one
+  stage_tables(s_off, p.offsets, p.counts);
+  __syncthreads();
   const int ntiles = build_schedule(sched, GU_SCHED_CAP, p.blocks, s_off, s_cnt, GU_MBLK, p.T, p.err, true, BLOCKS_ALL);
   __syncthreads();
   constexpr int NKB = HID / 64;
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
                                                       const __nv_bfloat16* x, __nv_bfloat16* out, int T,
                                                       int residual, NextLayerIn nx) {
   const int t = blockIdx.x, c = threadIdx.x;
+  grid_dep_wait();   // y, the slot tables and x come from the kernels before this one
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -554,17 +557,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 cudaError_t launch_gateup(const CUtensorMap& qg, const CUtensorMap& qu, const CUtensorMap& sqg,
                           const CUtensorMap& squ, const CUtensorMap& hs, const GateUpParams& p, int grid,
                           cudaStream_t s) {
-  if (p.wait_ns == WAIT_LIMIT_NS)
-    gateup_kernel<false><<<grid, GU_THREADS, GU_SMEM, s>>>(qg, qu, sqg, squ, hs, p);
-  else
-    gateup_kernel<true><<<grid, GU_THREADS, GU_SMEM, s>>>(qg, qu, sqg, squ, hs, p);
-  return cudaGetLastError();
+  return launch_pdl(p.wait_ns == WAIT_LIMIT_NS ? gateup_kernel<false> : gateup_kernel<true>, grid, GU_THREADS,
+                    GU_SMEM, s, qg, qu, sqg, squ, hs, p);
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int* slot_row, const float* row_w, const __nv_bfloat16* x,
                            __nv_bfloat16* out, int T, int residual, const NextLayerIn& nx, cudaStream_t s) {
-  combine_kernel<<<T, 256, 0, s>>>(y, slot_row, row_w, x, out, T, residual, nx);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, T, 256, 0, s, y, slot_row, row_w, x, out, T, residual, nx);
 }
 
 cudaError_t set_gemm_attributes() {

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();   // x (and, in a stack, the workspace) come from the kernels before this one
   constexpr int NKB = HID / 64;
   int issued = 0;   // TMA producer: K steps whose loads it issued
 
@@ -269,7 +270,6 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   for (int i = tid; i < NEXP; i += RC_THREADS) {
     bias_s[i] = p.router_bias ? p.router_bias[i] : 0.0f;
     hist_s[i] = 0;
-    if (rank == 0) p.hist[b * NEXP + i] = 0;   // the other CTAs add to it after the cluster barriers
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 256);
@@ -279,6 +279,9 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();   // x (and, in a stack, the workspace) come from the kernels before this one
+  if (rank == 0)   // the other CTAs add to the block's histogram row after the cluster barriers
+    for (int i = tid; i < NEXP; i += RC_THREADS) p.hist[b * NEXP + i] = 0;
   constexpr int NK = HID / 64 / RC_SPLIT;   // K steps of this CTA's quarter
   const int kb0 = static_cast<int>(rank) * NK;
   int issued = 0;   // TMA producer: K steps whose loads it issued
@@ -437,6 +440,7 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   __shared__ int s_part[NEXP + 1];   // each expert's partial block (the shared expert last)
   const int e = threadIdx.x % NEXP, q = threadIdx.x / NEXP, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool lead = q == 0;
+  grid_dep_wait();   // the histograms come from the router
   const int per_q = (p.nblk + SCAN_Q - 1) / SCAN_Q;
   const int b_lo = q * per_q, b_hi = min(p.nblk, b_lo + per_q);
   constexpr int CH = 8;   // histogram entries loaded together (independent loads in flight)
@@ -551,6 +555,7 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
   __shared__ int wh[8][NEXP];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int slot0 = b * SLOTS;
+  grid_dep_wait();   // the routing and the bases come from the kernels before this one
   const int nslots = min(SLOTS, p.T * TOPK - slot0);
   const int n8 = 8 * p.T;
   if (blockIdx.y == 0) {
@@ -671,6 +676,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ xn, int T) {
   __shared__ float s_warp[8];
   const int row = blockIdx.x, c = threadIdx.x;
+  grid_dep_wait();   // x may come from the kernel before this one
   const uint4 v = ldg_nc_v4(x + static_cast<size_t>(row) * HID + c * 8);
   const float r = row_inv_rms(v, s_warp);
   *reinterpret_cast<uint4*>(xn + static_cast<size_t>(row) * HID + c * 8) = rms_scale8(v, ldg_nc_v4(w + c * 8), r);
@@ -678,32 +684,27 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
 
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* w, __nv_bfloat16* xn, int T,
                            cudaStream_t s) {
-  rmsnorm_kernel<<<T, 256, 0, s>>>(x, w, xn, T);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, T, 256, 0, s, x, w, xn, T);
 }
 
 cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
                                   cudaStream_t s) {
   const int nblk = (p.T + RT_BM - 1) / RT_BM;
-  router_prefill_kernel<<<nblk, RT_THREADS, RT_SMEM, s>>>(tm_x, tm_wr, p);
-  return cudaGetLastError();
+  return launch_pdl(router_prefill_kernel, nblk, RT_THREADS, RT_SMEM, s, tm_x, tm_wr, p);
 }
 
 cudaError_t launch_router_cluster(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
                                   cudaStream_t s) {
   const int nblk = (p.T + RT_BM - 1) / RT_BM;
-  router_cluster_kernel<<<dim3(nblk, RC_SPLIT), RC_THREADS, RC_SMEM, s>>>(tm_x, tm_wr, p);
-  return cudaGetLastError();
+  return launch_pdl(router_cluster_kernel, dim3(nblk, RC_SPLIT), RC_THREADS, RC_SMEM, s, tm_x, tm_wr, p);
 }
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
-  route_scan_kernel<<<1, SCAN_Q * NEXP, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(route_scan_kernel, 1, SCAN_Q * NEXP, 0, s, p);
 }
 
 cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
-  route_scatter_kernel<<<dim3(nblk, p.gather ? SC_SPLIT : 1), SC_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(route_scatter_kernel, dim3(nblk, p.gather ? SC_SPLIT : 1), SC_THREADS, 0, s, p);
 }
 
 cudaError_t set_router_attributes() {
