@@ -44,8 +44,7 @@ constexpr int RT_THREADS = 128 * RT_SEGS;
 constexpr int RC_MAX_T = 4096;
 constexpr int RC_SPLIT = 4;
 constexpr int RC_STAGES = 4;
-constexpr int RC_ROW = NEXP + 4;                    // floats per received partial row
-constexpr int RC_SMEM = RC_STAGES * RT_STAGE_BYTES + 1024 + 8192 + 1024;
+constexpr int RC_SMEM = RC_STAGES * RT_STAGE_BYTES + 1024 + 10240 + 1024;
 constexpr int RC_THREADS = 128;
 
 

@@ -244,14 +244,14 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
   float* bias_s = reinterpret_cast<float*>(misc + 256);                // [256]
   int* hist_s = reinterpret_cast<int*>(misc + 256 + NEXP * 4);         // [256]
-  float* cand_v = reinterpret_cast<float*>(misc + 256 + NEXP * 8);     // [3 segments][8][32 tokens]
-  int* cand_e = reinterpret_cast<int*>(cand_v + 3 * TOPK * 32);
-  // the four partials of this CTA's 32 tokens, [quarter][token][RC_ROW], over the stage
-  // buffers once every MMA of the cluster is done (row stride 1040 bytes: the 16-byte
-  // accesses of 8 consecutive tokens fall in distinct banks)
-  float* recv = reinterpret_cast<float*>(smem);
-  static_assert(RC_SPLIT * 32 * RC_ROW * 4 <= RC_STAGES * RT_STAGE_BYTES, "partials fit the stage buffers");
-  static_assert(256 + NEXP * 8 + 2 * 3 * TOPK * 32 * 4 + 1024 <= RC_SMEM - RC_STAGES * RT_STAGE_BYTES, "router smem");
+  float* cand_v = reinterpret_cast<float*>(misc + 256 + NEXP * 8);     // [4 segments][8][32 tokens]
+  int* cand_e = reinterpret_cast<int*>(cand_v + 4 * TOPK * 32);
+  // the four partials of this CTA's 32 tokens over the stage buffers once every MMA of
+  // the cluster is done: float4 [quarter][expert / 4][token], so that a warp's 16-byte
+  // stores into a peer, and its loads here, cover 512 contiguous bytes
+  float4* recv = reinterpret_cast<float4*>(smem);
+  static_assert(RC_SPLIT * (NEXP / 4) * 32 * 16 <= RC_STAGES * RT_STAGE_BYTES, "partials fit the stage buffers");
+  static_assert(256 + NEXP * 8 + 2 * 4 * TOPK * 32 * 4 + 1024 <= RC_SMEM - RC_STAGES * RT_STAGE_BYTES, "router smem");
   static_assert(RC_THREADS == 128 && NEXP == 4 * 64 && RT_BM == RC_SPLIT * 32, "one warp per token quarter / segment");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -341,14 +341,15 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   if (ok) {
     // warp w holds TMEM lanes 32w..32w+31 = tokens 32w.. of the block, owned by CTA w
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t dst = mapa_shared(smem_u32(recv + (rank * 32 + lane) * RC_ROW), static_cast<uint32_t>(warp));
+    const uint32_t dst = mapa_shared(smem_u32(recv + rank * (NEXP / 4) * 32 + lane), static_cast<uint32_t>(warp));
 #pragma unroll 1
     for (int c = 0; c < NEXP / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(lane_base + c * 32, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 8; ++j) st_cluster_v4(dst + (c * 32 + 4 * j) * 4, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      for (int j = 0; j < 8; ++j)   // experts 32c + 4j .. + 3
+        st_cluster_v4(dst + (c * 8 + j) * 32 * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
     }
   }
   tc_fence_before();
@@ -378,33 +379,56 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   };
   const int t = m0 + static_cast<int>(rank) * 32 + lane;
   const int seg = warp;
+  // eight experts per pass, all loads first: the four quarters summed in order, then the bias
 #pragma unroll 1
-  for (int e4 = 0; e4 < 64; e4 += 4) {
-    const int e = seg * 64 + e4;
-    float4 acc = *reinterpret_cast<const float4*>(recv + lane * RC_ROW + e);
+  for (int e8 = 0; e8 < 64; e8 += 8) {
+    const int e = seg * 64 + e8;
+    float4 a[2][RC_SPLIT];
 #pragma unroll
-    for (int q = 1; q < RC_SPLIT; ++q) {   // quarters in order
-      const float4 v = *reinterpret_cast<const float4*>(recv + (q * 32 + lane) * RC_ROW + e);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int q = 0; q < RC_SPLIT; ++q) a[h][q] = recv[(q * (NEXP / 4) + e / 4 + h) * 32 + lane];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float4 acc = a[h][0];
+#pragma unroll
+      for (int q = 1; q < RC_SPLIT; ++q) {
+        acc.x += a[h][q].x; acc.y += a[h][q].y; acc.z += a[h][q].z; acc.w += a[h][q].w;
+      }
+      const float4 bv = *reinterpret_cast<const float4*>(bias_s + e + 4 * h);
+      insert(acc.x + bv.x, e + 4 * h);
+      insert(acc.y + bv.y, e + 4 * h + 1);
+      insert(acc.z + bv.z, e + 4 * h + 2);
+      insert(acc.w + bv.w, e + 4 * h + 3);
     }
-    insert(acc.x + bias_s[e], e);
-    insert(acc.y + bias_s[e + 1], e + 1);
-    insert(acc.z + bias_s[e + 2], e + 2);
-    insert(acc.w + bias_s[e + 3], e + 3);
   }
-  if (seg > 0) {
 #pragma unroll
-    for (int k = 0; k < TOPK; ++k) {
-      cand_v[((seg - 1) * TOPK + k) * 32 + lane] = tv[k];
-      cand_e[((seg - 1) * TOPK + k) * 32 + lane] = ti[k];
-    }
+  for (int k = 0; k < TOPK; ++k) {
+    cand_v[(seg * TOPK + k) * 32 + lane] = tv[k];
+    cand_e[(seg * TOPK + k) * 32 + lane] = ti[k];
   }
   __syncthreads();
   if (seg == 0 && t < p.T) {
-#pragma unroll 1
-    for (int sg = 0; sg < 3; ++sg)
+    // the four segments' lists (each in descending order, equal logits by ascending
+    // expert) merged: each step takes the largest head, the lowest segment on equal
+    // values -- the order of one strictly-greater insertion pass over all 256 experts
+    int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
+    float h0 = cand_v[(0 * TOPK) * 32 + lane], h1 = cand_v[(1 * TOPK) * 32 + lane];
+    float h2 = cand_v[(2 * TOPK) * 32 + lane], h3 = cand_v[(3 * TOPK) * 32 + lane];
 #pragma unroll
-      for (int k = 0; k < TOPK; ++k) insert(cand_v[(sg * TOPK + k) * 32 + lane], cand_e[(sg * TOPK + k) * 32 + lane]);
+    for (int k = 0; k < TOPK; ++k) {
+      int bs = 0;
+      float bv = h0;
+      if (h1 > bv) { bv = h1; bs = 1; }
+      if (h2 > bv) { bv = h2; bs = 2; }
+      if (h3 > bv) { bv = h3; bs = 3; }
+      const int pk = bs == 0 ? p0 : bs == 1 ? p1 : bs == 2 ? p2 : p3;
+      tv[k] = bv;
+      ti[k] = cand_e[(bs * TOPK + pk) * 32 + lane];
+      const int nx = pk + 1;
+      const float hn = nx < TOPK ? cand_v[(bs * TOPK + nx) * 32 + lane] : -INFINITY;
+      if (bs == 0) { p0 = nx; h0 = hn; } else if (bs == 1) { p1 = nx; h1 = hn; } else if (bs == 2) { p2 = nx; h2 = hn; } else { p3 = nx; h3 = hn; }
+    }
     // fewer than 8 ordered logits (NaN input): record it and route to expert 0 ..
     if (ti[TOPK - 1] >= NEXP) {
       atomicOr(p.err, ERRBIT_BOUNDS);
