@@ -76,7 +76,8 @@ constexpr int DL_REGS_SPLIT = DL_THREADS * DL_REGS_COMPUTE + DL_COPY * DL_REGS_C
 constexpr int DL_ROWS_C = 16;                 // output rows per CTA in phase C
 constexpr int DL_CTAS_C = HID / DL_ROWS_C;    // 128 CTAs carry phase C
 constexpr int NROW_A = NEXP + 1;              // router rows + the shared-expert gate row
-constexpr unsigned DL_POLL_NS = 100;          // pause between polls of a stale tagged word
+constexpr unsigned DL_POLL_NS = 0;            // pause between polls of a stale tagged word (none:
+                                               // 17.40 against 17.55 us per layer at T = 1 with 100 ns)
 // gate/up unit in a slot: 8 gate rows, 8 up rows (1 KB each), then the scales and biases of
 // both (8 x 32 bf16 each)
 constexpr int U_ROWB = HID / 2;                        // 1024 bytes of packed codes per row
@@ -203,7 +204,7 @@ struct PollClock {
       atomicExch(cx.abort_word, 1u);
       return false;
     }
-    __nanosleep(DL_POLL_NS);   // keeps the polling of 152 CTAs from crowding the L2 slices
+    if (DL_POLL_NS != 0) __nanosleep(DL_POLL_NS);
     return true;
   }
 };

@@ -79,8 +79,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
       if (!mbar_wait(empty0 + 8 * s, ph ^ 1, p.err, abort_flag, p.wait_ns)) break;
       uint8_t* st = smem + s * RT_STAGE_BYTES;
       mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
-      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kb * 64, m0);
-      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kb * 64, 0);
+      // the CTAs start at different K steps (7 is prime to the 32 steps), so that they do
+      // not all read the same 32 KB of the router matrix from the same L2 slices at once
+      const int kr = (kb + static_cast<int>(blockIdx.x) * 7) % NKB;
+      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kr * 64, m0);
+      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kr * 64, 0);
       issued = kb + 1;
     }
   } else if (warp == 1 && lane == 0) {
@@ -295,8 +298,11 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
       if (!mbar_wait(empty0 + 8 * s, ((i / RC_STAGES) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) break;
       uint8_t* st = smem + s * RT_STAGE_BYTES;
       mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
-      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, (kb0 + i) * 64, m0);
-      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, (kb0 + i) * 64, 0);
+      // the clusters start at different K steps of their quarter, so that the CTAs of one
+      // quarter do not all read the same router rows from the same L2 slices at once
+      const int kr = kb0 + (i + static_cast<int>(blockIdx.x)) % NK;
+      tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kr * 64, m0);
+      tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kr * 64, 0);
       issued = i + 1;
     }
   } else if (warp == 1 && lane == 0) {
