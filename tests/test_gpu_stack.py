@@ -112,6 +112,30 @@ def _teacher_forced(oracle, lib, hosts, layers, x_np, sample, label):
     return cur, per_layer
 
 
+def test_short_prefill_stack_T1000(oracle, lib):
+    """Four stacked layers at T=1000, the size where the router runs as four-CTA clusters
+    and the small token blocks take the swapped down GEMM: the stack entry (each layer's
+    combine writing the next layer's normalised input, its interleaved copy and its shared
+    gate) equals the layer-by-layer computation bit for bit, and every layer follows the
+    oracle on its own input (teacher-forced) for a sample of tokens."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(4) as ex:
+        hosts = list(ex.map(lambda l: synth.stack_layer(l, threads=2), range(4)))
+    T = 1000
+    ws = lib.new_workspace(T)
+    layers = [lib.MoELayer(lib.DeviceWeights(h), T, workspace=ws) for h in hosts]
+    stack = lib.MoEStack(layers)
+    x_np = synth.make_x(3, T)
+    x = to_dev(x_np)
+    stack.forward_(x)
+    torch.cuda.synchronize()
+    assert layers[0].get_error() == 0
+    rng = np.random.default_rng(1000)
+    sample = np.unique(np.concatenate([rng.choice(T, 40, replace=False), [0, T - 2, T - 1]]))
+    final, _ = _teacher_forced(oracle, lib, hosts, layers, x_np, sample, "stack prefill T=1000")
+    assert torch.equal(final.view(torch.int16), x.view(torch.int16))
+
+
 @pytest.fixture(scope="module")
 def stack40(lib):
     from concurrent.futures import ThreadPoolExecutor
