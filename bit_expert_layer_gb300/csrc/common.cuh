@@ -39,13 +39,15 @@ constexpr int RT_SEGS = 4;                          // expert segments scanned b
 constexpr int RT_CAND_BYTES = (RT_SEGS - 1) * 8 * RT_BM * 8;   // top-8 lists of segments 1-3
 constexpr int RT_SMEM = RT_STAGES * RT_STAGE_BYTES + 1024 + 3072 + RT_CAND_BYTES;
 constexpr int RT_THREADS = 128 * RT_SEGS;
-// router for T <= RC_MAX_T: a cluster of RC_SPLIT CTAs per 128-token block, each over a
-// quarter of K (48 KB stages); the partial logits meet in distributed shared memory
+// cluster router: a cluster of S CTAs per 128-token block, each over a part of K (48 KB
+// stages); the partial logits meet in distributed shared memory.  S = 4 up to RC_MAX_T
+// tokens, S = 2 up to RC2_MAX_T; above, router_prefill_kernel (one CTA per block, whole K)
 constexpr int RC_MAX_T = 4096;
-constexpr int RC_SPLIT = 4;
+constexpr int RC2_MAX_T = 8192;
 constexpr int RC_STAGES = 4;
-constexpr int RC_SMEM = RC_STAGES * RT_STAGE_BYTES + 1024 + 10240 + 1024;
-constexpr int RC_THREADS = 128;
+__host__ __device__ constexpr int rc_threads(int S) { return 4 * (RT_BM / S); }
+__host__ __device__ constexpr int rc_misc(int S) { return 256 + NEXP * 8 + 2 * 4 * TOPK * (RT_BM / S) * 4; }
+__host__ __device__ constexpr int rc_smem(int S) { return RC_STAGES * RT_STAGE_BYTES + 1024 + rc_misc(S) + 1024; }
 
 
 // Grouped expert GEMMs: 128 weight rows (M) x up to 256 tokens (N) per tile, K step 64

@@ -335,12 +335,12 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
   if (!encode_bf16_rows(&tm_x, x, HID, T, RT_BM)) return MOE_ERR_CUDA;
   RouteParams rp{static_cast<const __nv_bfloat16*>(x), T, L->w.router_bias, L->topk_idx, L->topk_w, L->hist, L->err,
                  wait_limit_ns()};
-  // up to RC_MAX_T tokens a token block's contraction is cut in four K quarters, one CTA
-  // of a cluster each (four times the CTAs, a quarter of the K steps each)
+  // up to RC2_MAX_T tokens a token block's contraction is cut in K parts, one CTA of a
+  // cluster each (four parts up to RC_MAX_T tokens, two above)
   MOE_TRY(timed(K_ROUTER, s, L->err,
                 [&] {
-                  return T <= RC_MAX_T ? launch_router_cluster(tm_x, L->tm_wr, rp, s)
-                                       : launch_router_prefill(tm_x, L->tm_wr, rp, s);
+                  return T <= RC2_MAX_T ? launch_router_cluster(tm_x, L->tm_wr, rp, s)
+                                        : launch_router_prefill(tm_x, L->tm_wr, rp, s);
                 }),
           "router launch");
   ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->blocks};

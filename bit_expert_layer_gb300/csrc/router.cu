@@ -203,15 +203,17 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   }
 }
 
-// router_cluster_kernel: the same routing for T <= RC_MAX_T, where one CTA per 128
-// tokens would leave most SMs idle.  The contraction over the 2048 hidden columns is cut
-// in RC_SPLIT = 4 quarters: a cluster of four CTAs per token block, CTA r accumulating
-// quarter r of K for all 256 experts (MMA N = 256, 8 K steps).  The partial logits move
-// through distributed shared memory -- CTA r sends the rows of tokens 32j..32j+31 to
-// CTA j -- and CTA j adds the four partials in quarter order (a fixed order, so the
-// result does not depend on timing), adds the bias and keeps the top 8 of each of its 32
-// tokens as router_prefill_kernel does: four 64-expert segments (one warp each) with
-// strictly-greater insertion over ascending experts, merged in segment order.  Rank 0
+// router_cluster_kernel<S>: the same routing where one CTA per 128 tokens would leave
+// SMs idle.  The contraction over the 2048 hidden columns is cut in S parts: a cluster of
+// S CTAs per token block, CTA r accumulating part r of K for all 256 experts (MMA N = 256,
+// 32/S K steps).  The partial logits move through distributed shared memory -- CTA r
+// sends the rows of tokens (128/S) j.. to CTA j -- and CTA j adds the S partials in part
+// order (a fixed order, so the result does not depend on timing), adds the bias and keeps
+// the top 8 of each of its 128/S tokens as router_prefill_kernel does: four 64-expert
+// segments with strictly-greater insertion over ascending experts, merged in segment
+// order.  S = 4 up to RC_MAX_T tokens, S = 2 up to RC2_MAX_T (measured per-launch: T =
+// 8192 25 us against 31 for router_prefill_kernel; at T = 16384, 3.4 waves of clusters,
+// 48 against 35).  Rank 0
 // clears the block's histogram row before the first cluster barrier; every CTA adds its
 // tokens' counts after the second.  Every thread passes both cluster barriers on every
 // path (a launch that gave up included), so no CTA waits for a peer that has left.
@@ -236,9 +238,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1)
+template <int S>
+__global__ void __cluster_dims__(1, S, 1) __launch_bounds__(rc_threads(S), 1)
     router_cluster_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wr,
                           RouteParams p) {
+  constexpr int TPO = RT_BM / S;        // tokens whose top 8 this CTA selects
+  constexpr int NTH = rc_threads(S);    // 4 segments x TPO tokens
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* misc = smem + RC_STAGES * RT_STAGE_BYTES;
@@ -247,15 +252,15 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
   float* bias_s = reinterpret_cast<float*>(misc + 256);                // [256]
   int* hist_s = reinterpret_cast<int*>(misc + 256 + NEXP * 4);         // [256]
-  float* cand_v = reinterpret_cast<float*>(misc + 256 + NEXP * 8);     // [4 segments][8][32 tokens]
-  int* cand_e = reinterpret_cast<int*>(cand_v + 4 * TOPK * 32);
-  // the four partials of this CTA's 32 tokens over the stage buffers once every MMA of
-  // the cluster is done: float4 [quarter][expert / 4][token], so that a warp's 16-byte
-  // stores into a peer, and its loads here, cover 512 contiguous bytes
+  float* cand_v = reinterpret_cast<float*>(misc + 256 + NEXP * 8);     // [4 segments][8][TPO tokens]
+  int* cand_e = reinterpret_cast<int*>(cand_v + 4 * TOPK * TPO);
+  // the S partials of this CTA's TPO tokens over the stage buffers once every MMA of the
+  // cluster is done: float4 [part][expert / 4][token], so that a warp's 16-byte stores
+  // into a peer, and its loads here, cover 512 contiguous bytes
   float4* recv = reinterpret_cast<float4*>(smem);
-  static_assert(RC_SPLIT * (NEXP / 4) * 32 * 16 <= RC_STAGES * RT_STAGE_BYTES, "partials fit the stage buffers");
-  static_assert(256 + NEXP * 8 + 2 * 4 * TOPK * 32 * 4 + 1024 <= RC_SMEM - RC_STAGES * RT_STAGE_BYTES, "router smem");
-  static_assert(RC_THREADS == 128 && NEXP == 4 * 64 && RT_BM == RC_SPLIT * 32, "one warp per token quarter / segment");
+  static_assert(S * (NEXP / 4) * TPO * 16 <= RC_STAGES * RT_STAGE_BYTES, "partials fit the stage buffers");
+  static_assert(rc_misc(S) + 1024 <= rc_smem(S) - RC_STAGES * RT_STAGE_BYTES, "router smem");
+  static_assert((S == 2 || S == 4) && NEXP == 4 * 64 && TPO % 32 == 0, "whole warps per token group and segment");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, m0 = b * RT_BM;
@@ -270,7 +275,7 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < NEXP; i += RC_THREADS) {
+  for (int i = tid; i < NEXP; i += NTH) {
     bias_s[i] = p.router_bias ? p.router_bias[i] : 0.0f;
     hist_s[i] = 0;
   }
@@ -284,13 +289,13 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   const uint32_t tmem = *tmem_slot;
   grid_dep_wait();   // x (and, in a stack, the workspace) come from the kernels before this one
   if (rank == 0)   // the other CTAs add to the block's histogram row after the cluster barriers
-    for (int i = tid; i < NEXP; i += RC_THREADS) p.hist[b * NEXP + i] = 0;
-  constexpr int NK = HID / 64 / RC_SPLIT;   // K steps of this CTA's quarter
+    for (int i = tid; i < NEXP; i += NTH) p.hist[b * NEXP + i] = 0;
+  constexpr int NK = HID / 64 / S;   // K steps of this CTA's part
   const int kb0 = static_cast<int>(rank) * NK;
   int issued = 0;   // TMA producer: K steps whose loads it issued
 
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer: the block's x rows and all 256 router rows, K quarter `rank`
+    // ---- TMA producer: the block's x rows and all 256 router rows, K part `rank`
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_wr);
     for (int i = 0; i < NK; ++i) {
@@ -298,8 +303,8 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
       if (!mbar_wait(empty0 + 8 * s, ((i / RC_STAGES) & 1) ^ 1, p.err, abort_flag, p.wait_ns)) break;
       uint8_t* st = smem + s * RT_STAGE_BYTES;
       mbar_arrive_expect_tx(full0 + 8 * s, RT_STAGE_BYTES);
-      // the clusters start at different K steps of their quarter, so that the CTAs of one
-      // quarter do not all read the same router rows from the same L2 slices at once
+      // the clusters start at different K steps of their part, so that the CTAs of one
+      // part do not all read the same router rows from the same L2 slices at once
       const int kr = kb0 + (i + static_cast<int>(blockIdx.x)) % NK;
       tma_load_2d(smem_u32(st), &tm_x, full0 + 8 * s, kr * 64, m0);
       tma_load_2d(smem_u32(st + RT_A_BYTES), &tm_wr, full0 + 8 * s, kr * 64, 0);
@@ -344,10 +349,12 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   tc_fence_after();
   // ---- every CTA of the cluster is done with its stage buffers
   cluster_sync();
-  if (ok) {
-    // warp w holds TMEM lanes 32w..32w+31 = tokens 32w.. of the block, owned by CTA w
+  if (ok && warp < 4) {
+    // warp w holds TMEM lanes 32w..32w+31 = tokens 32w.. of the block, owned by CTA
+    // 32w / TPO (local tokens 32w % TPO ..)
+    const int tq = 32 * warp + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t dst = mapa_shared(smem_u32(recv + rank * (NEXP / 4) * 32 + lane), static_cast<uint32_t>(warp));
+    const uint32_t dst = mapa_shared(smem_u32(recv + rank * (NEXP / 4) * TPO + tq % TPO), static_cast<uint32_t>(tq / TPO));
 #pragma unroll 1
     for (int c = 0; c < NEXP / 32; ++c) {
       uint32_t r[32];
@@ -355,7 +362,7 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
       tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 8; ++j)   // experts 32c + 4j .. + 3
-        st_cluster_v4(dst + (c * 8 + j) * 32 * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        st_cluster_v4(dst + (c * 8 + j) * TPO * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
     }
   }
   tc_fence_before();
@@ -365,7 +372,7 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
-  // ---- warp g = expert segment g, lane = token 32 rank + lane of the block
+  // ---- thread: expert segment tid / TPO, local token tid % TPO (token TPO rank + that)
   float tv[TOPK];
   int ti[TOPK];
 #pragma unroll
@@ -383,22 +390,22 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
       }
     }
   };
-  const int t = m0 + static_cast<int>(rank) * 32 + lane;
-  const int seg = warp;
+  const int lt = tid % TPO, seg = tid / TPO;
+  const int t = m0 + static_cast<int>(rank) * TPO + lt;
   // eight experts per pass, all loads first: the four quarters summed in order, then the bias
 #pragma unroll 1
   for (int e8 = 0; e8 < 64; e8 += 8) {
     const int e = seg * 64 + e8;
-    float4 a[2][RC_SPLIT];
+    float4 a[2][S];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int q = 0; q < RC_SPLIT; ++q) a[h][q] = recv[(q * (NEXP / 4) + e / 4 + h) * 32 + lane];
+      for (int q = 0; q < S; ++q) a[h][q] = recv[(q * (NEXP / 4) + e / 4 + h) * TPO + lt];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float4 acc = a[h][0];
 #pragma unroll
-      for (int q = 1; q < RC_SPLIT; ++q) {
+      for (int q = 1; q < S; ++q) {
         acc.x += a[h][q].x; acc.y += a[h][q].y; acc.z += a[h][q].z; acc.w += a[h][q].w;
       }
       const float4 bv = *reinterpret_cast<const float4*>(bias_s + e + 4 * h);
@@ -410,8 +417,8 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
   }
 #pragma unroll
   for (int k = 0; k < TOPK; ++k) {
-    cand_v[(seg * TOPK + k) * 32 + lane] = tv[k];
-    cand_e[(seg * TOPK + k) * 32 + lane] = ti[k];
+    cand_v[(seg * TOPK + k) * TPO + lt] = tv[k];
+    cand_e[(seg * TOPK + k) * TPO + lt] = ti[k];
   }
   __syncthreads();
   if (seg == 0 && t < p.T) {
@@ -419,8 +426,8 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
     // expert) merged: each step takes the largest head, the lowest segment on equal
     // values -- the order of one strictly-greater insertion pass over all 256 experts
     int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
-    float h0 = cand_v[(0 * TOPK) * 32 + lane], h1 = cand_v[(1 * TOPK) * 32 + lane];
-    float h2 = cand_v[(2 * TOPK) * 32 + lane], h3 = cand_v[(3 * TOPK) * 32 + lane];
+    float h0 = cand_v[(0 * TOPK) * TPO + lt], h1 = cand_v[(1 * TOPK) * TPO + lt];
+    float h2 = cand_v[(2 * TOPK) * TPO + lt], h3 = cand_v[(3 * TOPK) * TPO + lt];
 #pragma unroll
     for (int k = 0; k < TOPK; ++k) {
       int bs = 0;
@@ -430,9 +437,9 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
       if (h3 > bv) { bv = h3; bs = 3; }
       const int pk = bs == 0 ? p0 : bs == 1 ? p1 : bs == 2 ? p2 : p3;
       tv[k] = bv;
-      ti[k] = cand_e[(bs * TOPK + pk) * 32 + lane];
+      ti[k] = cand_e[(bs * TOPK + pk) * TPO + lt];
       const int nx = pk + 1;
-      const float hn = nx < TOPK ? cand_v[(bs * TOPK + nx) * 32 + lane] : -INFINITY;
+      const float hn = nx < TOPK ? cand_v[(bs * TOPK + nx) * TPO + lt] : -INFINITY;
       if (bs == 0) { p0 = nx; h0 = hn; } else if (bs == 1) { p1 = nx; h1 = hn; } else if (bs == 2) { p2 = nx; h2 = hn; } else { p3 = nx; h3 = hn; }
     }
     // fewer than 8 ordered logits (NaN input): record it and route to expert 0 ..
@@ -454,7 +461,7 @@ __global__ void __cluster_dims__(1, RC_SPLIT, 1) __launch_bounds__(RC_THREADS, 1
     }
   }
   __syncthreads();
-  for (int i = tid; i < NEXP; i += RC_THREADS)
+  for (int i = tid; i < NEXP; i += NTH)
     if (hist_s[i] != 0) atomicAdd(p.hist + b * NEXP + i, hist_s[i]);
 }
 
@@ -747,7 +754,9 @@ cudaError_t launch_router_prefill(const CUtensorMap& tm_x, const CUtensorMap& tm
 cudaError_t launch_router_cluster(const CUtensorMap& tm_x, const CUtensorMap& tm_wr, const RouteParams& p,
                                   cudaStream_t s) {
   const int nblk = (p.T + RT_BM - 1) / RT_BM;
-  return launch_pdl(router_cluster_kernel, dim3(nblk, RC_SPLIT), RC_THREADS, RC_SMEM, s, tm_x, tm_wr, p);
+  if (p.T <= RC_MAX_T)
+    return launch_pdl(router_cluster_kernel<4>, dim3(nblk, 4), rc_threads(4), rc_smem(4), s, tm_x, tm_wr, p);
+  return launch_pdl(router_cluster_kernel<2>, dim3(nblk, 2), rc_threads(2), rc_smem(2), s, tm_x, tm_wr, p);
 }
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t s) {
@@ -760,7 +769,10 @@ cudaError_t launch_scatter(const ScatterParams& p, int nblk, cudaStream_t s) {
 
 cudaError_t set_router_attributes() {
   cudaError_t e = cudaFuncSetAttribute(router_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(router_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RC_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(router_cluster_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, rc_smem(4));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(router_cluster_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, rc_smem(2));
   return e;
 }
 
