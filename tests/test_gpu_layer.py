@@ -156,9 +156,10 @@ def test_exact_ties_lowest_index(oracle, lib, T):
 @pytest.mark.parametrize("T", [4095, 4096, 4097])
 def test_router_kernel_switch(oracle, lib, T):
     """Up to 4096 tokens the router runs as four-CTA clusters that split K and exchange
-    partial logits; above, one CTA per 128 tokens over the whole K.  Both sides of the
-    switch, with ragged last blocks: the routing of every token, the tables, and the output
-    of a sample that includes the last block."""
+    partial logits; above, as two-CTA clusters (up to 8192; beyond, one CTA per 128 tokens
+    over the whole K, covered by test_prefill_T8192 at T = 8200).  Both sides of the first
+    switch, with ragged last blocks: the routing of every token, the tables, and the
+    output of a sample that includes the last block."""
     L = synth.make_layer(13)
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=4100)
     x = synth.make_x(13, T)
@@ -174,7 +175,8 @@ def test_router_kernel_switch(oracle, lib, T):
 @pytest.mark.parametrize("T", [8192, 8200])
 def test_prefill_T8192(oracle, lib, T):
     """A larger prefill (about 256 rows per expert: full token blocks and a partial one for
-    most experts) and a ragged T: the routing of every token and the output of a sample
+    most experts) on both sides of the switch from the two-CTA cluster router (T = 8192)
+    to the whole-K one (T = 8200): the routing of every token and the output of a sample
     that includes the partial blocks of the fullest experts and the last tokens."""
     L = synth.make_layer(17)
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=8200)
@@ -192,19 +194,19 @@ def test_prefill_T8192(oracle, lib, T):
     print(f"T={T} near_ties={rep['near_ties']} flips={rep['flips']} max_err={err:.3e} scale={scale:.3e}")
 
 
-def test_exact_ties_whole_k_router(oracle, lib):
-    """Exact ties (zero router matrix) above 4096 tokens, where the router keeps one CTA
-    per 128 tokens: experts 0..7 with weight 1/8 for every token."""
+@pytest.mark.parametrize("T", [4100, 8200])
+def test_exact_ties_large_T(oracle, lib, T):
+    """Exact ties (zero router matrix) with the two-CTA cluster router (T = 4100) and the
+    whole-K router (T = 8200): experts 0..7 with weight 1/8 for every token."""
     L = synth.make_layer(11)
     L.router_w = np.zeros_like(L.router_w)
-    T = 4100
     layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=T)
     x = synth.make_x(11, T)
     out, r = run(layer, x)
     assert (r["idx"] == np.arange(8)[None, :]).all()
     assert (r["w"] == np.float32(0.125)).all()
     assert (r["counts"][:8] == T).all() and (r["counts"][8:256] == 0).all()
-    check_output(oracle, L, x, out, tokens=np.array([0, 1, 2047, 4095, 4096, 4099]))
+    check_output(oracle, L, x, out, tokens=np.array([0, 1, 2047, 4095, 4096, T - 1]))
 
 
 @pytest.mark.parametrize("T", [5, 40])
