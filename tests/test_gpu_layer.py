@@ -194,6 +194,27 @@ def test_prefill_T8192(oracle, lib, T):
     print(f"T={T} near_ties={rep['near_ties']} flips={rep['flips']} max_err={err:.3e} scale={scale:.3e}")
 
 
+def test_max_tokens(oracle, lib):
+    """The largest token count a layer accepts (65536): router blocks in several waves,
+    the scan's longest histogram walk, schedules near their capacity (about 68 gate/up and
+    270 down tiles per CTA).  The tables over every slot, the routing of a sample and the
+    output of a sample that includes the last tokens."""
+    T = 65536
+    L = synth.make_layer(19)
+    layer = lib.MoELayer(lib.DeviceWeights(L), max_tokens=T)
+    x = synth.make_x(19, T)
+    out, r = run(layer, x)
+    check_tables(r["idx"], r["counts"], r["offsets"], r["perm"])
+    rng = np.random.default_rng(T)
+    sub = np.unique(np.concatenate([rng.choice(T, 512, replace=False), np.arange(T - 8, T)]))
+    rep, alt = check_routing(oracle, L, x[sub], r["idx"][sub], r["w"][sub])
+    alt = {int(sub[i]): v for i, v in alt.items()}
+    # output tokens from the routing sample, so that a near-tie choice is known for each
+    tok = np.unique(np.concatenate([rng.choice(sub, 24, replace=False), np.arange(T - 4, T)]))
+    err, scale = check_output(oracle, L, x, out, tokens=tok, alt=alt)
+    print(f"T={T} near_ties={rep['near_ties']} flips={rep['flips']} max_err={err:.3e} scale={scale:.3e}")
+
+
 @pytest.mark.parametrize("T", [4100, 8200])
 def test_exact_ties_large_T(oracle, lib, T):
     """Exact ties (zero router matrix) with the two-CTA cluster router (T = 4100) and the
