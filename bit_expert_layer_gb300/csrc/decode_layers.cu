@@ -17,8 +17,10 @@
 //            computes its gate/up units: 8 features x (gate row, up row) of one active
 //            expert, an m16n8k16 tile whose two row halves are the gate and the up rows
 //            of the same features, so SwiGLU needs no exchange.  Two units per round, the
-//            16 warps splitting K; a fixed-order reduction gives h' = weight * silu(g) * u,
-//            published only for the tokens that chose the expert (h' is zero otherwise).
+//            16 warps splitting K; the 4-bit codes enter the MMAs as 128 + q and each
+//            quantisation group's scale and bias are applied to its partial sum in fp32;
+//            a fixed-order reduction gives h' = weight * silu(g) * u, published only for
+//            the tokens that chose the expert (h' is zero otherwise).
 //   phase C  16 output rows per CTA (128 CTAs): the weighted h' columns of every active
 //            expert, four experts per job, accumulate in one MMA accumulator per warp
 //            (four warps split the K of one expert: the combine over the 8 routed + 1
@@ -40,18 +42,18 @@
 // gate/up unit (8 KB of gate rows, 8 KB of up rows, their scales and biases) or the down
 // rows of four experts for the CTA's 16 output rows (4 KB each, with scales and biases).
 // The four copy warps queue the CTA's job list as soon as the routing is known -- its
-// gate/up units, then (once the first round of units has landed) its down rows -- each
-// into a slot the compute warps have released (full / empty mbarriers per slot), so the
-// weights stream while the compute warps work.  Copies are 16-byte cp.async (consecutive
-// threads on consecutive pieces of a contiguous block, which streams at the HBM rate,
-// where per-copy costs make small bulk-engine copies slow), counted on the slot's
-// mbarrier; one copy warp alone issues too slowly to keep up, four do.  The 16-byte chunks
-// of every weight row are stored XOR-swizzled by the row (chunk c of row r at c ^ (r & 7)),
-// so the MMA fragments' loads, eight rows at a time, hit distinct banks.  The copy warps
-// also fetch the next layer's router rows and norm weights.  The compute warps synchronise
-// on a named barrier of their own; the copy warps hand their registers to them
-// (setmaxnreg).  Every wait (tags, copies, slots) gives up after a time limit (error bit,
-// abort flags shared by the CTA's warps and by all CTAs).
+// gate/up units, then its down rows -- each into a slot the compute warps have released
+// (full / empty mbarriers per slot), so the weights stream while the compute warps work.
+// Copies are 16-byte cp.async (consecutive threads on consecutive pieces of a contiguous
+// block, which streams at the HBM rate, where per-copy costs make small bulk-engine
+// copies slow), counted on the slot's mbarrier; one copy warp alone issues too slowly to
+// keep up, four do.  The 16-byte chunks of every weight row are stored XOR-swizzled by the
+// row (chunk c of row r at c ^ (r & 7)), so the MMA fragments' loads, eight rows at a
+// time, hit distinct banks.  The copy warps also fetch the next layer's router rows and
+// norm weights.  The compute warps synchronise on a named barrier of their own; the copy
+// warps hand their registers to them (setmaxnreg).  Every wait (tags, copies, slots)
+// gives up after a time limit (error bit, abort flags shared by the CTA's warps and by all
+// CTAs).
 #include "common.cuh"
 #include "decode_tag.h"
 #include "gemm_common.cuh"
@@ -98,6 +100,7 @@ struct alignas(16) DlShared {
   float red[2][UNITS_PER_ROUND][DL_WARPS][32][4];   // K-split partials of a round (by round parity)
   __nv_bfloat16 rrow[2][HID];                   // this CTA's router rows
   __nv_bfloat16 normw[HID];                     // the layer's norm weights
+  float xg[DEC_MAX_T][HID / GROUP];             // sum of each token's xn over each quantisation group
   uint64_t mb_a;                                // router rows / norm weights of the layer landed
   uint64_t mb_full[NSLOT], mb_empty[NSLOT];     // weight slots: landed / released by the 16 compute warps
   uint64_t mb_route;                            // the layer's routing tables are built
@@ -149,6 +152,15 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ __nv_bfloat162 bf2h(uint16_t bits) {
   const uint32_t v = static_cast<uint32_t>(bits) * 0x00010001u;
   return *reinterpret_cast<const __nv_bfloat162*>(&v);
+}
+
+// The eight 4-bit codes of a packed word as bf16 pairs of 128 + q (exact), in the pair
+// order of the K-interleave (q0,q4), (q1,q5), (q2,q6), (q3,q7).  The affine map of the
+// codes is applied after the MMA, once per quantisation group and output element:
+// sum_k (s q_k + b) x_k = s * sum_k (128 + q_k) x_k + (b - 128 s) * sum_k x_k.
+__device__ __forceinline__ uint4 codes8(uint32_t w) {
+  return make_uint4((w & 0x000F000Fu) | 0x43004300u, ((w >> 4) & 0x000F000Fu) | 0x43004300u,
+                    ((w >> 8) & 0x000F000Fu) | 0x43004300u, ((w >> 12) & 0x000F000Fu) | 0x43004300u);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -358,16 +370,10 @@ __device__ void issue_job(const DecLayer& L, DlShared& s, const Jobs& J, int j) 
 // The copy warps' work for one layer: every job of this CTA in order, each into a slot the
 // compute warps have released, then the next layer's phase-A inputs.  False if a wait gave up.
 __device__ bool copy_layer(const DecLayersParams& p, int l, const Ctx& cx, DlShared& s, const Jobs& J) {
+  // The down rows follow the gate/up units at once (holding them back until the first
+  // round of units had landed measured 0.1-0.7 % slower at T = 1 and 8).
   for (int j = 0; j < J.n; ++j) {
     const uint32_t q = J.j0 + static_cast<uint32_t>(j);
-    const uint32_t q0 = J.j0 + static_cast<uint32_t>(min(J.nb, UNITS_PER_ROUND) - 1);
-    if (j == J.nb && J.nb > 0 && q0 + NSLOT >= J.j0 + static_cast<uint32_t>(J.nb)) {
-      // the down rows are needed only after every gate/up unit: let the first round of
-      // units land before their copies compete for the memory bandwidth (when the first
-      // round's last slot has been reused already, that round has long landed)
-      if (!copy_bar_and(mbar_wait(smem_u32(&s.mb_full[q0 % NSLOT]), (q0 / NSLOT) & 1, cx.err, &s.abort, cx.limit)))
-        return false;
-    }
     // the slot's previous job has been released (its first use needs no wait)
     if (!copy_bar_and(mbar_wait(smem_u32(&s.mb_empty[q % NSLOT]), ((q / NSLOT) & 1) ^ 1, cx.err, &s.abort,
                                 cx.limit)))
@@ -562,6 +568,24 @@ __device__ bool phase_a(const DecLayersParams& p, const DecLayer& L, int l, cons
     }
   }
   stamp(cx, 3);
+  // each token's xn summed over each quantisation group (zero for tokens past T), for the
+  // bias terms of phase B; the upper warps do it while the lower ones poll the logits (the
+  // barriers of the routing separate it from its readers)
+  static_assert(DEC_MAX_T * (HID / GROUP) <= DL_THREADS / 2, "one sum per thread of the upper half");
+  if (tid >= DL_THREADS - DEC_MAX_T * (HID / GROUP)) {
+    const int i = tid - (DL_THREADS - DEC_MAX_T * (HID / GROUP));
+    const int t = i / (HID / GROUP), gq = i % (HID / GROUP);
+    const uint4* src = reinterpret_cast<const uint4*>(&s.xn[t][gq * GROUP]);
+    float a = 0.0f;
+#pragma unroll
+    for (int j = 0; j < GROUP / 8; ++j) {
+      const uint4 v = src[j];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) a += bf16lo(u[k]) + bf16hi(u[k]);
+    }
+    s.xg[t][gq] = a;
+  }
   return true;
 }
 
@@ -682,25 +706,41 @@ __device__ bool phase_b_route(const DecLayersParams& p, const DecLayer& L, int l
   return true;
 }
 
-// Gate/up units, four per round (warp quarter wg = warp / 4 takes unit 4r + wg of the round,
-// its four warps split K into quarters of 512); the K partials are reduced in a fixed order
-// and h' = weight * silu(g) * u is published as tagged words.
+// Gate/up units, UNITS_PER_ROUND per round, the 16 warps splitting K (128 inputs, two
+// quantisation groups each); the K partials are reduced in a fixed order and
+// h' = weight * silu(g) * u is published as tagged words.
+//
+// Each MMA's K lies inside one quantisation group: lane quarter c4 feeds words 2 c4 and
+// 2 c4 + 1 of the warp's first group (eight inputs each, K-interleaved) to the first four
+// MMAs and words 8 + 2 c4, 9 + 2 c4 of its second group to the last four, as the codes
+// 128 + q; each group's accumulator is then scaled into the running sum with the group's
+// scale s and bias term (b - 128 s) * sum(x) of the output row (see codes8).
 __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int l, const Ctx& cx, DlShared& s,
                                const Jobs& J) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c4 = lane & 3;
   const int T = p.T, G = gridDim.x;
   const int kbase = warp * (HID / DL_WARPS);           // 128 inputs per warp
-  const int ch = kbase / 32 + c4;                      // this lane's 16-byte chunk of a row
-  const int gi = (kbase + 32 * c4) / GROUP;            // its quantisation group
+  const int gq0 = kbase / GROUP;                       // its first quantisation group (even)
+  // 16-byte chunk of a row holding words 2 c4, 2 c4 + 1, and their offset in it (the
+  // second group's pair sits two chunks on)
+  const int c0 = kbase / 32 + (c4 >> 1), o8 = (c4 & 1) * 8;
   unsigned long long* ht = p.ht + static_cast<size_t>(l & 1) * DEC_MAX_ACTIVE * DEC_MAX_T * (INTER / 2);
-  // B fragments (token g, this lane's 32 inputs), the same for every unit
+  // B fragments (token g; word slot k = word 2 c4 + k of the first group, 8 + 2 c4 + k - 2
+  // of the second), the same for every unit
   uint4 xb[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
+    const int wd = (k < 2 ? 0 : 6) + 2 * c4 + k;
     xb[k] = make_uint4(0, 0, 0, 0);
-    if (g < T) xb[k] = interleave8(*reinterpret_cast<const uint4*>(&s.xn[g][kbase + 32 * c4 + 8 * k]));
+    if (g < T) xb[k] = interleave8(*reinterpret_cast<const uint4*>(&s.xn[g][kbase + 8 * wd]));
   }
+  // group sums of x for this lane's output tokens 2 c4, 2 c4 + 1 (zero past T)
+  float xs[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) xs[q][i] = s.xg[2 * c4 + i][gq0 + q];
   const int nr = (J.nb + UNITS_PER_ROUND - 1) / UNITS_PER_ROUND;
   for (int r = 0; r < nr; ++r) {
     const int jlo = r * UNITS_PER_ROUND, jhi = min(J.nb, jlo + UNITS_PER_ROUND);
@@ -716,35 +756,56 @@ __device__ bool phase_b_gateup(const DecLayersParams& p, const DecLayer& L, int 
       if (!ok || jlo + u2 >= jhi) break;
       const bool two = jlo + u2 + 1 < jhi;                 // uniform
       uint32_t gw[2][4], uw[2][4];
-      __nv_bfloat162 mg[2], ag[2], mu[2], au[2];
+      uint32_t ms[2], mb[2], ns[2], nb[2];                 // [unit]: bf16 pairs of groups gq0, gq0 + 1
 #pragma unroll
       for (int v = 0; v < 2; ++v) {
         const uint8_t* U = s.ring[(J.j0 + jlo + u2 + (two ? v : 0)) % NSLOT];
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(U + U_SC);
-        const uint4 wgt = *reinterpret_cast<const uint4*>(U + g * U_ROWB + ((ch ^ g) << 4));
-        const uint4 wup = *reinterpret_cast<const uint4*>(U + (8 + g) * U_ROWB + ((ch ^ g) << 4));
-        gw[v][0] = wgt.x; gw[v][1] = wgt.y; gw[v][2] = wgt.z; gw[v][3] = wgt.w;
-        uw[v][0] = wup.x; uw[v][1] = wup.y; uw[v][2] = wup.z; uw[v][3] = wup.w;
-        mg[v] = bf2h(sc[g * 32 + gi]);
-        ag[v] = bf2h(sc[256 + g * 32 + gi]);
-        mu[v] = bf2h(sc[512 + g * 32 + gi]);
-        au[v] = bf2h(sc[768 + g * 32 + gi]);
+        const uint8_t* rg = U + g * U_ROWB;
+        const uint8_t* ru = U + (8 + g) * U_ROWB;
+        const uint2 g0 = *reinterpret_cast<const uint2*>(rg + ((c0 ^ g) << 4) + o8);
+        const uint2 g1 = *reinterpret_cast<const uint2*>(rg + (((c0 + 2) ^ g) << 4) + o8);
+        const uint2 u0 = *reinterpret_cast<const uint2*>(ru + ((c0 ^ g) << 4) + o8);
+        const uint2 u1 = *reinterpret_cast<const uint2*>(ru + (((c0 + 2) ^ g) << 4) + o8);
+        gw[v][0] = g0.x; gw[v][1] = g0.y; gw[v][2] = g1.x; gw[v][3] = g1.y;
+        uw[v][0] = u0.x; uw[v][1] = u0.y; uw[v][2] = u1.x; uw[v][3] = u1.y;
+        // scales and biases of rows g (gate) and g (up) for groups gq0, gq0 + 1 (adjacent)
+        ms[v] = *reinterpret_cast<const uint32_t*>(sc + g * 32 + gq0);
+        mb[v] = *reinterpret_cast<const uint32_t*>(sc + 256 + g * 32 + gq0);
+        ns[v] = *reinterpret_cast<const uint32_t*>(sc + 512 + g * 32 + gq0);
+        nb[v] = *reinterpret_cast<const uint32_t*>(sc + 768 + g * 32 + gq0);
       }
-      float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float t[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int q = 0; q < 2; ++q) {   // quantisation group gq0 + q: word slots 2q, 2q + 1
+        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int k = 2 * q; k < 2 * q + 2; ++k) {
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const uint4 o0 = codes8(gw[v][k]), o1 = codes8(uw[v][k]);
+            mma16816(d[v], o0.x, o1.x, o0.y, o1.y, xb[k].x, xb[k].y);
+            mma16816(d[v], o0.z, o1.z, o0.w, o1.w, xb[k].z, xb[k].w);
+          }
+        }
+        // d[v][0..1]: gate row g, tokens 2 c4 and 2 c4 + 1; d[v][2..3]: up row g
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
-          const uint4 o0 = dequant8(gw[v][k], mg[v], ag[v]), o1 = dequant8(uw[v][k], mu[v], au[v]);
-          mma16816(d[v], o0.x, o1.x, o0.y, o1.y, xb[k].x, xb[k].y);
-          mma16816(d[v], o0.z, o1.z, o0.w, o1.w, xb[k].z, xb[k].w);
+          const float sg = q ? bf16hi(ms[v]) : bf16lo(ms[v]), su = q ? bf16hi(ns[v]) : bf16lo(ns[v]);
+          const float bg = fmaf(-128.0f, sg, q ? bf16hi(mb[v]) : bf16lo(mb[v]));
+          const float bu = fmaf(-128.0f, su, q ? bf16hi(nb[v]) : bf16lo(nb[v]));
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            t[v][i] = fmaf(sg, d[v][i], fmaf(bg, xs[q][i], t[v][i]));
+            t[v][2 + i] = fmaf(su, d[v][2 + i], fmaf(bu, xs[q][i], t[v][2 + i]));
+          }
         }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) red[u2][warp][lane][k] = d[0][k];
+      for (int k = 0; k < 4; ++k) red[u2][warp][lane][k] = t[0][k];
       if (two) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) red[u2 + 1][warp][lane][k] = d[1][k];
+        for (int k = 0; k < 4; ++k) red[u2 + 1][warp][lane][k] = t[1][k];
       }
     }
     for (int jj = jlo; jj < jhi; ++jj) release_job(J, jj, s);
