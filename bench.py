@@ -62,6 +62,10 @@ WORKLOADS = {
     "layer-decode-T8": dict(layers=1, T_prefill=0, T_decode=8, skew=False),
     "layer-T512": dict(layers=1, T_prefill=512, T_decode=0, skew=False),
     "layer-T32": dict(layers=1, T_prefill=32, T_decode=0, skew=False),
+    "layer-T64": dict(layers=1, T_prefill=64, T_decode=0, skew=False),
+    "layer-T256": dict(layers=1, T_prefill=256, T_decode=0, skew=False),
+    "layer-T192": dict(layers=1, T_prefill=192, T_decode=0, skew=False),
+    "layer-T128": dict(layers=1, T_prefill=128, T_decode=0, skew=False),
     "decode-T1": dict(layers=40, T_prefill=0, T_decode=1, skew=False),
     "decode-T8": dict(layers=40, T_prefill=0, T_decode=8, skew=False),
     # grouped-query decode attention alone (the full-attention layers' decode step)

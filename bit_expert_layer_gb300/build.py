@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_layer.so")
 SOURCES = ["router.cu", "expert_gemm.cu", "down.cu", "decode.cu", "decode_layers.cu", "moe_layer.cu", "noalloc.cu",
-           "gqa.cu"]
+           "gqa.cu", "gemv_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fno-strict-aliasing",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

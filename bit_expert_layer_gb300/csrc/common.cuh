@@ -106,6 +106,9 @@ constexpr int GX_SMALL = 128;
 // the steps pays only while most blocks are small (measured: T = 32 and 512 faster, 4096
 // and 16384 slower)
 constexpr int DS_MAX_T = 1024;
+// prefill of at most this many tokens: the expert GEMMs run as mma.sync GEMVs
+// (gemv_small.cu), every expert block holding at most GV_MAX_T rows
+constexpr int GV_MAX_T = 192;
 constexpr int DS_NP = 8;
 constexpr int DS_NW = 3;
 constexpr int DS_NH = 3;

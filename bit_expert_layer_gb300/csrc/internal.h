@@ -232,6 +232,10 @@ unsigned long long wait_limit_ns();
 // Record the calling thread's failure description that moe_last_error_detail returns:
 // `what`, followed by the CUDA error's name when e is not cudaSuccess.
 void set_error_detail(const char* what, cudaError_t e);
+cudaError_t launch_gateup_gemv(const GateUpParams& p, const void* gq, const void* uq, const void* sgq,
+                               const void* suq, cudaStream_t s);
+cudaError_t launch_down_gemv(const DownParams& p, const __nv_bfloat16* h, const void* dq, const void* sdq,
+                             cudaStream_t s);
 cudaError_t launch_down_swap(const CUtensorMap& qd, const CUtensorMap& sqd, const CUtensorMap& hmap, const DownParams& p,
                              int grid, cudaStream_t s);
 cudaError_t set_down_attributes();

@@ -478,20 +478,32 @@ moe_status_t forward_impl(moe_layer* L, const void* x_orig, int T, void* out, in
                   U16(w.gate.scales), U16(w.gate.biases), U16(w.up.scales), U16(w.up.biases),
                   U16(w.sh_gate.scales), U16(w.sh_gate.biases), U16(w.sh_up.scales), U16(w.sh_up.biases),
                   L->h, T, L->err, pipe_trace() ? L->pipe : nullptr, L->x_ilv, L->row_dst, wait_limit_ns()};
-  const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
-  MOE_TRY(timed(K_GATEUP, s, L->err,
-                [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
-          "gate/up launch");
   DownParams dp{L->blocks, L->offsets, L->counts, U16(w.down.scales), U16(w.down.biases),
                 U16(w.sh_down.scales), U16(w.sh_down.biases), L->y, T, L->err,
                 pipe_trace() ? L->pipe + 16 : nullptr, wait_limit_ns()};
-  dp.small_apart = T <= DS_MAX_T ? 1 : 0;
-  MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }), "down launch");
-  if (dp.small_apart) {
-    // the small token blocks (at most one per expert), operands swapped
-    const int grid_ds = L->num_sms < (NEXP + 1) * DS_PAIRS ? L->num_sms : (NEXP + 1) * DS_PAIRS;
-    MOE_TRY(timed(K_DOWN_SWAP, s, L->err, [&] { return launch_down_swap(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_ds, s); }),
-            "down (small blocks) launch");
+  if (T <= GV_MAX_T) {
+    // a few rows per expert: weight-streaming GEMVs instead of 128-row tcgen05 tiles
+    MOE_TRY(timed(K_GATEUP, s, L->err,
+                  [&] { return launch_gateup_gemv(gp, w.gate.q, w.up.q, w.sh_gate.q, w.sh_up.q, s); }),
+            "gate/up launch");
+    MOE_TRY(timed(K_DOWN, s, L->err, [&] { return launch_down_gemv(dp, L->h, w.down.q, w.sh_down.q, s); }),
+            "down launch");
+  } else {
+    const int grid_gu = gemm_grid(T, GU_MBLK, L->num_sms), grid_dn = gemm_grid(T, DN_MBLK, L->num_sms);
+    MOE_TRY(timed(K_GATEUP, s, L->err,
+                  [&] { return launch_gateup(L->tm_qg, L->tm_qu, L->tm_sqg, L->tm_squ, L->tm_hs, gp, grid_gu, s); }),
+            "gate/up launch");
+    dp.small_apart = T <= DS_MAX_T ? 1 : 0;
+    MOE_TRY(timed(K_DOWN, s, L->err,
+                  [&] { return launch_down(L->tm_qd, L->tm_sqd, L->tm_h, L->tm_y, dp, grid_dn, s); }),
+            "down launch");
+    if (dp.small_apart) {
+      // the small token blocks (at most one per expert), operands swapped
+      const int grid_ds = L->num_sms < (NEXP + 1) * DS_PAIRS ? L->num_sms : (NEXP + 1) * DS_PAIRS;
+      MOE_TRY(timed(K_DOWN_SWAP, s, L->err,
+                    [&] { return launch_down_swap(L->tm_qd, L->tm_sqd, L->tm_h, dp, grid_ds, s); }),
+              "down (small blocks) launch");
+    }
   }
   MOE_TRY(timed(K_COMBINE, s, L->err,
                 [&] {
@@ -674,7 +686,7 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
 
 int moe_forward_launches(const moe_layer_t* L, int T) {
   if (!L || T < 1 || T > L->cfg.max_tokens) return 0;
-  return T <= DEC_MAX_T ? 1 : 6 + (T <= DS_MAX_T ? 1 : 0) + (L->w.norm_w ? 1 : 0);
+  return T <= DEC_MAX_T ? 1 : 6 + (T > GV_MAX_T && T <= DS_MAX_T ? 1 : 0) + (L->w.norm_w ? 1 : 0);
 }
 
 int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, int T) {

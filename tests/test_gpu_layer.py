@@ -80,8 +80,10 @@ def test_decode(oracle, host0, dev0, T):
     print(f"T={T} {rep} max_err={err:.3e} scale={scale:.3e}")
 
 
-@pytest.mark.parametrize("T", [2, 3, 7, 9, 31, 33, 127, 128, 129])
+@pytest.mark.parametrize("T", [2, 3, 7, 9, 31, 33, 63, 64, 65, 127, 128, 129, 191, 192, 193])
 def test_ragged_sweep(oracle, host0, dev0, T):
+    """Both sides of the token counts where the path changes: decode (T <= 8), the GEMV
+    expert kernels (T <= 192) and the tcgen05 ones."""
     x = synth.make_x(100 + T, T)
     full_check(oracle, host0, dev0, x)
 
@@ -116,13 +118,14 @@ def test_skewed_T4096(oracle, lib):
           f"max_err={err:.3e} scale={scale:.3e}")
 
 
-@pytest.mark.parametrize("T", [128, 129, 384, 385, 600, 1024, 1025])
+@pytest.mark.parametrize("T", [33, 64, 129, 192, 193, 384, 385, 600, 1024, 1025])
 def test_all_tokens_on_one_expert_set(oracle, lib, T):
     """Every token on the same 8 experts (and the shared one), so each of them holds T
-    rows: blocks of exactly 128 and 129 rows (the largest small block, run with the
-    operands swapped up to T = 1024, and the smallest big one), a full block plus such a
-    partial block, and T on both sides of the token count above which the small blocks
-    stay in the ordinary down GEMM."""
+    rows: in the GEMV kernels (T <= 192) blocks of more rows than one CTA's chunk of 32,
+    up to six chunks; in the tcgen05 kernels a big block of 193 rows, a full block plus
+    a partial block of 128 and 129 rows (the largest small block, run with the operands
+    swapped up to T = 1024, and the smallest big one), and T on both sides of the token
+    count above which the small blocks stay in the ordinary down GEMM."""
     L = synth.make_layer(7)
     chosen = [3, 17, 40, 77, 100, 150, 200, 255]
     bias = np.zeros(256, np.float32)
