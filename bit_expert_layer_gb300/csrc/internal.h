@@ -66,6 +66,9 @@ struct ScatterParams {
   int gather;              // 0: routing tables only (moe_route; or the previous stacked layer's
                            // combine already wrote x_ilv and the shared rows)
   unsigned int* err;
+  int fused;               // 1: no scan launch; the bases come from the histograms and one
+                           // extra CTA column writes the scan's tables (scan below)
+  ScanParams scan;
 };
 
 struct GateUpParams {

@@ -344,11 +344,15 @@ moe_status_t route_prefill(moe_layer* L, const void* x, int T, int gather, cudaS
                 }),
           "router launch");
   ScanParams sp{L->hist, nblk, T, L->base, L->counts, L->offsets, L->blocks};
-  MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
+  // up to SCAN_FUSE_NBLK router blocks the scatter derives its bases from the histograms
+  // itself and one extra CTA of it writes the scan's tables: one launch (and one
+  // dependent-launch wait) fewer
+  const int fused = nblk <= SCAN_FUSE_NBLK ? 1 : 0;
+  if (!fused) MOE_TRY(timed(K_SCAN, s, L->err, [&] { return launch_scan(sp, s); }), "scan launch");
   ScatterParams scp{L->topk_idx, L->topk_w, L->base, T, L->row_dst, L->slot_row, L->row_w,
                     static_cast<const __nv_bfloat16*>(x),
-                    static_cast<const __nv_bfloat16*>(L->w.shared_gate_w), L->x_ilv, gather, L->err};
-  MOE_TRY(timed(K_SCATTER, s, L->err, [&] { return launch_scatter(scp, nblk, s); }), "scatter launch");
+                    static_cast<const __nv_bfloat16*>(L->w.shared_gate_w), L->x_ilv, gather, L->err, fused, sp};
+  MOE_TRY(timed(K_SCATTER, s, L->err, [&] { return launch_scatter(scp, nblk + fused, s); }), "scatter launch");
   return MOE_OK;
 }
 
@@ -686,7 +690,9 @@ moe_status_t moe_stack_forward_host(moe_layer_t* const* layers, int n_layers, co
 
 int moe_forward_launches(const moe_layer_t* L, int T) {
   if (!L || T < 1 || T > L->cfg.max_tokens) return 0;
-  return T <= DEC_MAX_T ? 1 : 6 + (T > GV_MAX_T && T <= DS_MAX_T ? 1 : 0) + (L->w.norm_w ? 1 : 0);
+  return T <= DEC_MAX_T ? 1
+                        : 6 + (T > GV_MAX_T && T <= DS_MAX_T ? 1 : 0) + (L->w.norm_w ? 1 : 0) -
+                              ((T + RT_BM - 1) / RT_BM <= SCAN_FUSE_NBLK ? 1 : 0);
 }
 
 int moe_stack_forward_launches(const moe_layer_t* const* layers, int n_layers, int T) {

@@ -465,11 +465,13 @@ __global__ void __cluster_dims__(1, S, 1) __launch_bounds__(rc_threads(S), 1)
     if (hist_s[i] != 0) atomicAdd(p.hist + b * NEXP + i, hist_s[i]);
 }
 
-// 1024 threads: thread (q, e) = expert e's router blocks of quarter q (the per-expert
-// sums and prefixes over the blocks run four ways in parallel); the per-expert steps
-// below run on the q = 0 threads, every thread reaching the barriers.
-constexpr int SCAN_Q = 4;
-__global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p) {
+// The routing tables from the router's per-block histograms, on Q * 256 threads: thread
+// (q, e) = expert e's router blocks of part q (the per-expert sums and prefixes over the
+// blocks run Q ways in parallel); the per-expert steps below run on the q = 0 threads,
+// every thread reaching the barriers.  route_scan_kernel runs it on 1024 threads; a
+// short prefill runs it on one extra CTA of the scatter (256 threads).
+template <int SCAN_Q>
+__device__ __forceinline__ void scan_tables(const ScanParams& p) {
   __shared__ int sc[NEXP];      // inclusive scan of the experts' row counts
   __shared__ int sf[NEXP];      // inclusive scan of their numbers of full blocks
   __shared__ int s_wtot[2][NEXP / 32];
@@ -477,7 +479,6 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   __shared__ int s_part[NEXP + 1];   // each expert's partial block (the shared expert last)
   const int e = threadIdx.x % NEXP, q = threadIdx.x / NEXP, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool lead = q == 0;
-  grid_dep_wait();   // the histograms come from the router
   const int per_q = (p.nblk + SCAN_Q - 1) / SCAN_Q;
   const int b_lo = q * per_q, b_hi = min(p.nblk, b_lo + per_q);
   constexpr int CH = 8;    // histogram entries loaded together (independent loads in flight)
@@ -594,7 +595,8 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
     return r[0] + r[1] + r[2] + r[3] + (s_part[NEXP] > px);   // the shared expert sorts last among equals
   };
   if (lead && part > 0) blk[n_full + prank(e)] = e | (full << 9);
-  if (threadIdx.x == NEXP && s_part[NEXP] > 0) blk[n_full + prank(NEXP)] = NEXP | (full_sh << 9);
+  // the shared expert's partial block: thread 256 (a q = 1 thread), or thread 0 after its own
+  if (threadIdx.x == (SCAN_Q > 1 ? NEXP : 0) && s_part[NEXP] > 0) blk[n_full + prank(NEXP)] = NEXP | (full_sh << 9);
   const int np = __syncthreads_count(lead && part > 0) + (s_part[NEXP] > 0);
   // the big blocks (more than GX_SMALL rows): every full block and the partial blocks
   // above GX_SMALL rows, which the order puts right after them
@@ -608,12 +610,49 @@ __global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p)
   }
 }
 
+constexpr int SCAN_Q = 4;
+__global__ void __launch_bounds__(SCAN_Q * NEXP) route_scan_kernel(ScanParams p) {
+  grid_dep_wait();   // the histograms come from the router
+  scan_tables<SCAN_Q>(p);
+}
+
+// Expert e's (= this thread's) first permuted row in router block b, straight from the
+// histograms: the exclusive scan of the experts' totals plus e's rows in the earlier
+// blocks (the same integers route_scan_kernel writes to base).  Every thread of the CTA
+// (256) calls it.
+__device__ __forceinline__ int fused_base(const int* hist, int nblk, int b) {
+  __shared__ int s_w[NEXP / 32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int tot = 0, pre = 0;
+  for (int bb = 0; bb < nblk; ++bb) {
+    const int h = __ldg(hist + bb * NEXP + e);
+    tot += h;
+    pre += bb < b ? h : 0;
+  }
+  int inc = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) s_w[warp] = inc;
+  __syncthreads();
+  int add = 0;
+  for (int w = 0; w < warp; ++w) add += s_w[w];
+  return add + inc - tot + pre;
+}
+
 __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams p) {
   constexpr int SLOTS = RT_BM * TOPK;   // 1024 slots per router block
   __shared__ int wh[8][NEXP];
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slot0 = b * SLOTS;
   grid_dep_wait();   // the routing and the bases come from the kernels before this one
+  if (p.fused && b == p.scan.nblk) {   // the extra CTA column of a short prefill: the scan's tables
+    static_assert(SC_THREADS == NEXP, "the scan's tables on one thread per expert");
+    if (blockIdx.y == 0) scan_tables<1>(p.scan);
+    return;
+  }
+  const int slot0 = b * SLOTS;
   const int nslots = min(SLOTS, p.T * TOPK - slot0);
   const int n8 = 8 * p.T;
   if (blockIdx.y == 0) {
@@ -627,7 +666,7 @@ __global__ void __launch_bounds__(SC_THREADS) route_scatter_kernel(ScatterParams
     ev[j] = (sl < nslots) ? __ldg(p.topk_idx + slot0 + sl) : -1;
     wv[j] = (sl < nslots) ? __ldg(p.topk_w + slot0 + sl) : 0.0f;
   }
-  const int base_e = __ldg(p.base + b * NEXP + tid);
+  const int base_e = p.fused ? fused_base(p.scan.hist, p.scan.nblk, b) : __ldg(p.base + b * NEXP + tid);
   for (int i = tid; i < 8 * NEXP; i += SC_THREADS) (&wh[0][0])[i] = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
