@@ -8,15 +8,16 @@
 // columns at a time, so the weights are dequantised in registers and streamed through
 // the MMAs once per group of eight tokens.
 //
-// gateup_gemv_kernel: one CTA per (token block, 64 h columns), one warp per 8 columns:
+// gateup_gemv_kernel: one CTA per (token block, chunk of 32 of its rows, 64 h columns),
+// one warp per 8 columns:
 // the warp's A rows 0-7 are the gate rows and 8-15 the up rows of the features whose
 // K-interleaved h columns are pos0 .. pos0 + 7, so that the accumulator pairs gate and up
 // of the same feature (SwiGLU needs no exchange).  Lane quarter c4 takes words 2 c4 and
 // 2 c4 + 1 of each quantisation group (eight inputs each); the B fragments are the same
 // words of the K-interleaved activation rows.  down_gemv_kernel: one CTA per (token
-// block, 128 output rows), one warp per 16 rows, B = the h rows of the block.
+// block, chunk of 32 rows, 128 output rows), one warp per 16 rows, B = the h rows.
 //
-// Both read every weight word once per pass of up to 8 rows (one pass unless an expert
+// Both read every weight word once per pass of up to 8 rows (one pass unless the chunk
 // holds more rows), with the next words of a warp in flight while it computes; the pass's
 // activation (or h) rows are staged in shared memory first.  The dequantised weight is
 // bf16(scale * q + bias), one rounding, as in the tcgen05 kernels.  No waits beyond the
