@@ -128,7 +128,7 @@ constexpr int DN_MBLK = HID / GX_BM;                // 16 row blocks
 // places the slots, all of them copy their share of the tokens
 constexpr int SC_THREADS = 256;
 constexpr int SC_SPLIT = 4;
-constexpr int SCAN_FUSE_NBLK = 16;   // router blocks (T <= 2048) up to which the scatter does the scan's work
+constexpr int SCAN_FUSE_NBLK = 128;  // router blocks (T <= 16384) up to which the scatter does the scan's work
 
 // decode path (T <= 8)
 constexpr int DEC_MAX_T = 8;
