@@ -10,15 +10,21 @@
 //                          weights exp(l_k - l_1) / sum (equal to softmax over all 256
 //                          followed by renormalisation over the 8), and a per-CTA
 //                          expert histogram.
+//   router_cluster_kernel  the same up to 8192 tokens with each 128-token block's K
+//                          split over a cluster of 2 or 4 CTAs (partials through
+//                          distributed shared memory).
 //   route_scan_kernel      per-expert counts, exclusive-scan offsets, the first
 //                          permuted row of every (router block, expert), and the
-//                          ordered token blocks that both grouped GEMMs deal as tiles.
+//                          ordered token blocks that both grouped GEMMs deal as tiles
+//                          (above 16384 tokens; up to that the scatter does this work).
 //   route_scatter_kernel   stable permutation of the slots t*8+k into expert order and
 //                          the per-row weight (first CTA of each router block), one
 //                          K-interleaved copy of x per token (the gate/up GEMM gathers
 //                          its rows from it by token) and, on the same read of x, the
 //                          shared-expert gate sigmoid(g_s . x) (in a stack, the previous
-//                          layer's combine writes these two instead).
+//                          layer's combine writes these two instead); up to 16384
+//                          tokens also the scan's tables (one extra CTA) and the first
+//                          rows straight from the histograms.
 #include "common.cuh"
 #include "internal.h"
 
